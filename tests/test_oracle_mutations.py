@@ -1,0 +1,100 @@
+"""The oracle pins must catch plausible mistakes.
+
+Each case plants one slip in a copy of the oracle's update (on the CPU, by
+monkeypatching) and checks that the pins above reject it.
+"""
+import numpy as np
+import pytest
+
+import oracle.gdn as gdn_mod
+import oracle.mamba2 as m2_mod
+from tests import test_oracle_gdn as gdn_pins
+from tests import test_oracle_mamba2 as m2_pins
+
+
+def _m2_mutants():
+    def decay_after_input(self, h, dt, x, B, C):
+        dt = np.asarray(dt, np.float64); x = np.asarray(x, np.float64)
+        Bh = np.asarray(B, np.float64)[:, self.g]; Ch = np.asarray(C, np.float64)[:, self.g]
+        a = np.exp(dt * self.A[None])
+        h = a[:, :, None, None] * (h + (dt[:, :, None] * x)[..., None] * Bh[:, :, None, :])
+        return h, np.einsum("bhpn,bhn->bhp", h, Ch) + self.D[None, :, None] * x
+
+    def dropped_dt_on_input(self, h, dt, x, B, C):
+        dt = np.asarray(dt, np.float64); x = np.asarray(x, np.float64)
+        Bh = np.asarray(B, np.float64)[:, self.g]; Ch = np.asarray(C, np.float64)[:, self.g]
+        a = np.exp(dt * self.A[None])
+        h = a[:, :, None, None] * h + x[..., None] * Bh[:, :, None, :]
+        return h, np.einsum("bhpn,bhn->bhp", h, Ch) + self.D[None, :, None] * x
+
+    def swapped_B_C(self, h, dt, x, B, C):
+        return m2_mod.Mamba2Stepwise._orig(self, h, dt, x, C, B)
+
+    def wrong_group(self, h, dt, x, B, C):
+        g = self.g
+        self.g = np.arange(len(g)) % B.shape[1]
+        try:
+            return m2_mod.Mamba2Stepwise._orig(self, h, dt, x, B, C)
+        finally:
+            self.g = g
+
+    def no_skip_term(self, h, dt, x, B, C):
+        h, y = m2_mod.Mamba2Stepwise._orig(self, h, dt, x, B, C)
+        return h, y - self.D[None, :, None] * np.asarray(x, np.float64)
+
+    def output_before_update(self, h, dt, x, B, C):
+        Ch = np.asarray(C, np.float64)[:, self.g]
+        y = np.einsum("bhpn,bhn->bhp", h, Ch) + self.D[None, :, None] * np.asarray(x, np.float64)
+        h, _ = m2_mod.Mamba2Stepwise._orig(self, h, dt, x, B, C)
+        return h, y
+
+    return [decay_after_input, dropped_dt_on_input, swapped_B_C, wrong_group,
+            no_skip_term, output_before_update]
+
+
+def _run_pins(module):
+    failed = 0
+    for name in dir(module):
+        if name.startswith("test_"):
+            try:
+                getattr(module, name)()
+            except AssertionError:
+                failed += 1
+    return failed
+
+
+@pytest.mark.parametrize("mutant", _m2_mutants(), ids=lambda f: f.__name__)
+def test_mamba2_pins_catch(monkeypatch, mutant):
+    m2_mod.Mamba2Stepwise._orig = m2_mod.Mamba2Stepwise._update
+    monkeypatch.setattr(m2_mod.Mamba2Stepwise, "_update", mutant)
+    assert _run_pins(m2_pins) > 0
+
+
+def _gdn_mutants():
+    def sign_flip(self, S, q, k, v, alpha, beta):
+        return gdn_mod.GDNStepwise._orig(self, S, q, k, -np.asarray(v), alpha, beta)
+
+    def decay_outside(self, S, q, k, v, alpha, beta):
+        q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+        a = np.asarray(alpha, np.float64)[:, :, None, None]; bt = np.asarray(beta, np.float64)[:, :, None, None]
+        Sk = np.einsum("bhvk,bhk->bhv", S, k)
+        S = a * (S - bt * Sk[..., None] * k[:, :, None, :] + bt * v[..., None] * k[:, :, None, :])
+        return S, np.einsum("bhvk,bhk->bhv", S, q)
+
+    def transposed_outer(self, S, q, k, v, alpha, beta):
+        q = np.asarray(q, np.float64); k = np.asarray(k, np.float64); v = np.asarray(v, np.float64)
+        a = np.asarray(alpha, np.float64)[:, :, None, None]; bt = np.asarray(beta, np.float64)[:, :, None, None]
+        kS = np.einsum("bhvk,bhv->bhk", S, k[..., :S.shape[2]]) if S.shape[2] == S.shape[3] else None
+        if kS is None:
+            raise AssertionError("shape")
+        S = a * (S - bt * k[..., None] * kS[:, :, None, :]) + bt * v[..., None] * k[:, :, None, :]
+        return S, np.einsum("bhvk,bhk->bhv", S, q)
+
+    return [sign_flip, decay_outside, transposed_outer]
+
+
+@pytest.mark.parametrize("mutant", _gdn_mutants(), ids=lambda f: f.__name__)
+def test_gdn_pins_catch(monkeypatch, mutant):
+    gdn_mod.GDNStepwise._orig = gdn_mod.GDNStepwise._update
+    monkeypatch.setattr(gdn_mod.GDNStepwise, "_update", mutant)
+    assert _run_pins(gdn_pins) > 0

@@ -1,0 +1,275 @@
+/*
+ * replayssm.h -- C ABI of the ReplaySSM decode-state library (libreplayssm.so).
+ *
+ * The method (three web pages: AT Pulse, "NVIDIA and Princeton's ReplaySSM
+ * stores a checkpoint and recent inputs instead of full SSM state to speed up
+ * hybrid-model decoding"; The Clarity, "NVIDIA and Princeton cache SSM inputs
+ * in place of state to speed hybrid-model decoding"; WittyWires, "ReplaySSM
+ * cuts memory traffic to speed up hybrid-model decoding") keeps each
+ * sequence's SSM state as a high-precision checkpoint plus a buffer of at most
+ * L per-token input records.  Normal decode steps compute the output from the
+ * checkpoint and the buffer and write only the new record; every L steps a
+ * flush folds the buffer into the checkpoint (AT Pulse §What happened,
+ * §Technical analysis "core idea"; Clarity claim ledger [17], [18], [22]).
+ * Speculative verify scores draft tokens from the same data and rollback is a
+ * buffer-pointer move (AT Pulse §Technical analysis "speculative decoding").
+ * A low-precision copy of the checkpoint may serve the reads while the FP32
+ * checkpoint drives the recurrence (AT Pulse §Technical analysis
+ * "quantization").  The conventional in-place decode, which loads and stores
+ * the whole state every step (Clarity claim ledger [6], [7]), and the
+ * conventional snapshot-per-draft verify (Clarity claim ledger [13]) are kept
+ * as comparison paths.
+ *
+ * Conventions for every entry point:
+ *  - Every pointer is a DEVICE pointer unless said otherwise; every buffer is
+ *    allocated and owned by the caller, dense (C order, the layouts below) and
+ *    16-byte aligned.  The library allocates nothing and keeps no state.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    stream-ordered and asynchronous: it validates its arguments on the host,
+ *    enqueues one kernel, and returns without synchronising.
+ *  - Host-detectable errors (NULL or misaligned pointers, unsupported shapes,
+ *    T out of range) return a status before anything is enqueued.  A failed
+ *    launch returns RSSM_ERR_CUDA.  Metadata that only the device can see to
+ *    be bad (a ring pointer out of range, an accepted count above T) makes the
+ *    kernel leave that sequence untouched and OR an RSSM_DEVERR_* bit into
+ *    *err.  Kernels never trap; the only thing a kernel ever waits for is its
+ *    own asynchronous copies, and those waits give up after ~2 s
+ *    (RSSM_DEVERR_TIMEOUT).
+ *  - Calls that touch the same cache must be ordered on one stream (the
+ *    per-sequence arrival counters below are shared by every call).
+ *
+ * Mamba-2 notation (per sequence b, head h, group g(h) = h / (nheads/ngroups)):
+ *   state h_c[h][p][n] (p < headdim, n < dstate); token inputs dt[h] > 0,
+ *   x[h][p], B[g][n], C[g][n]; parameters A[h] < 0, D[h].  One stepwise update
+ *   is h <- exp(dt*A) h + dt x B^T, y = h C + D x.  With the checkpoint h_c
+ *   taken before records j = 1..k (k = the current token) and S_j the running
+ *   sum of dt, the replay output is
+ *     y = exp(A S_k) (h_c C) + sum_j exp(A (S_k - S_j)) dt_j (B_j . C) x_j + D x.
+ */
+#ifndef REPLAYSSM_H
+#define REPLAYSSM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RSSM_OK = 0,
+    RSSM_ERR_NULL = 1,        /* a required pointer is NULL */
+    RSSM_ERR_ALIGN = 2,       /* a pointer is not 16-byte aligned */
+    RSSM_ERR_SHAPE = 3,       /* a size is out of the supported range */
+    RSSM_ERR_RING = 4,        /* T outside [1, min(L, 8)] */
+    RSSM_ERR_CUDA = 5,        /* the kernel launch failed (cudaGetLastError) */
+    RSSM_ERR_UNSUPPORTED = 6  /* a supported-but-not-built combination */
+} rssm_status;
+
+/* Bits that kernels OR into the caller's *err word. */
+#define RSSM_DEVERR_RING_META 0x1u /* ring_head/ring_len out of range: sequence skipped */
+#define RSSM_DEVERR_ROLLBACK  0x2u /* accepted outside [0,T] or ring_len < T - accepted */
+#define RSSM_DEVERR_SLOT      0x4u /* snapshot slot index outside [0, T] */
+#define RSSM_DEVERR_TIMEOUT   0x8u /* an asynchronous tile copy did not complete within ~2 s;
+                                      the kernel abandoned the rest of its work and the
+                                      cache (and its arrival counters) must be reset */
+
+/* ------------------------------------------------------------------------ */
+/* Mamba-2                                                                    */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int32_t batch;      /* sequences, 1..65535 */
+    int32_t nheads;     /* H, multiple of ngroups */
+    int32_t headdim;    /* P, multiple of 8, <= 256; headdim * dstate a multiple of 256 */
+    int32_t dstate;     /* N, one of 16, 32, 64, 128 */
+    int32_t ngroups;    /* G */
+    int32_t L;          /* ring capacity = flush threshold, 1..32 */
+    int32_t read_copy;  /* 0: reads use the FP32 checkpoint; 1: FP8 E4M3 read copy */
+    int32_t io_bf16;    /* 1: x, B, C and their records are bf16; 0: float32 */
+} rssm_mamba2_dims;
+
+typedef struct {
+    float    *ckpt;       /* [batch][nheads][headdim][dstate] FP32 checkpoint h_c */
+    uint8_t  *ckpt_q;     /* [batch][nheads][headdim][dstate] E4M3 codes (read_copy = 1) */
+    float    *ckpt_scale; /* [batch][nheads][headdim] one scale per row (read_copy = 1) */
+    float    *rec_dt;     /* [batch][nheads][L] */
+    void     *rec_x;      /* [batch][nheads][L][headdim], bf16 or float32 per io_bf16 */
+    void     *rec_B;      /* [batch][ngroups][L][dstate] */
+    void     *rec_C;      /* [batch][ngroups][L][dstate]; NULL = C is not kept */
+    int32_t  *ring_head;  /* [batch] ring slot of the oldest buffered record, [0, L) */
+    int32_t  *ring_len;   /* [batch] buffered records, [0, L] */
+    int32_t  *arrive;     /* [batch] scratch counters: zero before the first call,
+                             every call leaves them zero again */
+    const float *A;       /* [nheads] */
+    const float *D;       /* [nheads] */
+    uint32_t *err;        /* one word; RSSM_DEVERR_* bits are ORed in */
+} rssm_mamba2_cache;
+
+/*
+ * Replay decode of one token per sequence (AT Pulse §What happened: normal
+ * steps compute each output from the checkpoint plus the buffered records and
+ * write only the new record; Clarity claim ledger [18]).
+ *   dt [batch][nheads] f32; x [batch][nheads][headdim]; B, C
+ *   [batch][ngroups][dstate] (bf16 or f32 per io_bf16); y [batch][nheads][headdim] f32.
+ * With len = ring_len[b] records buffered:
+ *   len + 1 <  L: append (dt, x, B, C) at slot (ring_head + len) mod L,
+ *                 ring_len += 1; the checkpoint is only read.
+ *   len + 1 >= L: flush fused into this step (AT Pulse §Technical analysis:
+ *                 every L steps the buffer is folded into the checkpoint):
+ *                 h_c <- exp(A S) h_c + sum_j exp(A (S - S_j)) dt_j x_j B_j^T
+ *                 over the buffered records and the current token, the read
+ *                 copy is re-quantised, ring_head <- (ring_head + len + 1) mod L,
+ *                 ring_len <- 0; the current token is not stored.
+ * y is the replay output above in every case.  Non-flush steps read the FP8
+ * copy when dims->read_copy = 1.
+ */
+rssm_status replayssm_decode(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
+                             const float *dt, const void *x, const void *B, const void *C,
+                             float *y, void *stream);
+
+/*
+ * Standalone flush (WittyWires §What happened: the checkpoint is updated when
+ * the buffer fills): for every sequence with mask[b] != 0 (mask = NULL: all),
+ * fold its ring_len records into the checkpoint with the same arithmetic as
+ * the fused flush, re-quantise the read copy, ring_head <- (ring_head +
+ * ring_len) mod L, ring_len <- 0.  mask is a device array of batch bytes.
+ */
+rssm_status replayssm_flush(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
+                            const uint8_t *mask, void *stream);
+
+/*
+ * Speculative verify of T drafts per sequence by output-only evaluation
+ * (AT Pulse §Technical analysis "speculative decoding": no intermediate state
+ * is built).  dt [batch][T][nheads]; x [batch][T][nheads][headdim]; B, C
+ * [batch][T][ngroups][dstate]; y [batch][T][nheads][headdim] f32.
+ * If ring_len + T > L the buffered records are folded first (as
+ * replayssm_flush).  Draft i (1-based) is scored against the checkpoint, the
+ * buffered records and drafts 1..i; the T drafts are appended at slots
+ * (ring_head + ring_len + i - 1) mod L and ring_len += T.  Drafts are never
+ * folded by a verify.  1 <= T <= min(L, 8).  Reads use the FP32 checkpoint.
+ */
+rssm_status replayssm_verify(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
+                             int32_t T, const float *dt, const void *x, const void *B,
+                             const void *C, float *y, void *stream);
+
+/*
+ * Rollback after a verify of T drafts (AT Pulse §Technical analysis: rolling
+ * back rejected drafts is a buffer-pointer move): ring_len[b] -= T -
+ * accepted[b].  accepted [batch] int32 in [0, T]; a sequence with an accepted
+ * count outside that range, or fewer than T - accepted records, is left as it
+ * is and RSSM_DEVERR_ROLLBACK is raised.  No state or record bytes move.
+ */
+rssm_status replayssm_rollback(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
+                               int32_t T, const int32_t *accepted, void *stream);
+
+/*
+ * (Re)build the FP8 read copy from the FP32 checkpoint for every sequence:
+ * per (head, row) amax = max|h|, scale = amax/448, code = E4M3 round-to-
+ * nearest-even, saturating, of h * (448/amax); a zero row gets scale 1 and
+ * zero codes (AT Pulse §Technical analysis "quantization").  Used once after
+ * the checkpoint is initialised; flushes keep the copy current afterwards.
+ */
+rssm_status replayssm_requant(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
+                              void *stream);
+
+/*
+ * Conventional in-place decode (Clarity claim ledger [6]: each step updates
+ * the state, reads the output from it and stores it): state
+ * [batch][nheads][headdim][dstate] f32 is loaded, updated
+ * h <- exp(dt A) h + dt x B^T, contracted y = h C + D x, and stored back.
+ * Inputs as replayssm_decode.  dims->L and read_copy are ignored.
+ */
+rssm_status replayssm_conventional_decode(const rssm_mamba2_dims *dims, float *state,
+                                          const float *A, const float *D, const float *dt,
+                                          const void *x, const void *B, const void *C,
+                                          float *y, void *stream);
+
+/*
+ * Conventional speculative verify with a snapshot per draft (Clarity claim
+ * ledger [13]: one state read and T state writes per step).  pool is
+ * [batch][T+1][nheads][headdim][dstate] f32; slot [batch] int32 names the
+ * pool entry holding the current state.  The T drafts are applied stepwise;
+ * the state after draft i is stored in entry (slot + i) mod (T + 1) and y of
+ * draft i is read from it.  Inputs/outputs as replayssm_verify.  A slot
+ * outside [0, T] raises RSSM_DEVERR_SLOT and the sequence is skipped.
+ */
+rssm_status replayssm_conventional_verify(const rssm_mamba2_dims *dims, float *pool,
+                                          const int32_t *slot, int32_t T, const float *A,
+                                          const float *D, const float *dt, const void *x,
+                                          const void *B, const void *C, float *y,
+                                          uint32_t *err, void *stream);
+
+/*
+ * Conventional rollback: slot[b] <- (slot[b] + accepted[b]) mod (T + 1), i.e.
+ * keep the snapshot after the accepted prefix (0 = the state before the
+ * drafts).  An accepted count outside [0, T] raises RSSM_DEVERR_ROLLBACK.
+ */
+rssm_status replayssm_conventional_select(int32_t batch, int32_t *slot, int32_t T,
+                                          const int32_t *accepted, uint32_t *err, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Gated DeltaNet (gated delta rule)                                          */
+/* ------------------------------------------------------------------------ */
+/*
+ * Per sequence and head: state S[dv][dk]; token (q, k in R^dk, v in R^dv,
+ * alpha, beta scalars):  S <- alpha S (I - beta k k^T) + beta v k^T,  o = S q
+ * (AT Pulse §Capabilities and access: Gated DeltaNet kernels; the replay idea
+ * of §Technical analysis applied to the gated delta rule).  Replay form with
+ * checkpoint S_c and records j = 1..k (k = current): u_k = q,
+ * u_{j-1} = alpha_j (u_j - beta_j k_j (k_j . u_j)),
+ * o = S_c u_0 + sum_j beta_j (k_j . u_j) v_j.
+ */
+typedef struct {
+    int32_t batch;
+    int32_t nheads;
+    int32_t dk;    /* one of 16, 32, 64, 128 */
+    int32_t dv;    /* multiple of 8, <= 256; dk * dv a multiple of 256 */
+    int32_t L;     /* 1..32 */
+} rssm_gdn_dims;
+
+typedef struct {
+    float    *ckpt;       /* [batch][nheads][dv][dk] FP32 checkpoint S_c */
+    uint16_t *rec_k;      /* [batch][nheads][L][dk] bf16 */
+    uint16_t *rec_v;      /* [batch][nheads][L][dv] bf16 */
+    float    *rec_alpha;  /* [batch][nheads][L] */
+    float    *rec_beta;   /* [batch][nheads][L] */
+    int32_t  *ring_head;  /* [batch] */
+    int32_t  *ring_len;   /* [batch] */
+    int32_t  *arrive;     /* [batch] scratch counters, zero before the first call */
+    uint32_t *err;
+} rssm_gdn_cache;
+
+/*
+ * GDN replay decode, same ring rules as replayssm_decode (fused flush when
+ * ring_len + 1 >= L folds the records and the current token row by row:
+ * s <- alpha_j (s - beta_j (s . k_j) k_j) + beta_j v_j[r] k_j).
+ * q, k [batch][nheads][dk] bf16; v [batch][nheads][dv] bf16; alpha, beta
+ * [batch][nheads] f32; o [batch][nheads][dv] f32.
+ */
+rssm_status replayssm_gdn_decode(const rssm_gdn_dims *dims, const rssm_gdn_cache *cache,
+                                 const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                 const float *alpha, const float *beta, float *o, void *stream);
+
+/* GDN standalone flush of the masked sequences (mask NULL = all). */
+rssm_status replayssm_gdn_flush(const rssm_gdn_dims *dims, const rssm_gdn_cache *cache,
+                                const uint8_t *mask, void *stream);
+
+/* GDN conventional in-place decode of state [batch][nheads][dv][dk] f32. */
+rssm_status replayssm_gdn_conventional_decode(const rssm_gdn_dims *dims, float *state,
+                                              const uint16_t *q, const uint16_t *k,
+                                              const uint16_t *v, const float *alpha,
+                                              const float *beta, float *o, void *stream);
+
+/* ------------------------------------------------------------------------ */
+
+/* Static string for a status code (host). */
+const char *replayssm_status_string(rssm_status s);
+
+/* Library ABI version: 0x00MMmmpp. */
+uint32_t replayssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REPLAYSSM_H */

@@ -1,0 +1,98 @@
+"""Algorithmic HBM bytes of each decode path, per sequence and step.
+
+Only the bytes the method must move are counted: the checkpoint (or its read
+copy) read once, written only when folded; the token inputs read once; the
+output written once; the new record written once; each buffered record read
+once.  The pages' size arithmetic is the unit check of this model: a 4 MiB
+FP32 state per sequence and layer equals the KV cache of 8,192 tokens at
+0.5 KiB per token; with five SSM layers per attention layer that is 40,960
+tokens, and a load plus a store every step 81,920 (Clarity, key figures and
+claim ledger [10], [11], [19]-[21]).  Replay keeps the checkpoint reads and
+drops most of the writes, which roughly halves the state traffic (AT Pulse
+§What happened).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+
+@dataclass(frozen=True)
+class Mamba2Units:
+    S: int    # FP32 checkpoint
+    Sq: int   # FP8 read copy: codes + one float32 scale per row
+    I: int    # one token's inputs: dt, x, B, C
+    Y: int    # one token's output y (float32)
+    Rw: int   # one record written: dt, x, B, C
+    Rr: int   # one buffered record read: dt, x, B (C is never read back)
+
+
+def mamba2_units(nheads, headdim, dstate, ngroups, io_bytes=2, keep_C=True) -> Mamba2Units:
+    H, P, N, G = nheads, headdim, dstate, ngroups
+    S = H * P * N * 4
+    Sq = H * P * N + H * P * 4
+    I = H * 4 + H * P * io_bytes + 2 * G * N * io_bytes
+    Y = H * P * 4
+    Rw = H * 4 + H * P * io_bytes + (2 if keep_C else 1) * G * N * io_bytes
+    Rr = H * 4 + H * P * io_bytes + G * N * io_bytes
+    return Mamba2Units(S, Sq, I, Y, Rw, Rr)
+
+
+def mamba2_conventional(u: Mamba2Units) -> int:
+    return 2 * u.S + u.I + u.Y
+
+
+def mamba2_replay_decode(u: Mamba2Units, len_before: int, L: int, read_copy: bool = False) -> int:
+    """One replay decode step of a sequence holding ``len_before`` records."""
+    fold = len_before + 1 >= L
+    b = u.I + u.Y + len_before * u.Rr
+    if fold:
+        b += 2 * u.S + (u.Sq if read_copy else 0)
+    else:
+        b += (u.Sq if read_copy else u.S) + u.Rw
+    return b
+
+
+def mamba2_replay_period(u: Mamba2Units, L: int, read_copy: bool = False) -> float:
+    """Mean over one flush period of L steps from an empty ring."""
+    return sum(mamba2_replay_decode(u, k, L, read_copy) for k in range(L)) / L
+
+
+def mamba2_verify(u: Mamba2Units, len_before: int, T: int, L: int) -> int:
+    pre = len_before + T > L
+    return u.S + (u.S if pre else 0) + T * (u.I + u.Y + u.Rw) + len_before * u.Rr
+
+
+def mamba2_conventional_verify(u: Mamba2Units, T: int) -> int:
+    return u.S + T * u.S + T * (u.I + u.Y)
+
+
+@dataclass(frozen=True)
+class GDNUnits:
+    S: int
+    I: int
+    Y: int
+    Rw: int
+    Rr: int
+
+
+def gdn_units(nheads, dk, dv) -> GDNUnits:
+    H = nheads
+    S = H * dv * dk * 4
+    I = 2 * H * dk * 2 + H * dv * 2 + 2 * H * 4
+    Y = H * dv * 4
+    R = H * dk * 2 + H * dv * 2 + 2 * H * 4
+    return GDNUnits(S, I, Y, R, R)
+
+
+def gdn_conventional(u: GDNUnits) -> int:
+    return 2 * u.S + u.I + u.Y
+
+
+def gdn_replay_decode(u: GDNUnits, len_before: int, L: int) -> int:
+    fold = len_before + 1 >= L
+    b = u.I + u.Y + len_before * u.Rr
+    return b + (2 * u.S if fold else u.S + u.Rw)
+
+
+def gdn_replay_period(u: GDNUnits, L: int) -> float:
+    return sum(gdn_replay_decode(u, k, L) for k in range(L)) / L

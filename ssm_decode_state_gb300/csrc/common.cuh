@@ -1,0 +1,236 @@
+// Device helpers shared by the ReplaySSM kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "replayssm.h"
+
+namespace rssm {
+
+constexpr int kMaxL = 32;   // ring capacity limit
+constexpr int kMaxT = 8;    // drafts per verify limit
+
+// ---------------------------------------------------------------- loads/stores
+
+// Streaming (evict-first) 16-byte load/store for checkpoint tiles: each tile
+// is touched once per step, so it should not push the ring records out of L2.
+__device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
+__device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t *p) { return __ldcs(p); }
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// A 16-byte chunk of an input or record row holds 8 bf16 or 4 float32 values.
+__device__ __forceinline__ void unpack_chunk(uint4 c, bool bf16, float *out) {
+    if (bf16) {
+        out[0] = bf16lo(c.x); out[1] = bf16hi(c.x);
+        out[2] = bf16lo(c.y); out[3] = bf16hi(c.y);
+        out[4] = bf16lo(c.z); out[5] = bf16hi(c.z);
+        out[6] = bf16lo(c.w); out[7] = bf16hi(c.w);
+    } else {
+        out[0] = __uint_as_float(c.x); out[1] = __uint_as_float(c.y);
+        out[2] = __uint_as_float(c.z); out[3] = __uint_as_float(c.w);
+    }
+}
+
+// --------------------------------------------------------------- reductions
+
+// Sum V per-lane values over aligned groups of G lanes (G, V powers of two,
+// G <= 32) with V/2 + V/4 + ... shuffles instead of V*log2(G): each round
+// every lane keeps one half of its values and trades the other half with its
+// partner.  On return:
+//   V <= G: v[0] holds the group sum of value index (lane % G) / (G / V);
+//   V >  G: v[i] (i < V/G) holds the group sum of value (lane % G) * (V/G) + i.
+template <int O, int C, int V>
+struct GroupReduce {
+    static __device__ __forceinline__ void run(float (&v)[V], int lane) {
+        if constexpr (O >= 1) {
+            if constexpr (C > 1) {
+                const bool up = (lane & O) != 0;
+#pragma unroll
+                for (int i = 0; i < C / 2; ++i) {
+                    const float send = up ? v[i] : v[i + C / 2];
+                    const float keep = up ? v[i + C / 2] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+                }
+                GroupReduce<O / 2, C / 2, V>::run(v, lane);
+            } else {
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+                GroupReduce<O / 2, 1, V>::run(v, lane);
+            }
+        }
+    }
+};
+
+template <int G, int V>
+__device__ __forceinline__ void group_reduce(float (&v)[V]) {
+    GroupReduce<G / 2, V, V>::run(v, threadIdx.x & 31);
+}
+
+// Value index of v[i] after group_reduce<G, V>, and whether this lane is the
+// one (of the G/V lanes holding the same sum) that should publish it.
+template <int G, int V>
+__device__ __forceinline__ int reduced_index(int i) {
+    const int lg = threadIdx.x & (G - 1);
+    if constexpr (V <= G) return lg / (G / V);
+    else return lg * (V / G) + i;
+}
+template <int G, int V>
+__device__ __forceinline__ bool reduced_writer() {
+    if constexpr (V <= G) return (threadIdx.x & (G / V - 1)) == 0;
+    else return true;
+}
+
+// Like group_reduce, but every lane of the group ends with all V sums in v.
+template <int G, int V>
+__device__ __forceinline__ void group_allreduce(float (&v)[V]) {
+    float t[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) t[i] = v[i];
+    group_reduce<G, V>(t);
+    const int base = (threadIdx.x & 31) & ~(G - 1);
+#pragma unroll
+    for (int vi = 0; vi < V; ++vi) {
+        if constexpr (V <= G) v[vi] = __shfl_sync(0xffffffffu, t[0], base + vi * (G / V));
+        else v[vi] = __shfl_sync(0xffffffffu, t[vi % (V / G)], base + vi / (V / G));
+    }
+}
+
+template <int G>
+__device__ __forceinline__ float group_max(float x) {
+#pragma unroll
+    for (int o = G / 2; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+// ----------------------------------------------------------------------- FP8
+
+// Four float32 values -> four E4M3 codes (round to nearest even, saturating),
+// byte i of the result = element i.
+__device__ __forceinline__ uint32_t e4m3_pack4(float a, float b, float c, float d) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return (lo & 0xffffu) | (hi << 16);
+}
+
+// Four E4M3 codes (byte i = element i) -> float4.
+__device__ __forceinline__ float4 e4m3_unpack4(uint32_t w) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Per-row read-copy scale: scale = amax/448 and inv = 448/amax, each one
+// correctly rounded float32 division; a zero row (or one whose inverse
+// overflows) is stored as zero codes with scale 1.
+__device__ __forceinline__ void e4m3_row_scale(float amax, float &scale, float &inv) {
+    inv = __fdiv_rn(448.0f, amax);
+    scale = __fdiv_rn(amax, 448.0f);
+    if (!(amax > 0.0f) || isinf(inv)) {
+        inv = 0.0f;
+        scale = 1.0f;
+    }
+}
+
+// ------------------------------------------------------------------ the ring
+
+// Sum of dt[j+1 .. e] accumulated from the newest record backwards (j = -1:
+// the whole prefix 0..e).  Every path that needs a decay exponent uses this
+// one order, so fused and standalone flushes agree bit for bit.
+__device__ __forceinline__ float suffix_sum(const float *dt, int j, int e) {
+    float s = 0.0f;
+    for (int m = e; m > j; --m) s += dt[m];
+    return s;
+}
+
+__device__ __forceinline__ void flag_error(uint32_t *err, uint32_t bit) {
+    if (err) atomicOr(err, bit);
+}
+
+// ------------------------------------------------- async copies (sm_90+ PTX)
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// One-dimensional bulk copy global -> this CTA's shared memory (TMA engine);
+// completion is signalled on `bar` as transaction bytes.  dst, src and bytes
+// must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after ~2 s (returns
+// false); a copy that never lands must not hang the GPU.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0 && global_ns() - t0 > 2000000000ull) return false;
+    }
+    return false;
+}
+
+// Ampere-style asynchronous 16- and 4-byte copies into shared memory, for
+// small scattered record rows.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+}  // namespace rssm

@@ -1,0 +1,48 @@
+// Launcher of the persistent Mamba-2 replay decode (serving shapes).
+#include "host_common.h"
+#include "mamba2_persist.cuh"
+
+namespace rssm {
+
+// Returns RSSM_ERR_UNSUPPORTED (without launching) when the shape is not one
+// the persistent kernel handles; the caller then uses the per-tile kernel.
+rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &args, cudaStream_t st) {
+    if (!d->io_bf16 || d->dstate != 128 || d->headdim != 64) return RSSM_ERR_UNSUPPORTED;
+    const int hpg = d->nheads / d->ngroups;
+    const int sms = sm_count();
+    int hpi = 0;
+    for (int c : {8, 4, 2, 1}) {
+        if (hpg % c) continue;
+        if ((long long)d->batch * d->nheads / c >= 16LL * sms || c == 1) { hpi = c; break; }
+    }
+    const long long items = (long long)d->batch * d->nheads / hpi;
+    if (items < 2LL * sms || items > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;
+    int stages = 0;
+    size_t smem = 0;
+    for (int s = 6; s >= 2; --s) {
+        const PSmem lay(64, 128, d->L, hpi, s);
+        if (lay.total <= 227 * 1024) { stages = s; smem = lay.total; break; }
+    }
+    if (!stages) return RSSM_ERR_UNSUPPORTED;
+    PersistCfg pc;
+    pc.items = (int)items;
+    pc.nchunk = hpg / hpi;
+    pc.stages = stages;
+    pc.arrivals = d->nheads / hpi;
+    void *k = nullptr;
+    switch (hpi) {
+        case 8: k = (void *)m2_decode_persistent<128, 8, 8>; break;
+        case 4: k = (void *)m2_decode_persistent<128, 8, 4>; break;
+        case 2: k = (void *)m2_decode_persistent<128, 8, 2>; break;
+        default: k = (void *)m2_decode_persistent<128, 8, 1>; break;
+    }
+    rssm_status s = ensure_smem((const void *)k, smem);
+    if (s != RSSM_OK) return s;
+    const int grid = (int)(items < sms ? items : sms);
+    M2Args a = args;
+    void *params[] = {&a, &pc};
+    if (cudaLaunchKernel(k, dim3(grid), dim3(256), params, smem, st) != cudaSuccess) return RSSM_ERR_CUDA;
+    return launch_status();
+}
+
+}  // namespace rssm

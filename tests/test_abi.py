@@ -1,0 +1,133 @@
+"""The C ABI: the library builds, loads, exports every declared entry point,
+its structs match the binding, and host-side argument checks return their
+status before anything is launched (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "replayssm.h")
+
+
+@pytest.fixture(scope="module")
+def rs():
+    import __graft_entry__
+    __graft_entry__.build()
+    from ssm_decode_state_gb300 import replayssm
+    return replayssm
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(replayssm_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(rs):
+    lib = ctypes.CDLL(rs.library_path())
+    declared = _declared()
+    assert len(declared) >= 13
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(rs.EXPORTS) == declared
+
+
+def test_struct_layout_matches_binding(rs, tmp_path):
+    """Compile a C probe against the header and compare sizes/offsets."""
+    probe = tmp_path / "probe.c"
+    probe.write_text(r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "replayssm.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(rssm_mamba2_dims), sizeof(rssm_mamba2_cache),
+         sizeof(rssm_gdn_dims), sizeof(rssm_gdn_cache), offsetof(rssm_mamba2_cache, err),
+         offsetof(rssm_mamba2_cache, arrive), offsetof(rssm_gdn_cache, err));
+  return 0;
+}''')
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(probe), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert out == [ctypes.sizeof(rs.Mamba2Dims), ctypes.sizeof(rs.Mamba2CacheC),
+                   ctypes.sizeof(rs.GDNDims), ctypes.sizeof(rs.GDNCacheC),
+                   rs.Mamba2CacheC.err.offset, rs.Mamba2CacheC.arrive.offset, rs.GDNCacheC.err.offset]
+
+
+def test_status_strings(rs):
+    for code in range(7):
+        assert rs.status_string(code)
+    assert rs.version() == 0x100
+
+
+# ---- host-side argument checks (each returns before any launch)
+
+FAKE = 0x10000          # 16-byte aligned, never dereferenced: every case fails first
+MIS = 0x10008
+
+
+def _m2(rs, **kw):
+    d = dict(batch=2, nheads=4, headdim=16, dstate=16, ngroups=1, L=16, read_copy=0, io_bf16=1)
+    d.update(kw)
+    return rs.Mamba2Dims(**d)
+
+
+def _cache(rs, **kw):
+    c = {f: FAKE for f, _ in rs.Mamba2CacheC._fields_}
+    c.update(kw)
+    return rs.Mamba2CacheC(**c)
+
+
+def _decode(rs, dims, cache, x=FAKE):
+    lib = rs._lib
+    return lib.replayssm_decode(ctypes.byref(dims) if dims is not None else None,
+                                ctypes.byref(cache), FAKE, x, FAKE, FAKE, FAKE, None)
+
+
+def test_null_and_shape_errors(rs):
+    assert _decode(rs, None, _cache(rs)) == 1
+    assert _decode(rs, _m2(rs, dstate=48), _cache(rs)) == 3
+    assert _decode(rs, _m2(rs, headdim=12), _cache(rs)) == 3
+    assert _decode(rs, _m2(rs, nheads=6, ngroups=4), _cache(rs)) == 3
+    assert _decode(rs, _m2(rs, L=0), _cache(rs)) == 3
+    assert _decode(rs, _m2(rs, L=33), _cache(rs)) == 3
+    assert _decode(rs, _m2(rs, read_copy=2), _cache(rs)) == 3
+    assert _decode(rs, _m2(rs), _cache(rs, ring_len=None)) == 1
+    assert _decode(rs, _m2(rs), _cache(rs, arrive=None)) == 1
+    assert _decode(rs, _m2(rs, read_copy=1), _cache(rs, ckpt_q=None)) == 1
+
+
+def test_alignment_errors(rs):
+    assert _decode(rs, _m2(rs), _cache(rs, ckpt=MIS)) == 2
+    assert _decode(rs, _m2(rs), _cache(rs, rec_x=MIS)) == 2
+    assert _decode(rs, _m2(rs), _cache(rs), x=MIS) == 2
+
+
+def test_verify_draft_count(rs):
+    lib = rs._lib
+    d, c = _m2(rs, L=4), _cache(rs)
+    for T in (0, 5, 9):
+        assert lib.replayssm_verify(ctypes.byref(d), ctypes.byref(c), T, FAKE, FAKE, FAKE, FAKE,
+                                    FAKE, None) == 4
+    assert lib.replayssm_rollback(ctypes.byref(d), ctypes.byref(c), 0, FAKE, None) == 4
+    assert lib.replayssm_conventional_select(4, FAKE, 9, FAKE, FAKE, None) == 4
+    assert lib.replayssm_conventional_select(0, FAKE, 2, FAKE, FAKE, None) == 3
+
+
+def test_gdn_checks(rs):
+    lib = rs._lib
+    c = rs.GDNCacheC(**{f: FAKE for f, _ in rs.GDNCacheC._fields_})
+    bad = [rs.GDNDims(2, 4, 48, 64, 16), rs.GDNDims(2, 4, 64, 12, 16), rs.GDNDims(0, 4, 64, 64, 16)]
+    for d in bad:
+        assert lib.replayssm_gdn_decode(ctypes.byref(d), ctypes.byref(c), FAKE, FAKE, FAKE, FAKE,
+                                        FAKE, FAKE, None) == 3
+    d = rs.GDNDims(2, 4, 64, 64, 16)
+    c2 = rs.GDNCacheC(**{**{f: FAKE for f, _ in rs.GDNCacheC._fields_}, "rec_k": MIS})
+    assert lib.replayssm_gdn_decode(ctypes.byref(d), ctypes.byref(c2), FAKE, FAKE, FAKE, FAKE,
+                                    FAKE, FAKE, None) == 2
+    assert lib.replayssm_gdn_conventional_decode(ctypes.byref(d), None, FAKE, FAKE, FAKE, FAKE,
+                                                 FAKE, FAKE, None) == 1

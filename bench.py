@@ -1,0 +1,353 @@
+"""Benchmark of the ReplaySSM decode path on one GB300 (or N replicas).
+
+Default workload: the Mamba-2 layer at serving shape (nheads 128, headdim 64,
+dstate 128, ngroups 8; 4 MiB FP32 state per sequence), batch 256, L = 16,
+replay decode steps with the flush fused into every 16th step.  One step is
+one replay decode of the whole batch (append, decay weights, record
+contractions, checkpoint contraction, output, and on flush steps the fold).
+
+Prints one JSON line (rank 0):
+  value        sequences*tokens/s per layer over the K timed steps, inputs
+               resident in HBM, device time (CUDA events on the launch stream)
+  e2e          the same metric with each step's inputs copied from pinned host
+               memory and y copied back inside the timed region
+  roofline     algorithmic bytes per decode launch / its average duration
+               against the measured HBM copy bandwidth
+  cpu_baseline the CPU oracle (float64 stepwise recurrence) on a bounded
+               sample of the same workload
+`--impl reference` times the CPU oracle as the reference arm instead.
+
+N > 1 (torchrun): every rank runs its own replica on its own GPU (the path
+has no exchange step); value = all ranks' tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ssm_decode_state_gb300 import bytes_model as bm  # noqa: E402
+from ssm_decode_state_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "replay SSM decode tokens/s/layer at B=256; achieved HBM GB/s vs GB300 peak"
+UNIT = "seq*tok/s/layer"
+POOL = 32                       # distinct per-step input sets kept on the device
+KERNEL_SOURCES = ["ssm_decode_state_gb300/csrc/mamba2_persist.cuh",
+                  "ssm_decode_state_gb300/csrc/common.cuh"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_per_launch():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "replay_decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_sources_sha") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline (reference arm and cpu_baseline)
+# --------------------------------------------------------------------------
+
+def oracle_rate(shape: gen.Mamba2Shape, seed: int, seqs: int, steps: int):
+    """Time the oracle's stepwise recurrence on `seqs` sequences x `steps`
+    tokens of the workload; returns (seq*tok/s, seconds, sample text)."""
+    from oracle.mamba2 import Mamba2Stepwise
+    prm = gen.mamba2_params(shape, seed)
+    sub = gen.Mamba2Shape(seqs, shape.nheads, shape.headdim, shape.dstate, shape.ngroups, shape.L,
+                          shape.bf16_io)
+    h0 = gen.mamba2_random_state(shape, seed, batch_slice=slice(0, seqs))
+    m = Mamba2Stepwise(prm.A, prm.D, shape.ngroups, h0)
+    toks = [gen.mamba2_step_inputs(sub, prm, seed, t) for t in range(steps)]
+    t0 = time.perf_counter()
+    for st in toks:
+        m.step(st.dt, st.x, st.B, st.C)
+    el = time.perf_counter() - t0
+    return seqs * steps / el, el, f"{seqs} sequences x {steps} decode steps of the batch-{shape.batch} shape"
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def _timed(stream, fn, steps):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(steps):
+        fn(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def run_native(args, rank, world, local_rank):
+    import torch
+    import __graft_entry__
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    if rank == 0:
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+    from ssm_decode_state_gb300 import replayssm as rs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = gen.workloads()["mamba2_b256"]
+    shape = w.shape
+    if args.batch:
+        shape = gen.Mamba2Shape(args.batch, shape.nheads, shape.headdim, shape.dstate, shape.ngroups,
+                                shape.L, shape.bf16_io)
+    B, H, P, N, G, L = shape.batch, shape.nheads, shape.headdim, shape.dstate, shape.ngroups, shape.L
+    seed = w.seed + 17 * rank
+    prm = gen.mamba2_params(shape, seed)
+    dims = rs.mamba2_dims(B, H, P, N, G, L, read_copy=0, io_bf16=True)
+
+    gcuda = torch.Generator(device=dev)
+    gcuda.manual_seed(seed)
+    ckpt = torch.randn(B, H, P, N, device=dev, generator=gcuda).mul_(0.1)   # N(0, 0.1^2)
+    cache = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D), ckpt=ckpt, device=dev)
+
+    # pool of per-step inputs (seeded, the workload's distributions)
+    host = [gen.mamba2_step_inputs(shape, prm, seed, t) for t in range(POOL)]
+    pool = [(torch.from_numpy(s.dt).to(dev), torch.from_numpy(s.x).to(torch.bfloat16).to(dev),
+             torch.from_numpy(s.B).to(torch.bfloat16).to(dev), torch.from_numpy(s.C).to(torch.bfloat16).to(dev))
+            for s in host]
+    y = torch.empty(B, H, P, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    u = bm.mamba2_units(H, P, N, G)
+
+    K, W = args.steps, args.warmup
+    for t in range(W):
+        rs.decode(cache, *pool[t % POOL], y=y)
+    torch.cuda.synchronize(dev)
+    start_len = int(cache.ring_len[0].item())
+    alg_bytes, ln, nflush = 0, start_len, 0
+    for _ in range(K):
+        alg_bytes += bm.mamba2_replay_decode(u, ln, L) * B
+        if ln + 1 >= L:
+            ln, nflush = 0, nflush + 1
+        else:
+            ln += 1
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ms = _timed(stream, lambda t: rs.decode(cache, *pool[(W + t) % POOL], y=y), K)
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    assert int(cache.err.item()) == 0, "device error word set"
+
+    # ---- conventional in-place decode on the same shape (comparison path)
+    conv_ms = 0.0
+    if not args.no_conventional:
+        state = ckpt.clone()
+        for t in range(W):
+            rs.conventional_decode(dims, state, cache.A, cache.D, *pool[t % POOL], y=y)
+        torch.cuda.synchronize(dev)
+        conv_ms = _timed(stream, lambda t: rs.conventional_decode(dims, state, cache.A, cache.D,
+                                                                  *pool[(W + t) % POOL], y=y), K)
+        del state
+
+    # ---- end to end: inputs from pinned host memory, y back to host, per step
+    hpin = [tuple(t.to("cpu").pin_memory() for t in p) for p in pool]
+    ypin = torch.empty(B, H, P).pin_memory()
+    dbuf = tuple(torch.empty_like(t) for t in pool[0])
+    h2d = sum(t.numel() * t.element_size() for t in hpin[0])
+    d2h = ypin.numel() * ypin.element_size()
+    Ke = max(16, min(K, args.e2e_steps))
+
+    def e2e_step(t):
+        for d_, h_ in zip(dbuf, hpin[t % POOL]):
+            d_.copy_(h_, non_blocking=True)
+        rs.decode(cache, *dbuf, y=y)
+        ypin.copy_(y, non_blocking=True)
+
+    for t in range(W):
+        e2e_step(t)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    e2e_ms = _timed(stream, e2e_step, Ke)
+
+    times = torch.tensor([ms, e2e_ms, conv_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms, e2e_ms, conv_ms = times.tolist()
+    if rank != 0:
+        return
+    value = world * B * K / (ms / 1e3)
+    per_launch_s = ms / 1e3 / K
+    achieved = alg_bytes / K / per_launch_s / 1e9
+    peak, peak_src = peaks()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; distributions of the workload)",
+        "config": {"workload": f"mamba2 replay decode B={B} H={H} P={P} N={N} G={G} L={L}",
+                   "batch": B, "state_bytes_per_seq": H * P * N * 4, "io": "bf16 x/B/C, f32 dt/A/D/y",
+                   "flush_steps_timed": nflush, "ring_len_at_start": start_len,
+                   "l2": "no flush needed: 1 GiB of checkpoint per step > 129 MB L2",
+                   "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic_per_launch(),
+                     "kernel": "m2_decode_persistent",
+                     "alg_bytes_per_launch": int(alg_bytes / K),
+                     "peak_source": f"{peak_src} hbm_gbs (copy), of measured"},
+        "e2e": {"value": round(world * B * Ke / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if conv_ms:
+        line["conventional"] = {"value": round(world * B * K / (conv_ms / 1e3), 1),
+                                "ms_per_step": round(conv_ms / K, 5),
+                                "alg_bytes_per_launch": bm.mamba2_conventional(u) * B,
+                                "replay_speedup": round(conv_ms / ms, 3)}
+    if world == 1 and not args.no_cpu_baseline:
+        rate, el, sample = oracle_rate(shape, seed, args.cpu_seqs, args.cpu_steps)
+        line["cpu_baseline"] = {"value": round(rate, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": sample, "seconds": round(el, 2)}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = gen.workloads()["mamba2_b256"]
+    shape = w.shape
+    seqs = args.cpu_seqs
+    steps = max(1, min(args.cpu_steps, max(args.steps, 1)))
+    oracle_rate(shape, w.seed, 1, 2)                  # warm-up pass, untimed
+    rate, el, sample = oracle_rate(shape, w.seed, seqs, steps)
+    line = {
+        "metric": METRIC, "value": round(rate, 3), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"mamba2 replay decode B={shape.batch} H={shape.nheads} P={shape.headdim} "
+                               f"N={shape.dstate} G={shape.ngroups} L={shape.L}",
+                   "batch": shape.batch},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(rate, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(rate, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=32)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=512)
+    ap.add_argument("--cpu-seqs", type=int, default=8)
+    ap.add_argument("--cpu-steps", type=int, default=200)
+    ap.add_argument("--no-conventional", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_native(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+"""FP8 read copy, Gated DeltaNet, device-side error reporting, and the
+persistent decode kernel's shape variants."""
+import numpy as np
+import pytest
+import torch
+
+from oracle.fp8 import quantize_rows
+from oracle.gdn import GDNStepwise
+from ssm_decode_state_gb300 import inputs as gen
+from tests.helpers import RTOL_INPLACE, assert_close, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+# ----------------------------------------------------------------------- FP8
+
+def test_requant_matches_oracle_bitwise():
+    """The read copy built from an FP32 checkpoint equals the oracle's E4M3
+    quantisation of the same values, codes and scales bit for bit (including
+    a zero row, a row of tiny values and saturating values)."""
+    from ssm_decode_state_gb300 import replayssm as rs
+    shape = gen.Mamba2Shape(batch=3, nheads=4, headdim=64, dstate=128, ngroups=1, L=16)
+    h0 = gen.mamba2_random_state(shape, 91)
+    h0[0, 0, 3] = 0.0
+    h0[1, 2, 5] *= 1e-30
+    h0[2, 1, 7, :5] = 1e6
+    prm = gen.mamba2_params(shape, 91)
+    dims = rs.mamba2_dims(3, 4, 64, 128, 1, 16, read_copy=1)
+    c = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D), ckpt=to_dev(h0))
+    rs.requant(c)
+    codes, scale = quantize_rows(h0)
+    np.testing.assert_array_equal(c.ckpt_q.cpu().numpy(), codes)
+    np.testing.assert_array_equal(c.ckpt_scale.cpu().numpy(), scale)
+
+
+def _fp8_bound(h32, scale, C, decay):
+    """Per row: decay * sum_n |C_n| (2^-4 |h_n| + 2^-10 s), the E4M3 rounding
+    bound (half a code step: 2^-4 relative for normals, 2^-10 * scale below
+    the smallest normal).  h32 [b,H,P,N], scale [b,H,P], C [b,H,N], decay [b,H]."""
+    e = np.abs(h32.astype(np.float64)) * 2.0 ** -4 + 2.0 ** -10 * scale[..., None].astype(np.float64)
+    return decay[..., None] * np.einsum("bhpn,bhn->bhp", e, np.abs(C))
+
+
+def test_fp8_read_copy_b256():
+    """Serving shape at batch 256, 1024 decode steps with the FP8 read copy:
+    per-step error of y against the FP32 oracle stays within the E4M3 bound;
+    the FP32 checkpoint of the FP8 run equals that of an FP32-read run bit for
+    bit at every flush (reads never feed the recurrence); the error does not
+    drift across the 64 flush windows."""
+    from ssm_decode_state_gb300 import replayssm as rs
+    from tests.m2_runner import M2Run
+    w = gen.workloads()["mamba2_fp8read_b256"]
+    sample = [7, 200]
+    h0 = gen.mamba2_random_state(w.shape, w.seed)
+    r8 = M2Run(w.shape, w.seed, h0=h0, read_copy=1, sample=sample, conventional=False)
+    r32 = M2Run(w.shape, w.seed, h0=h0, read_copy=0, sample=[0], conventional=False,
+                h0_sample=h0[:1])
+    del h0
+    prm = r8.params
+    g = np.arange(w.shape.nheads) // (w.shape.nheads // w.shape.ngroups)
+    errs = []
+    for t in range(w.steps):
+        st = gen.mamba2_step_inputs(w.shape, prm, w.seed, t)
+        dt, x, B, C = r8.dev_inputs(st)
+        # checkpoint and read copy as the kernel sees them before this step
+        ln = int(r8.cache.ring_len[0].item())
+        ck = r8.cache.ckpt[sample].cpu().numpy()
+        q = r8.cache.ckpt_q[sample].cpu().numpy()
+        sc = r8.cache.ckpt_scale[sample].cpu().numpy()
+        y8 = rs.decode(r8.cache, dt, x, B, C)
+        rs.decode(r32.cache, dt, x, B, C)
+        yo = r8.oracle.step(*r8._slice(st))
+        r8.ring.decode([t] * w.shape.batch)
+        y8s = y8.cpu().numpy()[sample]
+        if ln + 1 < w.shape.L:
+            # decay exp(A * sum of dt since the checkpoint), from the inputs
+            S = np.zeros((len(sample), w.shape.nheads))
+            dts = [r8.tokens[k].dt[sample] for k in sorted(r8.tokens)][-ln:] if ln else []
+            for d_ in dts + [st.dt[sample]]:
+                S += d_
+            decay = np.exp(prm.A[None].astype(np.float64) * S)
+            bound = _fp8_bound(ck, sc, st.C[sample][:, g], decay)
+            tau = 1e-2 * np.sqrt(np.mean(yo ** 2))
+            slack = 1e-4 * np.maximum(np.abs(yo), tau)
+            assert np.all(np.abs(y8s - yo) <= bound + slack), f"fp8 bound violated at step {t}"
+            assert np.all((q & 0x7F) != 0x7F)                  # no NaN codes
+        else:
+            # flush step: y from the FP32 values, FP32 checkpoints identical
+            np.testing.assert_array_equal(r8.cache.ckpt[sample].cpu().numpy(),
+                                          r32.cache.ckpt[sample].cpu().numpy())
+        r8._keep(t, st)
+        errs.append(np.linalg.norm(y8s - yo) / np.linalg.norm(yo))
+    errs = np.array(errs)
+    win = errs.reshape(-1, w.shape.L).mean(axis=1)
+    assert win[-8:].mean() <= 1.5 * win[:8].mean(), (win[:8].mean(), win[-8:].mean())
+    assert errs.max() < 0.1
+    print("fp8 normwise rel err: mean %.3e max %.3e" % (errs.mean(), errs.max()))
+
+
+# ----------------------------------------------------------------------- GDN
+
+class GDNRun:
+    def __init__(self, shape, seed, sample=None):
+        from ssm_decode_state_gb300 import replayssm as rs
+        self.rs, self.shape, self.seed = rs, shape, seed
+        b = shape.batch
+        self.sample = np.arange(b) if sample is None else np.asarray(sample)
+        S0 = gen.gdn_random_state(shape, seed)
+        self.dims = rs.gdn_dims(b, shape.nheads, shape.dk, shape.dv, shape.L)
+        self.cache = rs.gdn_cache(self.dims, ckpt=to_dev(S0))
+        self.conv = to_dev(S0)
+        self.oracle = GDNStepwise(S0[self.sample])
+        self.len = 0
+        self.max_err = 0.0
+
+    def step(self, t):
+        st = gen.gdn_step_inputs(self.shape, self.seed, t)
+        q, k, v = (to_dev(a, torch.bfloat16) for a in (st.q, st.k, st.v))
+        al, be = to_dev(st.alpha), to_dev(st.beta)
+        o = self.rs.gdn_decode(self.cache, q, k, v, al, be)
+        oc = self.rs.gdn_conventional_decode(self.dims, self.conv, q, k, v, al, be)
+        s = self.sample
+        oo = self.oracle.step(st.q[s], st.k[s], st.v[s], st.alpha[s], st.beta[s])
+        # the gated delta fold applies its L rank-one updates one after the
+        # other, rounding the state once per record like the in-place path, so
+        # both GDN paths take the in-place gate
+        e = assert_close(o.cpu().numpy()[s], oo, f"gdn replay o step {t}", RTOL_INPLACE)
+        self.max_err = max(self.max_err, e)
+        assert_close(oc.cpu().numpy()[s], oo, f"gdn conventional o step {t}", RTOL_INPLACE)
+        fold = self.len + 1 >= self.shape.L
+        self.len = 0 if fold else self.len + 1
+        assert (self.cache.ring_len.cpu().numpy() == self.len).all()
+        assert int(self.cache.err.item()) == 0
+        if fold:
+            e = rel_err(self.cache.ckpt.cpu().numpy()[s], self.oracle.S)
+            assert e <= RTOL_INPLACE, f"gdn checkpoint after step {t}: {e:.3e}"
+
+
+@pytest.mark.parametrize("dk,dv,L", [(16, 16, 4), (32, 24, 16), (64, 64, 8)])
+def test_gdn_small(dk, dv, L):
+    shape = gen.GDNShape(batch=3, nheads=4, dk=dk, dv=dv, L=L)
+    r = GDNRun(shape, 300 + dk)
+    for t in range(3 * L + 1):
+        r.step(t)
+
+
+def test_gdn_flush_standalone():
+    from ssm_decode_state_gb300 import replayssm as rs
+    shape = gen.GDNShape(batch=3, nheads=4, dk=32, dv=32, L=8)
+    r = GDNRun(shape, 404)
+    for t in range(5):
+        r.step(t)
+    rs.gdn_flush(r.cache, torch.tensor([1, 0, 1], dtype=torch.uint8, device="cuda"))
+    assert r.cache.ring_len.cpu().tolist() == [0, 5, 0]
+    assert r.cache.ring_head.cpu().tolist() == [5, 0, 5]
+    ck = r.cache.ckpt.cpu().numpy()
+    for b in (0, 2):
+        assert rel_err(ck[b], r.oracle.S[b]) <= RTOL_INPLACE
+
+
+def test_gdn_b256_sampled():
+    """Gated DeltaNet layer, batch 256, 32 heads, dk = dv = 128, L = 16, 256
+    steps; the oracle follows 2 sequences."""
+    w = gen.workloads()["gdn_b256"]
+    r = GDNRun(w.shape, w.seed, sample=[3, 250])
+    for t in range(w.steps):
+        r.step(t)
+    print("gdn b256 max replay error", r.max_err)
+
+
+# ------------------------------------------------------------ device errors
+
+def test_bad_ring_pointers_skip_sequence():
+    from ssm_decode_state_gb300 import replayssm as rs
+    from tests.m2_runner import M2Run
+    for b_, H, P in [(3, 8, 32), (64, 128, 64)]:          # per-tile and persistent kernels
+        shape = gen.Mamba2Shape(batch=b_, nheads=H, headdim=P, dstate=128 if P == 64 else 64,
+                                ngroups=2, L=8)
+        h0 = gen.mamba2_random_state(shape, 5)
+        r = M2Run(shape, 5, h0=h0, sample=[0], conventional=False)
+        r.decode(0)
+        r.cache.ring_len[1] = 9                            # > L
+        before = r.cache.ckpt[1].clone()
+        rx = r.cache.rec_x[1].clone()
+        st = gen.mamba2_step_inputs(shape, r.params, 5, 1)
+        rs.decode(r.cache, *r.dev_inputs(st))
+        torch.cuda.synchronize()
+        assert int(r.cache.err.item()) & rs.DEVERR_RING_META
+        assert r.cache.ring_len[1].item() == 9
+        assert torch.equal(r.cache.ckpt[1], before) and torch.equal(r.cache.rec_x[1], rx)
+        assert r.cache.ring_len[0].item() == 2 and not r.cache.arrive.any().item()
+
+
+def test_rollback_out_of_range():
+    from ssm_decode_state_gb300 import replayssm as rs
+    shape = gen.Mamba2Shape(batch=3, nheads=4, headdim=16, dstate=16, ngroups=1, L=8)
+    prm = gen.mamba2_params(shape, 1)
+    dims = rs.mamba2_dims(3, 4, 16, 16, 1, 8)
+    c = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D))
+    d = gen.mamba2_draft_inputs(shape, prm, 1, 0, 3)
+    rs.verify(c, to_dev(d.dt), to_dev(d.x, torch.bfloat16), to_dev(d.B, torch.bfloat16),
+              to_dev(d.C, torch.bfloat16))
+    rs.rollback(c, 3, torch.tensor([4, 1, -1], dtype=torch.int32, device="cuda"))
+    assert c.ring_len.cpu().tolist() == [3, 1, 3]
+    assert int(c.err.item()) == rs.DEVERR_ROLLBACK
+
+
+# ------------------------------------------- persistent decode shape variants
+
+@pytest.mark.parametrize("batch,L", [(8, 16), (64, 4), (40, 32)])
+def test_persistent_variants(batch, L):
+    """Serving head shape at batches that pick 1 and 2 heads per work item
+    (batch 256 picks 8), and ring lengths 4..32 (32 lowers the pipeline depth)."""
+    from tests.m2_runner import M2Run
+    shape = gen.Mamba2Shape(batch=batch, nheads=128, headdim=64, dstate=128, ngroups=8, L=L)
+    h0 = gen.mamba2_random_state(shape, 21)
+    r = M2Run(shape, 21, h0=h0, sample=[0, batch - 1], conventional=False)
+    for t in range(2 * L + 3):
+        r.decode(t)
+        if t % 5 == 0:
+            r.check_records(seqs=[0, batch - 1])
+
+
+def test_persistent_fp8_small_batch():
+    """FP8 read copy through the persistent kernel with frequent flushes: ring
+    pointers stay exact and, after the flushes, the read copy encodes the new
+    FP32 checkpoint to within half an E4M3 step per element."""
+    from tests.m2_runner import M2Run
+    shape = gen.Mamba2Shape(batch=16, nheads=128, headdim=64, dstate=128, ngroups=8, L=4)
+    h0 = gen.mamba2_random_state(shape, 8)
+    r = M2Run(shape, 8, h0=h0, read_copy=1, sample=[3], conventional=False)
+    for t in range(9):
+        r.decode(t, check=False)
+        r.check_ring()
+    ck = r.cache.ckpt.cpu().numpy().astype(np.float64)
+    sc = r.cache.ckpt_scale.cpu().numpy().astype(np.float64)
+    codes = r.cache.ckpt_q.cpu().numpy()
+    sign = np.where(codes & 0x80, -1.0, 1.0)
+    e, m = (codes >> 3) & 0xF, codes & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e.astype(np.float64) - 7))
+    dq = sign * mag * sc[..., None]
+    bound = 2.0 ** -4 * np.abs(ck) + 2.0 ** -10 * sc[..., None] + 1e-6 * np.abs(ck)
+    assert np.all(np.abs(dq - ck) <= bound)

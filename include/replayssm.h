@@ -128,6 +128,31 @@ rssm_status replayssm_decode(const rssm_mamba2_dims *dims, const rssm_mamba2_cac
                              float *y, void *stream);
 
 /*
+ * replayssm_decode for callers that cannot allocate device memory (the paper
+ * has no counterpart; this is a library convenience).  Some callers cannot
+ * call cudaMalloc or keep a buffer of their own between calls -- for example
+ * a plugin inside an inference engine whose memory planner owns all device
+ * memory and passes the plugin only its inputs and outputs -- so they have no
+ * place for the per-sequence arrival counters that replayssm_decode takes in
+ * cache->arrive.  This entry point ignores cache->arrive (it may be NULL) and
+ * uses a fixed array of 4096 counters (16 KiB) in the library's own device
+ * memory instead; every GPU that loads the library holds that array until
+ * the process exits.  Everything else -- arguments, results, errors -- is as
+ * replayssm_decode.
+ *  - batch > 4096 returns RSSM_ERR_SHAPE before anything is enqueued.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - Each call clears the counters it uses (an asynchronous memset on
+ *    `stream`) and then enqueues the decode.
+ *  - All calls share the one array: calls that can overlap on the GPU (other
+ *    streams, other host threads) race on it and must be serialised.
+ */
+rssm_status replayssm_decode_noalloc(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
+                                     const float *dt, const void *x, const void *B, const void *C,
+                                     float *y, void *stream);
+
+/*
  * Standalone flush (WittyWires §What happened: the checkpoint is updated when
  * the buffer fills): for every sequence with mask[b] != 0 (mask = NULL: all),
  * fold its ring_len records into the checkpoint with the same arithmetic as

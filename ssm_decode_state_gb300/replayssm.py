@@ -22,7 +22,7 @@ if not os.path.exists(_LIB_PATH):
 _lib = ctypes.CDLL(_LIB_PATH)
 
 EXPORTS = [
-    "replayssm_decode", "replayssm_flush", "replayssm_verify", "replayssm_rollback",
+    "replayssm_decode", "replayssm_decode_noalloc", "replayssm_flush", "replayssm_verify", "replayssm_rollback",
     "replayssm_requant", "replayssm_conventional_decode", "replayssm_conventional_verify",
     "replayssm_conventional_select", "replayssm_gdn_decode", "replayssm_gdn_flush",
     "replayssm_gdn_conventional_decode", "replayssm_status_string", "replayssm_version",
@@ -63,6 +63,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int32
 _sig = {
     "replayssm_decode": [_P, _P, _P, _P, _P, _P, _P, _P],
+    "replayssm_decode_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P],
     "replayssm_flush": [_P, _P, _P, _P],
     "replayssm_verify": [_P, _P, _I, _P, _P, _P, _P, _P, _P],
     "replayssm_rollback": [_P, _P, _I, _P, _P],
@@ -167,6 +168,19 @@ def decode(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None) -> torch.Tensor
     cs = cache.c_struct()
     _check(_lib.replayssm_decode(ctypes.byref(d), ctypes.byref(cs), _ptr(dt), _ptr(x), _ptr(B), _ptr(C),
                                  _ptr(y), _stream(stream)))
+    return y
+
+
+def decode_noalloc(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None) -> torch.Tensor:
+    """decode() for callers that cannot allocate: the arrival counters live in
+    the library's own device memory (cache.arrive is not used; batch <= 4096)."""
+    d = cache.dims
+    if y is None:
+        y = torch.empty(d.batch, d.nheads, d.headdim, dtype=torch.float32, device=dt.device)
+    cs = cache.c_struct()
+    cs.arrive = None
+    _check(_lib.replayssm_decode_noalloc(ctypes.byref(d), ctypes.byref(cs), _ptr(dt), _ptr(x), _ptr(B),
+                                         _ptr(C), _ptr(y), _stream(stream)))
     return y
 
 

@@ -1,4 +1,6 @@
 // Launcher of the persistent Mamba-2 replay decode (serving shapes).
+#include <algorithm>
+
 #include "host_common.h"
 #include "mamba2_persist.cuh"
 
@@ -17,17 +19,19 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
     }
     const long long items = (long long)d->batch * d->nheads / hpi;
     if (items < 2LL * sms || items > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;
-    int stages = 0;
+    int stages = 0, recbufs = 0;
     size_t smem = 0;
     for (int s = 6; s >= 2; --s) {
-        const PSmem lay(64, 128, d->L, hpi, s);
-        if (lay.total <= 227 * 1024) { stages = s; smem = lay.total; break; }
+        const int rb = std::min(8, std::max(2, (s + hpi - 1) / hpi + 1));
+        const PSmem lay(64, 128, d->L, hpi, s, rb);
+        if (lay.total <= 227 * 1024) { stages = s; recbufs = rb; smem = lay.total; break; }
     }
     if (!stages) return RSSM_ERR_UNSUPPORTED;
     PersistCfg pc;
     pc.items = (int)items;
     pc.nchunk = hpg / hpi;
     pc.stages = stages;
+    pc.recbufs = recbufs;
     pc.arrivals = d->nheads / hpi;
     void *k = nullptr;
     switch (hpi) {
@@ -41,7 +45,7 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
     const int grid = (int)(items < sms ? items : sms);
     M2Args a = args;
     void *params[] = {&a, &pc};
-    if (cudaLaunchKernel(k, dim3(grid), dim3(256), params, smem, st) != cudaSuccess) return RSSM_ERR_CUDA;
+    if (cudaLaunchKernel(k, dim3(grid), dim3(kPThreads), params, smem, st) != cudaSuccess) return RSSM_ERR_CUDA;
     return launch_status();
 }
 

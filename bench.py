@@ -220,6 +220,20 @@ def run_native(args, rank, world, local_rank):
     clocks = sampler.stop()
     assert int(cache.err.item()) == 0, "device error word set"
 
+    # ---- per-step split: each launch between its own events, two flush periods
+    split = {"nonflush": [], "flush": []}
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * L)]
+    ln0 = int(cache.ring_len[0].item())
+    kinds = []
+    for i, (s0, s1) in enumerate(evs):
+        kinds.append("flush" if (ln0 + i) % L == L - 1 else "nonflush")
+        s0.record(stream)
+        rs.decode(cache, *pool[i % POOL], y=y)
+        s1.record(stream)
+    torch.cuda.synchronize(dev)
+    for kind, (s0, s1) in zip(kinds, evs):
+        split[kind].append(s0.elapsed_time(s1) * 1e3)
+
     # ---- conventional in-place decode on the same shape (comparison path)
     conv_ms = 0.0
     if not args.no_conventional:
@@ -278,6 +292,7 @@ def run_native(args, rank, world, local_rank):
                      "peak_source": f"{peak_src} hbm_gbs (copy), of measured"},
         "e2e": {"value": round(world * B * Ke / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},
+        "step_us": {k: round(statistics.median(v), 1) for k, v in split.items() if v},
         "gpu_launches": K,
         "clocks": clocks,
     }
@@ -291,6 +306,69 @@ def run_native(args, rank, world, local_rank):
         line["cpu_baseline"] = {"value": round(rate, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": sample, "seconds": round(el, 2)}
     print(json.dumps(line), flush=True)
+
+
+def run_sweep(args):
+    """Replay vs conventional decode across batch sizes (device time, CUDA
+    graphs of `steps` launches; inputs resident).  Batches up to 8 keep the
+    whole state in L2 and are labelled so."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from ssm_decode_state_gb300 import replayssm as rs
+    dev = torch.device("cuda", 0)
+    w = gen.workloads()["mamba2_b256"]
+    out = []
+    for B in [int(v) for v in args.sweep.split(",")]:
+        shape = gen.Mamba2Shape(B, w.shape.nheads, w.shape.headdim, w.shape.dstate, w.shape.ngroups,
+                                w.shape.L, True)
+        prm = gen.mamba2_params(shape, w.seed)
+        dims = rs.mamba2_dims(B, shape.nheads, shape.headdim, shape.dstate, shape.ngroups, shape.L)
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed)
+        ck = torch.randn(B, shape.nheads, shape.headdim, shape.dstate, device=dev, generator=g).mul_(0.1)
+        cache = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D), ckpt=ck, device=dev)
+        state = ck.clone()
+        pool = []
+        for t in range(4):
+            st = gen.mamba2_step_inputs(shape, prm, w.seed, t)
+            pool.append((torch.from_numpy(st.dt).to(dev), torch.from_numpy(st.x).to(torch.bfloat16).to(dev),
+                         torch.from_numpy(st.B).to(torch.bfloat16).to(dev),
+                         torch.from_numpy(st.C).to(torch.bfloat16).to(dev)))
+        y = torch.empty(B, shape.nheads, shape.headdim, device=dev)
+        steps = args.steps
+        res = {"batch": B, "state_MiB": B * 4, "l2_resident": B * 4 <= 64}
+        for name, fn in (("replay", lambda t: rs.decode(cache, *pool[t % 4], y=y)),
+                         ("conventional", lambda t: rs.conventional_decode(dims, state, cache.A, cache.D,
+                                                                           *pool[t % 4], y=y))):
+            for t in range(args.warmup):
+                fn(t)
+            torch.cuda.synchronize()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(gr, stream=s):
+                    for t in range(steps):
+                        fn(t)
+            torch.cuda.synchronize()
+            gr.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            gr.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            res[name + "_us_per_step"] = round(ms * 1e3 / steps, 2)
+            res[name + "_tok_s"] = round(B * steps / (ms / 1e3), 1)
+            del gr
+        res["replay_speedup"] = round(res["conventional_us_per_step"] / res["replay_us_per_step"], 3)
+        out.append(res)
+        assert int(cache.err.item()) == 0
+        del cache, state, ck
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": out}), flush=True)
 
 
 def run_reference(args, rank, world):
@@ -329,6 +407,8 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=200)
     ap.add_argument("--no-conventional", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", type=str, default="",
+                    help="comma-separated batch sizes: replay vs conventional table instead of the bench line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     os.environ.setdefault("OMP_NUM_THREADS", "1")
@@ -337,6 +417,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     if world > 1:
         import torch

@@ -6,10 +6,13 @@
 
 namespace rssm {
 
+// float4s per consumer thread per head tile: 8 -> 8 consumer warps of 8 rows each
+constexpr int kPersistVPT = 8;
+
 // Returns RSSM_ERR_UNSUPPORTED (without launching) when the shape is not one
 // the persistent kernel handles; the caller then uses the per-tile kernel.
 rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &args, cudaStream_t st) {
-    if (!d->io_bf16 || d->dstate != 128 || d->headdim != 64) return RSSM_ERR_UNSUPPORTED;
+    if (!d->io_bf16 || d->dstate != 128 || d->headdim != 64 || d->nheads > 4096) return RSSM_ERR_UNSUPPORTED;
     const int hpg = d->nheads / d->ngroups;
     const int sms = sm_count();
     int hpi = 0;
@@ -23,7 +26,7 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
     size_t smem = 0;
     for (int s = 6; s >= 2; --s) {
         const int rb = std::min(8, std::max(2, (s + hpi - 1) / hpi + 1));
-        const PSmem lay(64, 128, d->L, hpi, s, rb);
+        const PSmem lay(64, 128, d->L, hpi, s, rb, d->nheads);
         if (lay.total <= 227 * 1024) { stages = s; recbufs = rb; smem = lay.total; break; }
     }
     if (!stages) return RSSM_ERR_UNSUPPORTED;
@@ -33,19 +36,21 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
     pc.stages = stages;
     pc.recbufs = recbufs;
     pc.arrivals = d->nheads / hpi;
+    constexpr int VPT = kPersistVPT;
     void *k = nullptr;
     switch (hpi) {
-        case 8: k = (void *)m2_decode_persistent<128, 8, 8>; break;
-        case 4: k = (void *)m2_decode_persistent<128, 8, 4>; break;
-        case 2: k = (void *)m2_decode_persistent<128, 8, 2>; break;
-        default: k = (void *)m2_decode_persistent<128, 8, 1>; break;
+        case 8: k = (void *)m2_decode_persistent<128, 64, VPT, 8>; break;
+        case 4: k = (void *)m2_decode_persistent<128, 64, VPT, 4>; break;
+        case 2: k = (void *)m2_decode_persistent<128, 64, VPT, 2>; break;
+        default: k = (void *)m2_decode_persistent<128, 64, VPT, 1>; break;
     }
     rssm_status s = ensure_smem((const void *)k, smem);
     if (s != RSSM_OK) return s;
     const int grid = (int)(items < sms ? items : sms);
     M2Args a = args;
     void *params[] = {&a, &pc};
-    if (cudaLaunchKernel(k, dim3(grid), dim3(kPThreads), params, smem, st) != cudaSuccess) return RSSM_ERR_CUDA;
+    const int threads = persist_threads(64 * 128 / 4 / VPT);
+    if (cudaLaunchKernel(k, dim3(grid), dim3(threads), params, smem, st) != cudaSuccess) return RSSM_ERR_CUDA;
     return launch_status();
 }
 

@@ -44,16 +44,16 @@ struct PersistCfg {
     int arrivals;  // items per sequence = H / HPI
 };
 
-constexpr int kPConsumers = 256;            // 8 consumer warps
-constexpr int kPThreads = kPConsumers + 64; // + the tile warp and the record warp
+// Threads of a CTA: NC consumers + the tile warp and the record warp.
+constexpr int persist_threads(int nc) { return nc + 64; }
 
 // Byte layout of the persistent kernel's shared memory.
 struct PSmem {
     int stage_bytes, stages_off;
     int full_off, empty_off, rfull_off, rempty_off, mfull_off;
     int rec_off, rx_off, rB_off, rC_off, rdt_off, rec_bytes;
-    int meta_off, cb_off, w_off, decay_off, rt_off, wx_off, flag_off, total;
-    __host__ __device__ PSmem(int P, int N, int L, int HPI, int S, int RB) {
+    int meta_off, cb_off, w_off, decay_off, rt_off, wx_off, ad_off, flag_off, total;
+    __host__ __device__ PSmem(int P, int N, int L, int HPI, int S, int RB, int H) {
         const int KM = L + 1;
         auto up = [](int v, int a) { return (v + a - 1) / a * a; };
         stage_bytes = P * N * 4;
@@ -78,6 +78,7 @@ struct PSmem {
         decay_off = o; o += up(2 * HPI * 4, 16);            // [2][HPI]
         rt_off = o;    o += up(HPI * P * 4, 16);            // [HPI][P] (rows owned per warp)
         wx_off = o;    o += up(KM * P * 4, 16);             // [KM][P]  (rows owned per warp)
+        ad_off = o;    o += up(2 * H * 4, 16);              // A[H], D[H]
         flag_off = o;  o += 16;
         total = o;
     }
@@ -93,9 +94,27 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Named barrier among the consumer warps only.
+// Named barrier among the NC consumer threads only.
+template <int NC>
 __device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kPConsumers) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
+}
+
+// Packed pair of float32 (one 64-bit register) and the sm_100+ two-wide fma:
+// each lane of the pair is an ordinary fused multiply-add, rounded once.
+__device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
 // Bounded wait that also gives up as soon as another warp has aborted.
@@ -112,10 +131,11 @@ __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile i
     return false;
 }
 
-template <int N, int VPT, int HPI>
-__global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Args a, const PersistCfg pc) {
+template <int N, int P, int VPT, int HPI>
+__global__ void __launch_bounds__(persist_threads(P * N / 4 / VPT), 1)
+m2_decode_persistent(const M2Args a, const PersistCfg pc) {
+    constexpr int kPConsumers = P * N / 4 / VPT;         // consumer threads
     constexpr int G4 = N / 4;                            // lanes per row
-    constexpr int P = kPConsumers * VPT * 4 / N;         // rows per head tile
     constexpr int RSTEP = kPConsumers / G4;              // rows between a thread's consecutive float4s
     constexpr int CX = P / 8, CB = N / 8;                // 16-byte chunks per x / B row
     static_assert(G4 == 32, "a warp owns whole rows");
@@ -123,7 +143,7 @@ __global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Arg
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = a.L, H = a.H, G = a.G, hpg = a.hpg, KM = L + 1;
     const int S = pc.stages, RB = pc.recbufs;
-    const PSmem lay(P, N, L, HPI, S, RB);
+    const PSmem lay(P, N, L, HPI, S, RB, H);
     unsigned char *stages = smraw + lay.stages_off;
     uint64_t *full = reinterpret_cast<uint64_t *>(smraw + lay.full_off);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + lay.empty_off);
@@ -135,6 +155,7 @@ __global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Arg
     float *s_decay = reinterpret_cast<float *>(smraw + lay.decay_off);
     float *s_rt = reinterpret_cast<float *>(smraw + lay.rt_off);
     float *s_wx = reinterpret_cast<float *>(smraw + lay.wx_off);
+    float *s_A = reinterpret_cast<float *>(smraw + lay.ad_off), *s_D = s_A + H;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smraw + lay.flag_off);
 
     const int grid = gridDim.x;
@@ -161,6 +182,10 @@ __global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Arg
         }
         *s_abort = 0;
         fence_mbar_init();
+    }
+    for (int i = tid; i < H; i += blockDim.x) {
+        s_A[i] = a.A[i];
+        s_D[i] = a.D[i];
     }
     __syncthreads();                                     // the only CTA-wide barrier
     if (n_my <= 0) return;
@@ -293,7 +318,7 @@ __global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Arg
     bool live = true;                                    // false once any wait gave up
     for (int k = 0; k < n_my; ++k) {
         const int r = k % RB, pb = k & 1;
-        const int it = item_of(k), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
+        const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
         if (live && !pwait(rfull + r, (uint32_t)((k / RB) & 1), s_abort)) {
             live = false;
             *s_abort = 1;
@@ -308,6 +333,32 @@ __global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Arg
         const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
         const float *r_dt = reinterpret_cast<const float *>(rb + lay.rdt_off);
         float *cb = s_cb + pb * KM, *w = s_w + pb * HPI * KM, *dec = s_decay + pb * HPI;
+        if (work && !fold) {
+            // a non-flush step appends the token to the ring, slot (hd + ln) mod L, which
+            // no one reads during this launch; the token is already in the record buffer
+            const int slot = (hd + ln) % L;
+            const int g = h0 / hpg;
+            const int nBC = (h0 % hpg == 0) ? 2 * CB : 0;   // the group's first chunk writes B and C
+            for (int idx = ctid; idx < HPI * CX + nBC + HPI; idx += kPConsumers) {
+                if (idx < HPI * CX) {
+                    const int hh = idx / CX, c = idx - hh * CX;
+                    const size_t bh = (size_t)b * H + h0 + hh;
+                    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.rec_x) + (bh * L + slot) * P + c * 8) =
+                        *reinterpret_cast<const uint4 *>(r_x + (hh * KM + ln) * P + c * 8);
+                } else if (idx < HPI * CX + nBC) {
+                    const int rr = idx - HPI * CX;
+                    const bool isC = rr >= CB;
+                    const int c = isC ? rr - CB : rr;
+                    uint16_t *dst = static_cast<uint16_t *>(isC ? a.rec_C : a.rec_B);
+                    if (dst != nullptr)
+                        *reinterpret_cast<uint4 *>(dst + ((((size_t)b * G + g) * L + slot) * N + c * 8)) =
+                            *reinterpret_cast<const uint4 *>(isC ? r_C + c * 8 : r_B + ln * N + c * 8);
+                } else {
+                    const int hh = idx - HPI * CX - nBC;
+                    a.rec_dt[((size_t)b * H + h0 + hh) * L + slot] = r_dt[hh * KM + ln];
+                }
+            }
+        }
         if (work) {
             // B_j . C_t, one warp per record
             for (int j = cw; j < nrec; j += kPConsumers / 32) {
@@ -322,11 +373,11 @@ __global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Arg
             for (int idx = ctid; idx < HPI * KM; idx += kPConsumers) {
                 const int hh = idx / KM, j = idx - hh * KM;
                 const float *dth = r_dt + hh * KM;
-                if (j < nrec) w[idx] = expf(a.A[h0 + hh] * suffix_sum(dth, j, ln)) * dth[j];
+                if (j < nrec) w[idx] = expf(s_A[h0 + hh] * suffix_sum(dth, j, ln)) * dth[j];
             }
-            if (ctid < HPI) dec[ctid] = expf(a.A[h0 + ctid] * suffix_sum(r_dt + ctid * KM, -1, ln));
+            if (ctid < HPI) dec[ctid] = expf(s_A[h0 + ctid] * suffix_sum(r_dt + ctid * KM, -1, ln));
         }
-        consumer_sync();                                 // cb, w, dec of this item
+        consumer_sync<kPConsumers>();                    // cb, w, dec of this item
         if (work) {
             // record term of the rows this warp owns, for every head of the item
             for (int idx = lane; idx < HPI * VPT; idx += 32) {
@@ -335,7 +386,7 @@ __global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Arg
                 const uint16_t *xh = r_x + hh * KM * P;
                 float acc = 0.0f;
                 for (int j = 0; j < nrec; ++j) acc = fmaf(wh[j] * cb[j], bf16_at(xh, j * P + row), acc);
-                s_rt[hh * P + row] = fmaf(a.D[h0 + hh], bf16_at(xh, ln * P + row), acc);
+                s_rt[hh * P + row] = fmaf(s_D[h0 + hh], bf16_at(xh, ln * P + row), acc);
             }
         }
         __syncwarp();
@@ -392,19 +443,19 @@ __global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Arg
             if (fold) {
                 // rank-nrec update first (each B_j loaded once per lane), then the
                 // decayed checkpoint in one fma: the state is rounded once per flush
-                float4 acc[VPT];
+                unsigned long long acc01[VPT], acc23[VPT];      // packed (x, y) and (z, w)
 #pragma unroll
-                for (int v = 0; v < VPT; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int v = 0; v < VPT; ++v) acc01[v] = acc23[v] = 0ull;
                 for (int j = 0; j < nrec; ++j) {
                     const uint2 braw = *reinterpret_cast<const uint2 *>(r_B + j * N + col4 * 4);
-                    const float b0 = bf16lo(braw.x), b1 = bf16hi(braw.x), b2 = bf16lo(braw.y), b3 = bf16hi(braw.y);
+                    const unsigned long long b01 = f2pack(bf16lo(braw.x), bf16hi(braw.x));
+                    const unsigned long long b23 = f2pack(bf16lo(braw.y), bf16hi(braw.y));
 #pragma unroll
                     for (int v = 0; v < VPT; ++v) {
                         const float c = s_wx[j * P + cw + RSTEP * v];
-                        acc[v].x = fmaf(c, b0, acc[v].x);
-                        acc[v].y = fmaf(c, b1, acc[v].y);
-                        acc[v].z = fmaf(c, b2, acc[v].z);
-                        acc[v].w = fmaf(c, b3, acc[v].w);
+                        const unsigned long long cc = f2pack(c, c);
+                        acc01[v] = fma2(cc, b01, acc01[v]);
+                        acc23[v] = fma2(cc, b23, acc23[v]);
                     }
                 }
                 const float dk = dec[hh];
@@ -412,11 +463,10 @@ __global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Arg
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
                     const int row = cw + RSTEP * v;
-                    float4 o = acc[v];
-                    o.x = fmaf(dk, hv[v].x, o.x);
-                    o.y = fmaf(dk, hv[v].y, o.y);
-                    o.z = fmaf(dk, hv[v].z, o.z);
-                    o.w = fmaf(dk, hv[v].w, o.w);
+                    const unsigned long long dd = f2pack(dk, dk);
+                    float4 o;
+                    f2unpack(fma2(dd, f2pack(hv[v].x, hv[v].y), acc01[v]), o.x, o.y);
+                    f2unpack(fma2(dd, f2pack(hv[v].z, hv[v].w), acc23[v]), o.z, o.w);
                     st_stream(ckp + ctid + v * kPConsumers, o);
                     if (q8) {
                         float m = fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w)));
@@ -430,35 +480,6 @@ __global__ void __launch_bounds__(kPThreads, 1) m2_decode_persistent(const M2Arg
                     }
                 }
                 __syncwarp();                            // s_wx is rewritten for the next head
-            }
-        }
-        // ---- a non-flush step appends the token to the ring (rows of this item)
-        if (work && !fold) {
-            const int slot = (hd + ln) % L;
-            const uint16_t *ix = static_cast<const uint16_t *>(a.x);
-            uint16_t *wrx = static_cast<uint16_t *>(a.rec_x);
-            const int nBC = (h0 % hpg == 0) ? 2 * CB : 0;  // the group's first chunk writes B and C
-            const int total = HPI * CX + nBC + HPI;
-            for (int idx = ctid; idx < total; idx += kPConsumers) {
-                if (idx < HPI * CX) {
-                    const int hh = idx / CX, c = idx - hh * CX;
-                    const size_t bh = (size_t)b * H + h0 + hh;
-                    *reinterpret_cast<uint4 *>(wrx + (bh * L + slot) * P + c * 8) =
-                        __ldcg(reinterpret_cast<const uint4 *>(ix + bh * P + c * 8));
-                } else if (idx < HPI * CX + nBC) {
-                    const int rr = idx - HPI * CX;
-                    const bool isC = rr >= CB;
-                    const int c = isC ? rr - CB : rr;
-                    uint16_t *dst = static_cast<uint16_t *>(isC ? a.rec_C : a.rec_B);
-                    if (dst == nullptr) continue;
-                    const uint16_t *src = static_cast<const uint16_t *>(isC ? a.Cin : a.Bin);
-                    *reinterpret_cast<uint4 *>(dst + ((((size_t)b * G + g) * L + slot) * N + c * 8)) =
-                        __ldcg(reinterpret_cast<const uint4 *>(src + (((size_t)b * G + g) * N + c * 8)));
-                } else {
-                    const int hh = idx - HPI * CX - nBC;
-                    const size_t bh = (size_t)b * H + h0 + hh;
-                    a.rec_dt[bh * L + slot] = __ldcg(a.dt + bh);
-                }
             }
         }
         mbar_arrive(rempty + r);                         // record buffer r may be refilled

@@ -15,23 +15,33 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
     if (!d->io_bf16 || d->dstate != 128 || d->headdim != 64 || d->nheads > 4096) return RSSM_ERR_UNSUPPORTED;
     const int hpg = d->nheads / d->ngroups;
     const int sms = sm_count();
+    // heads per work item: the per-item work (records, weights, record term)
+    // is what limits this kernel, so take the largest item that still leaves
+    // at least 12 items per SM (balance across SMs); small batches get smaller
+    // items so that every SM has work
     int hpi = 0;
     for (int c : {8, 4, 2, 1}) {
         if (hpg % c) continue;
-        if ((long long)d->batch * d->nheads / c >= 16LL * sms || c == 1) { hpi = c; break; }
+        if ((long long)d->batch * d->nheads / c >= 12LL * sms || c == 1) { hpi = c; break; }
     }
     const long long items = (long long)d->batch * d->nheads / hpi;
     if (items < 2LL * sms || items > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;
+    const int grid = (int)(items < sms ? items : sms);
+    const int max_my = (int)((items + grid - 1) / grid);   // ring pointers of these are kept in smem
+    if (max_my > 2048) return RSSM_ERR_UNSUPPORTED;
     int stages = 0, recbufs = 0;
     size_t smem = 0;
     for (int s = 6; s >= 2; --s) {
-        const int rb = std::min(8, std::max(2, (s + hpi - 1) / hpi + 1));
-        const PSmem lay(64, 128, d->L, hpi, s, rb, d->nheads);
+        // record buffers: records of item k+1 land while item k is consumed, and the
+        // next item's preparation reads them during item k
+        const int rb = std::min(8, std::max(3, (s + hpi - 1) / hpi + 2));
+        const PSmem lay(64, 128, d->L, hpi, s, rb, d->nheads, max_my);
         if (lay.total <= 227 * 1024) { stages = s; recbufs = rb; smem = lay.total; break; }
     }
     if (!stages) return RSSM_ERR_UNSUPPORTED;
     PersistCfg pc;
     pc.items = (int)items;
+    pc.max_my = max_my;
     pc.nchunk = hpg / hpi;
     pc.stages = stages;
     pc.recbufs = recbufs;
@@ -46,7 +56,6 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
     }
     rssm_status s = ensure_smem((const void *)k, smem);
     if (s != RSSM_OK) return s;
-    const int grid = (int)(items < sms ? items : sms);
     M2Args a = args;
     void *params[] = {&a, &pc};
     const int threads = persist_threads(64 * 128 / 4 / VPT);

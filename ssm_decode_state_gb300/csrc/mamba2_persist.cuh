@@ -38,6 +38,7 @@ namespace rssm {
 
 struct PersistCfg {
     int items;     // B * H / HPI
+    int max_my;    // items of the busiest CTA: ceil(items / grid)
     int nchunk;    // head chunks per group = hpg / HPI
     int stages;    // S: checkpoint tiles in flight
     int recbufs;   // RB: record buffers in flight
@@ -50,10 +51,10 @@ constexpr int persist_threads(int nc) { return nc + 64; }
 // Byte layout of the persistent kernel's shared memory.
 struct PSmem {
     int stage_bytes, stages_off;
-    int full_off, empty_off, rfull_off, rempty_off, mfull_off;
+    int full_off, empty_off, rfull_off, rempty_off;
     int rec_off, rx_off, rB_off, rC_off, rdt_off, rec_bytes;
     int meta_off, cb_off, w_off, decay_off, rt_off, wx_off, ad_off, flag_off, total;
-    __host__ __device__ PSmem(int P, int N, int L, int HPI, int S, int RB, int H) {
+    __host__ __device__ PSmem(int P, int N, int L, int HPI, int S, int RB, int H, int MY) {
         const int KM = L + 1;
         auto up = [](int v, int a) { return (v + a - 1) / a * a; };
         stage_bytes = P * N * 4;
@@ -63,7 +64,6 @@ struct PSmem {
         empty_off = o;  o += 8 * S;
         rfull_off = o;  o += 8 * RB;
         rempty_off = o; o += 8 * RB;
-        mfull_off = o;  o += 8 * RB;
         o = up(o, 128);
         // one record buffer: x [HPI][KM][P] bf16, B [KM][N] bf16, C [N] bf16, dt [HPI][KM] f32
         rx_off = 0;
@@ -72,11 +72,11 @@ struct PSmem {
         rdt_off = rC_off + up(N * 2, 16);
         rec_bytes = up(rdt_off + HPI * KM * 4, 128);
         rec_off = o;   o += RB * rec_bytes;
-        meta_off = o;  o += up(RB * 8, 16);                 // [RB][head, len]
-        cb_off = o;    o += up(2 * KM * 4, 16);             // [2][KM]
-        w_off = o;     o += up(2 * HPI * KM * 4, 16);       // [2][HPI][KM]
-        decay_off = o; o += up(2 * HPI * 4, 16);            // [2][HPI]
-        rt_off = o;    o += up(HPI * P * 4, 16);            // [HPI][P] (rows owned per warp)
+        meta_off = o;  o += up(MY * 8, 16);                 // [items of this CTA][head, len]
+        cb_off = o;    o += up(3 * KM * 4, 16);             // [3 items][KM]
+        w_off = o;     o += up(3 * HPI * KM * 4, 16);       // [3][HPI][KM]
+        decay_off = o; o += up(3 * HPI * 4, 16);            // [3][HPI]
+        rt_off = o;    o += up(3 * HPI * P * 4, 16);        // [3][HPI][P] (rows owned per warp)
         wx_off = o;    o += up(KM * P * 4, 16);             // [KM][P]  (rows owned per warp)
         ad_off = o;    o += up(2 * H * 4, 16);              // A[H], D[H]
         flag_off = o;  o += 16;
@@ -143,7 +143,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = a.L, H = a.H, G = a.G, hpg = a.hpg, KM = L + 1;
     const int S = pc.stages, RB = pc.recbufs;
-    const PSmem lay(P, N, L, HPI, S, RB, H);
+    const PSmem lay(P, N, L, HPI, S, RB, H, pc.max_my);
     unsigned char *stages = smraw + lay.stages_off;
     uint64_t *full = reinterpret_cast<uint64_t *>(smraw + lay.full_off);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + lay.empty_off);
@@ -169,7 +169,6 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     };
     auto meta_bad = [&](int hd, int ln) { return hd < 0 || hd >= L || ln < 0 || ln > L; };
 
-    uint64_t *mfull = reinterpret_cast<uint64_t *>(smraw + lay.mfull_off);
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full + s, 1);
@@ -178,7 +177,6 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         for (int r = 0; r < RB; ++r) {
             mbar_init(rfull + r, 33);                    // 32 cp.async arrivals + lane 0's release
             mbar_init(rempty + r, kPConsumers);
-            mbar_init(mfull + r, 1);                     // the item's ring pointers are published
         }
         *s_abort = 0;
         fence_mbar_init();
@@ -186,6 +184,27 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     for (int i = tid; i < H; i += blockDim.x) {
         s_A[i] = a.A[i];
         s_D[i] = a.D[i];
+    }
+    // Ring pointers of every item of this CTA, read once here.  Each read is
+    // followed by that item's arrival on its sequence's counter; the thread that
+    // sees a sequence's last arrival commits the new pointers.  That is safe at
+    // once: every item of the sequence, in every CTA, has read them already.
+    for (int k = tid; k < n_my; k += blockDim.x) {
+        const int it = item_of(k), b = item_b(it);
+        const int hd = __ldcg(a.ring_head + b), ln = __ldcg(a.ring_len + b);
+        s_meta[k * 2 + 0] = hd;
+        s_meta[k * 2 + 1] = ln;
+        if (meta_bad(hd, ln) && item_h0(it) == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
+        __threadfence();
+        if (atomicAdd(a.arrive + b, 1) == pc.arrivals - 1) {
+            __threadfence();
+            if (!meta_bad(hd, ln)) {
+                const bool fold = ln + 1 >= L;
+                a.ring_head[b] = fold ? (hd + ln + 1) % L : hd;
+                a.ring_len[b] = fold ? 0 : ln + 1;
+            }
+            a.arrive[b] = 0;
+        }
     }
     __syncthreads();                                     // the only CTA-wide barrier
     if (n_my <= 0) return;
@@ -197,10 +216,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         bool ok = true;
         int issued = 0;
         for (int k = 0; k < n_my && ok; ++k) {
-            const int r = k % RB;
-            ok = pwait(mfull + r, (uint32_t)((k / RB) & 1), s_abort);
-            if (!ok) break;
-            const int hd = s_meta[r * 2 + 0], ln = s_meta[r * 2 + 1];
+            const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
             const bool fp32_tile = meta_bad(hd, ln) || !q8 || (ln + 1 >= L);
             const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
             for (int hh = 0; hh < HPI; ++hh) {
@@ -232,20 +248,6 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
 
     if (warp == 1) {
         // ================================ record warp =================================
-        int pend_b = -1, pend_prev = 0, pend_head = 0, pend_len = 0;     // lane 0 only
-        auto resolve = [&]() {
-            if (pend_b < 0) return;
-            if (pend_prev == pc.arrivals - 1) {
-                __threadfence();
-                if (!meta_bad(pend_head, pend_len)) {
-                    const bool fold = pend_len + 1 >= L;
-                    a.ring_head[pend_b] = fold ? (pend_head + pend_len + 1) % L : pend_head;
-                    a.ring_len[pend_b] = fold ? 0 : pend_len + 1;
-                }
-                a.arrive[pend_b] = 0;
-            }
-            pend_b = -1;
-        };
         const uint16_t *rx = static_cast<const uint16_t *>(a.rec_x);
         const uint16_t *rB = static_cast<const uint16_t *>(a.rec_B);
         const uint16_t *ix = static_cast<const uint16_t *>(a.x);
@@ -258,21 +260,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const int it = item_of(k), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
-            int hd = 0, ln = 0;
-            if (lane == 0) {
-                hd = __ldcg(a.ring_head + b);
-                ln = __ldcg(a.ring_len + b);
-                s_meta[r * 2 + 0] = hd;
-                s_meta[r * 2 + 1] = ln;
-                mbar_arrive(mfull + r);                  // release: the tile warp may read them
-                resolve();
-                __threadfence();
-                pend_prev = atomicAdd(a.arrive + b, 1);
-                pend_b = b; pend_head = hd; pend_len = ln;
-                if (meta_bad(hd, ln) && h0 == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
-            }
-            hd = __shfl_sync(0xffffffffu, hd, 0);
-            ln = __shfl_sync(0xffffffffu, ln, 0);
+            const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
             if (!meta_bad(hd, ln)) {
                 // records: list position j < ln is ring slot (hd + j) mod L, j = ln the current token
                 unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
@@ -297,7 +285,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 }
             }
             cp_async_arrive_noinc(rfull + r);
-            if (lane == 0) mbar_arrive(rfull + r);       // publishes s_meta[r] to the consumers
+            if (lane == 0) mbar_arrive(rfull + r);
         }
         cp_async_wait_all();
         if (!ok) {
@@ -307,7 +295,6 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             }
             return;
         }
-        if (lane == 0) resolve();
         return;
     }
 
@@ -316,28 +303,32 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     const int cw = ctid >> 5;                            // consumer warp: owns rows cw + RSTEP * v
     const int col4 = lane;                               // this lane's 4 columns
     bool live = true;                                    // false once any wait gave up
-    for (int k = 0; k < n_my; ++k) {
-        const int r = k % RB, pb = k & 1;
-        const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
-        if (live && !pwait(rfull + r, (uint32_t)((k / RB) & 1), s_abort)) {
+
+    // Item preparation, done by all consumers: wait for the item's records, append
+    // its token to the ring (non-flush steps), B_j . C_t, the decay weights and
+    // exp(A S) per head, then the record term of the rows each warp owns.  The
+    // item arrays are triple-buffered: item kk+1 is prepared right after the
+    // first tile of item kk, while the next tiles are still in flight.
+    auto prep_item = [&](int kk) {
+        const int r = kk % RB, ia = kk % 3;
+        const int it = item_of(kk), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
+        if (live && !pwait(rfull + r, (uint32_t)((kk / RB) & 1), s_abort)) {
             live = false;
             *s_abort = 1;
         }
-        const int hd = s_meta[r * 2 + 0], ln = s_meta[r * 2 + 1];
+        const int hd = s_meta[kk * 2 + 0], ln = s_meta[kk * 2 + 1];
         const bool work = live && !meta_bad(hd, ln);
-        const bool fold = work && (ln + 1 >= L);
         const int nrec = ln + 1;
         const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
         const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
         const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
         const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
         const float *r_dt = reinterpret_cast<const float *>(rb + lay.rdt_off);
-        float *cb = s_cb + pb * KM, *w = s_w + pb * HPI * KM, *dec = s_decay + pb * HPI;
-        if (work && !fold) {
+        float *cb = s_cb + ia * KM, *w = s_w + ia * HPI * KM, *dec = s_decay + ia * HPI;
+        if (work && ln + 1 < L) {
             // a non-flush step appends the token to the ring, slot (hd + ln) mod L, which
             // no one reads during this launch; the token is already in the record buffer
             const int slot = (hd + ln) % L;
-            const int g = h0 / hpg;
             const int nBC = (h0 % hpg == 0) ? 2 * CB : 0;   // the group's first chunk writes B and C
             for (int idx = ctid; idx < HPI * CX + nBC + HPI; idx += kPConsumers) {
                 if (idx < HPI * CX) {
@@ -377,19 +368,35 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             }
             if (ctid < HPI) dec[ctid] = expf(s_A[h0 + ctid] * suffix_sum(r_dt + ctid * KM, -1, ln));
         }
-        consumer_sync<kPConsumers>();                    // cb, w, dec of this item
+        consumer_sync<kPConsumers>();                    // cb, w, dec of item kk
         if (work) {
             // record term of the rows this warp owns, for every head of the item
+            float *rt = s_rt + ia * HPI * P;
             for (int idx = lane; idx < HPI * VPT; idx += 32) {
                 const int hh = idx / VPT, v = idx - hh * VPT, row = cw + RSTEP * v;
                 const float *wh = w + hh * KM;
                 const uint16_t *xh = r_x + hh * KM * P;
                 float acc = 0.0f;
                 for (int j = 0; j < nrec; ++j) acc = fmaf(wh[j] * cb[j], bf16_at(xh, j * P + row), acc);
-                s_rt[hh * P + row] = fmaf(s_D[h0 + hh], bf16_at(xh, ln * P + row), acc);
+                rt[hh * P + row] = fmaf(s_D[h0 + hh], bf16_at(xh, ln * P + row), acc);
             }
         }
         __syncwarp();
+    };
+
+    prep_item(0);
+    for (int k = 0; k < n_my; ++k) {
+        const int r = k % RB, ia = k % 3;
+        const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
+        const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+        const bool work = live && !meta_bad(hd, ln);
+        const bool fold = work && (ln + 1 >= L);
+        const int nrec = ln + 1;
+        const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
+        const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
+        const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
+        const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
+        const float *w = s_w + ia * HPI * KM, *dec = s_decay + ia * HPI, *rt = s_rt + ia * HPI * P;
         const float4 cfr = make_float4(bf16_at(r_C, col4 * 4 + 0), bf16_at(r_C, col4 * 4 + 1),
                                        bf16_at(r_C, col4 * 4 + 2), bf16_at(r_C, col4 * 4 + 3));
         for (int hh = 0; hh < HPI; ++hh) {
@@ -414,6 +421,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 for (int v = 0; v < VPT; ++v) hv[v] = reinterpret_cast<const float4 *>(stg)[ctid + v * kPConsumers];
             }
             mbar_arrive(empty + s);                      // this thread is done with the stage
+            if (hh == 0 && k + 1 < n_my) prep_item(k + 1);   // overlaps the tiles in flight
             if (!work) continue;
             const int h = h0 + hh;
             const size_t tile = ((size_t)b * H + h) * P;
@@ -438,7 +446,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             group_reduce<G4, VPT>(part);
             if (reduced_writer<G4, VPT>()) {
                 const int row = cw + RSTEP * reduced_index<G4, VPT>(0);
-                a.y[tile + row] = fmaf(dec[hh], part[0], s_rt[hh * P + row]);
+                a.y[tile + row] = fmaf(dec[hh], part[0], rt[hh * P + row]);
             }
             if (fold) {
                 // rank-nrec update first (each B_j loaded once per lane), then the

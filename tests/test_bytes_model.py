@@ -1,0 +1,31 @@
+"""The algorithmic-bytes model against the pages' size arithmetic (Clarity,
+Key figures and claim ledger [10], [11], [19]-[21]; AT Pulse, What happened:
+replay roughly halves the state traffic)."""
+from ssm_decode_state_gb300 import bytes_model as bm
+
+
+def test_state_size_and_kv_equivalents():
+    u = bm.mamba2_units(128, 64, 128, 8)
+    assert u.S == 4 * 1024 * 1024                    # 4 MiB FP32 state per sequence and layer
+    kv_token = 512                                   # 0.5 KiB FP8 KV entry per token
+    assert u.S // kv_token == 8192                   # one SSM layer = 8,192 KV tokens
+    assert 5 * u.S // kv_token == 40960              # five SSM layers per attention layer
+    assert 2 * 5 * u.S // kv_token == 81920          # load + store every step
+
+
+def test_replay_roughly_halves_traffic():
+    u = bm.mamba2_units(128, 64, 128, 8)
+    conv = bm.mamba2_conventional(u)
+    assert conv == 8442368
+    period = bm.mamba2_replay_period(u, 16)
+    assert round(period) == 4671968
+    assert 0.5 < period / conv < 0.6
+    assert round(bm.mamba2_replay_period(u, 16, read_copy=True)) == 1821152
+    assert bm.mamba2_conventional_verify(u, 4) == 21186560
+
+
+def test_gdn_units():
+    g = bm.gdn_units(32, 128, 128)
+    assert g.S == 2 * 1024 * 1024
+    assert bm.gdn_conventional(g) == 4235520
+    assert round(bm.gdn_replay_period(g, 16)) == 2409840

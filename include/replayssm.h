@@ -26,7 +26,8 @@
  *    16-byte aligned.  The library allocates nothing and keeps no state.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
  *    stream-ordered and asynchronous: it validates its arguments on the host,
- *    enqueues one kernel, and returns without synchronising.
+ *    enqueues its kernel (a verify at serving shapes enqueues two), and
+ *    returns without synchronising.
  *  - Host-detectable errors (NULL or misaligned pointers, unsupported shapes,
  *    T out of range) return a status before anything is enqueued.  A failed
  *    launch returns RSSM_ERR_CUDA.  Metadata that only the device can see to

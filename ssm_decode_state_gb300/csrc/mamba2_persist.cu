@@ -64,3 +64,51 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
 }
 
 }  // namespace rssm
+
+#include "mamba2_verify_persist.cuh"
+
+namespace rssm {
+
+// Persistent speculative verify (serving shapes, T <= 4), then the epilogue that
+// writes the drafts' B and C records.  RSSM_ERR_UNSUPPORTED (nothing launched)
+// sends the caller to the per-tile kernel.
+rssm_status launch_verify_persistent(const rssm_mamba2_dims *d, const M2Args &args, cudaStream_t st) {
+    constexpr int HPI = 8;
+    if (!d->io_bf16 || d->dstate != 128 || d->headdim != 64 || d->nheads > 4096) return RSSM_ERR_UNSUPPORTED;
+    if (args.T < 1 || args.T > 4 || args.T > d->L) return RSSM_ERR_UNSUPPORTED;
+    const int hpg = d->nheads / d->ngroups;
+    if (hpg % HPI) return RSSM_ERR_UNSUPPORTED;
+    const int sms = sm_count();
+    const long long items = (long long)d->batch * d->nheads / HPI;
+    if (items < 12LL * sms || items > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;
+    const int grid = sms;
+    const int max_my = (int)((items + grid - 1) / grid);
+    if (max_my > 2048) return RSSM_ERR_UNSUPPORTED;
+    const int rb = 3;
+    int stages = 0;
+    size_t smem = 0;
+    for (int s = 6; s >= 2; --s) {
+        const VSmem lay(64, 128, d->L, args.T, HPI, s, rb, d->nheads, max_my);
+        if (lay.total <= 227 * 1024) { stages = s; smem = lay.total; break; }
+    }
+    if (!stages) return RSSM_ERR_UNSUPPORTED;
+    PersistCfg pc;
+    pc.items = (int)items;
+    pc.max_my = max_my;
+    pc.nchunk = hpg / HPI;
+    pc.stages = stages;
+    pc.recbufs = rb;
+    pc.arrivals = d->nheads / HPI;
+    void *k = (void *)m2_verify_persistent<128, 64, 8, HPI>;
+    rssm_status s = ensure_smem((const void *)k, smem);
+    if (s != RSSM_OK) return s;
+    M2Args a = args;
+    void *params[] = {&a, &pc};
+    if (cudaLaunchKernel(k, dim3(grid), dim3(persist_threads(256)), params, smem, st) != cudaSuccess)
+        return RSSM_ERR_CUDA;
+    if ((s = launch_status()) != RSSM_OK) return s;
+    verify_bc_epilogue<<<d->batch, 128, 0, st>>>(a);
+    return launch_status();
+}
+
+}  // namespace rssm

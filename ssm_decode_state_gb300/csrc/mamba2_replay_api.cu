@@ -6,6 +6,7 @@
 namespace rssm {
 
 rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &a, cudaStream_t st);
+rssm_status launch_verify_persistent(const rssm_mamba2_dims *d, const M2Args &a, cudaStream_t st);
 
 namespace {
 
@@ -154,6 +155,9 @@ extern "C" rssm_status replayssm_verify(const rssm_mamba2_dims *d, const rssm_ma
     M2Args a = make_args(d, c, g);
     a.T = T; a.dt = dt; a.x = x; a.Bin = B; a.Cin = C; a.y = y;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // serving shapes: the persistent pipelined verify (+ its B/C epilogue)
+    s = launch_verify_persistent(d, a, st);
+    if (s != RSSM_ERR_UNSUPPORTED) return s;
     return T <= 4 ? launch<kVerify, 4>(d, a, g, st) : launch<kVerify, 8>(d, a, g, st);
 }
 

@@ -1,0 +1,457 @@
+// Persistent, warp-specialised speculative verify of T drafts (serving shapes).
+//
+// Same pipeline as the persistent decode (mamba2_persist.cuh): one CTA per SM,
+// a tile warp streaming each head's FP32 checkpoint through shared-memory
+// stages with bulk copies, a record warp copying each item's records with
+// cp.async, and eight consumer warps that own whole rows.  Per item (HPI heads
+// of one group of one sequence) the records are the len buffered ones plus the
+// T drafts; draft i is scored against the checkpoint, the buffered records and
+// drafts 1..i:
+//   y_i = exp(A S_i) (h_c . C_i) + sum_{j <= len+i} exp(A (S_i - S_j)) dt_j (B_j . C_i) x_j + D x_i,
+// with S the running sum of dt over the records.  If len + T > L the buffered
+// records are first folded into the checkpoint (the pre-flush), with the same
+// arithmetic as a flush; the outputs are read from the unfolded checkpoint
+// plus all records, which is the same number.
+//
+// Ring pointers are read once at kernel start and committed there by the
+// sequence's last arrival: pre-flush -> head <- (head + len) mod L, len <- T;
+// otherwise len <- len + T.  The drafts' x and dt rows (per head) are appended
+// by the consumers; the drafts' B and C rows are shared by the heads of a group
+// and, on a pre-flush, land on slots other CTAs may still be reading, so a
+// small epilogue kernel writes them after this one.
+#pragma once
+
+#include "mamba2_persist.cuh"
+
+namespace rssm {
+
+// Byte layout of the verify kernel's shared memory (T drafts, KM = L + T).
+struct VSmem {
+    int stage_bytes, stages_off;
+    int full_off, empty_off, rfull_off, rempty_off;
+    int rec_off, rx_off, rB_off, rC_off, rdt_off, rec_bytes;
+    int meta_off, cb_off, w_off, decay_off, wf_off, fdec_off, rt_off, wx_off, ad_off, flag_off, total;
+    __host__ __device__ VSmem(int P, int N, int L, int T, int HPI, int S, int RB, int H, int MY) {
+        const int KM = L + T;
+        auto up = [](int v, int a) { return (v + a - 1) / a * a; };
+        stage_bytes = P * N * 4;
+        int o = 0;
+        stages_off = o; o += S * stage_bytes;
+        full_off = o;   o += 8 * S;
+        empty_off = o;  o += 8 * S;
+        rfull_off = o;  o += 8 * RB;
+        rempty_off = o; o += 8 * RB;
+        o = up(o, 128);
+        // one record buffer: x [HPI][KM][P] bf16, B [KM][N] bf16, C [T][N] bf16, dt [HPI][KM] f32
+        rx_off = 0;
+        rB_off = up(HPI * KM * P * 2, 16);
+        rC_off = rB_off + up(KM * N * 2, 16);
+        rdt_off = rC_off + up(T * N * 2, 16);
+        rec_bytes = up(rdt_off + HPI * KM * 4, 128);
+        rec_off = o;   o += RB * rec_bytes;
+        meta_off = o;  o += up(MY * 8, 16);                 // [items of this CTA][head, len]
+        // per-item arrays, double-buffered (two consumer barriers per item)
+        cb_off = o;    o += up(2 * T * KM * 4, 16);         // [2][T][KM]     B_j . C_i
+        w_off = o;     o += up(2 * HPI * T * KM * 4, 16);   // [2][HPI][T][KM] query weights
+        decay_off = o; o += up(2 * HPI * T * 4, 16);        // [2][HPI][T]    exp(A S_i)
+        wf_off = o;    o += up(2 * HPI * KM * 4, 16);       // [2][HPI][KM]   fold weights
+        fdec_off = o;  o += up(2 * HPI * 4, 16);            // [2][HPI]       fold decay
+        rt_off = o;    o += up(2 * HPI * T * P * 4, 16);    // [2][HPI][T][P] record terms
+        wx_off = o;    o += up(KM * P * 4, 16);             // [KM][P] fold coefficients (rows owned per warp)
+        ad_off = o;    o += up(2 * H * 4, 16);              // A[H], D[H]
+        flag_off = o;  o += 16;
+        total = o;
+    }
+};
+
+template <int N, int P, int VPT, int HPI>
+__global__ void __launch_bounds__(persist_threads(P * N / 4 / VPT), 1)
+m2_verify_persistent(const M2Args a, const PersistCfg pc) {
+    constexpr int NC = P * N / 4 / VPT;                  // consumer threads
+    constexpr int G4 = N / 4;                            // lanes per row
+    constexpr int RSTEP = NC / G4;                       // rows between a thread's consecutive float4s
+    constexpr int CX = P / 8, CB = N / 8;                // 16-byte chunks per x / B row
+    constexpr int TQ = 4;                                // draft slots in registers (T <= 4)
+    static_assert(G4 == 32, "a warp owns whole rows");
+    static_assert(HPI * TQ == 32 && TQ * VPT == 32, "one (head, draft) pair per lane");
+    extern __shared__ __align__(128) unsigned char smraw[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int L = a.L, H = a.H, G = a.G, hpg = a.hpg, T = a.T, KM = L + T;
+    const int S = pc.stages, RB = pc.recbufs;
+    const VSmem lay(P, N, L, T, HPI, S, RB, H, pc.max_my);
+    unsigned char *stages = smraw + lay.stages_off;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smraw + lay.full_off);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + lay.empty_off);
+    uint64_t *rfull = reinterpret_cast<uint64_t *>(smraw + lay.rfull_off);
+    uint64_t *rempty = reinterpret_cast<uint64_t *>(smraw + lay.rempty_off);
+    int *s_meta = reinterpret_cast<int *>(smraw + lay.meta_off);
+    float *s_cb = reinterpret_cast<float *>(smraw + lay.cb_off);
+    float *s_w = reinterpret_cast<float *>(smraw + lay.w_off);
+    float *s_decay = reinterpret_cast<float *>(smraw + lay.decay_off);
+    float *s_wf = reinterpret_cast<float *>(smraw + lay.wf_off);
+    float *s_fdec = reinterpret_cast<float *>(smraw + lay.fdec_off);
+    float *s_rt = reinterpret_cast<float *>(smraw + lay.rt_off);
+    float *s_wx = reinterpret_cast<float *>(smraw + lay.wx_off);
+    float *s_A = reinterpret_cast<float *>(smraw + lay.ad_off), *s_D = s_A + H;
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smraw + lay.flag_off);
+
+    const int grid = gridDim.x;
+    const int n_my = (pc.items - (int)blockIdx.x + grid - 1) / grid;
+    auto item_of = [&](int k) { return (int)blockIdx.x + k * grid; };
+    auto item_b = [&](int it) { return it / (G * pc.nchunk); };      // item = (b * G + g) * nchunk + c
+    auto item_h0 = [&](int it) {
+        const int bg = it / pc.nchunk, c = it - bg * pc.nchunk;
+        return (bg % G) * hpg + c * HPI;
+    };
+    auto meta_bad = [&](int hd, int ln) { return hd < 0 || hd >= L || ln < 0 || ln > L; };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, NC);
+        }
+        for (int r = 0; r < RB; ++r) {
+            mbar_init(rfull + r, 33);                    // 32 cp.async arrivals + lane 0's release
+            mbar_init(rempty + r, NC);
+        }
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    for (int i = tid; i < H; i += blockDim.x) {
+        s_A[i] = a.A[i];
+        s_D[i] = a.D[i];
+    }
+    // ring pointers of every item, read once; the sequence's last arrival commits
+    // the verify's pointers (pre-flush when the drafts would overflow the ring)
+    for (int k = tid; k < n_my; k += blockDim.x) {
+        const int it = item_of(k), b = item_b(it);
+        const int hd = __ldcg(a.ring_head + b), ln = __ldcg(a.ring_len + b);
+        s_meta[k * 2 + 0] = hd;
+        s_meta[k * 2 + 1] = ln;
+        if (meta_bad(hd, ln) && item_h0(it) == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
+        __threadfence();
+        if (atomicAdd(a.arrive + b, 1) == pc.arrivals - 1) {
+            __threadfence();
+            if (!meta_bad(hd, ln)) {
+                const bool pre = ln + T > L;
+                a.ring_head[b] = pre ? (hd + ln) % L : hd;
+                a.ring_len[b] = (pre ? 0 : ln) + T;
+            }
+            a.arrive[b] = 0;
+        }
+    }
+    __syncthreads();                                     // the only CTA-wide barrier
+    if (n_my <= 0) return;
+
+    if (warp == 0) {
+        // ================================= tile warp ==================================
+        if (lane != 0) return;
+        const uint64_t pol = l2_evict_first_policy();
+        bool ok = true;
+        int issued = 0;
+        for (int k = 0; k < n_my && ok; ++k) {
+            const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
+            for (int hh = 0; hh < HPI; ++hh) {
+                const int t = k * HPI + hh, s = t % S;
+                if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort);
+                if (!ok) break;
+                const size_t tile = ((size_t)b * H + h0 + hh) * P;
+                mbar_arrive_expect_tx(full + s, P * N * 4);
+                bulk_g2s(stages + s * lay.stage_bytes, a.ckpt + tile * N, P * N * 4, full + s, pol);
+                issued = t + 1;
+            }
+        }
+        if (!ok) {
+            *s_abort = 1;
+            flag_error(a.err, RSSM_DEVERR_TIMEOUT);
+            for (int u = issued - S < 0 ? 0 : issued - S; u < issued; ++u)
+                mbar_wait(full + (u % S), (uint32_t)((u / S) & 1));
+        }
+        return;
+    }
+
+    if (warp == 1) {
+        // ================================ record warp =================================
+        // list position j < len: ring slot (hd + j) mod L; j = len + i: draft i
+        const uint16_t *rx = static_cast<const uint16_t *>(a.rec_x);
+        const uint16_t *rB = static_cast<const uint16_t *>(a.rec_B);
+        const uint16_t *ix = static_cast<const uint16_t *>(a.x);
+        const uint16_t *iB = static_cast<const uint16_t *>(a.Bin);
+        const uint16_t *iC = static_cast<const uint16_t *>(a.Cin);
+        bool ok = true;
+        for (int k = 0; k < n_my; ++k) {
+            const int r = k % RB;
+            if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const int it = item_of(k), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
+            const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+            if (!meta_bad(hd, ln)) {
+                unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
+                const int nrec = ln + T;
+                for (int row = lane / CX; row < HPI * nrec; row += 32 / CX) {
+                    const int hh = row / nrec, j = row - hh * nrec, c = lane % CX;
+                    const size_t bh = (size_t)b * H + h0 + hh;
+                    const uint16_t *src = j < ln ? rx + ((bh * L + (hd + j) % L) * P + c * 8)
+                                                 : ix + ((((size_t)b * T + (j - ln)) * H + h0 + hh) * P + c * 8);
+                    cp_async16(rb + lay.rx_off + ((hh * KM + j) * P + c * 8) * 2, src);
+                }
+                for (int idx = lane; idx < nrec * CB; idx += 32) {
+                    const int j = idx / CB, c = idx - j * CB;
+                    const uint16_t *src = j < ln ? rB + ((((size_t)b * G + g) * L + (hd + j) % L) * N + c * 8)
+                                                 : iB + ((((size_t)b * T + (j - ln)) * G + g) * N + c * 8);
+                    cp_async16(rb + lay.rB_off + (j * N + c * 8) * 2, src);
+                }
+                for (int idx = lane; idx < T * CB; idx += 32) {
+                    const int i = idx / CB, c = idx - i * CB;
+                    cp_async16(rb + lay.rC_off + (i * N + c * 8) * 2, iC + ((((size_t)b * T + i) * G + g) * N + c * 8));
+                }
+                for (int idx = lane; idx < HPI * nrec; idx += 32) {
+                    const int hh = idx / nrec, j = idx - hh * nrec;
+                    const size_t bh = (size_t)b * H + h0 + hh;
+                    cp_async4(rb + lay.rdt_off + (hh * KM + j) * 4,
+                              j < ln ? a.rec_dt + bh * L + (hd + j) % L : a.dt + ((size_t)b * T + (j - ln)) * H + h0 + hh);
+                }
+            }
+            cp_async_arrive_noinc(rfull + r);
+            if (lane == 0) mbar_arrive(rfull + r);
+        }
+        cp_async_wait_all();
+        if (!ok && lane == 0) {
+            *s_abort = 1;
+            flag_error(a.err, RSSM_DEVERR_TIMEOUT);
+        }
+        return;
+    }
+
+    // ================================ consumer warps =================================
+    const int ctid = tid - 64;                           // 0..NC-1
+    const int cw = ctid >> 5;                            // consumer warp: owns rows cw + RSTEP * v
+    const int col4 = lane;                               // this lane's 4 columns
+    bool live = true;
+
+    // Preparation of item kk (all consumers): wait for its records; after every
+    // warp is past item kk-2 (barrier 1) fill the double-buffered item arrays:
+    // draft appends (x, dt), B_j . C_i, query weights and decays, fold weights on a
+    // pre-flush; after barrier 2, the record terms of the rows each warp owns.
+    auto prep_item = [&](int kk) {
+        const int r = kk % RB, pb = kk & 1;
+        const int it = item_of(kk), b = item_b(it), h0 = item_h0(it);
+        if (live && !pwait(rfull + r, (uint32_t)((kk / RB) & 1), s_abort)) {
+            live = false;
+            *s_abort = 1;
+        }
+        const int hd = s_meta[kk * 2 + 0], ln = s_meta[kk * 2 + 1];
+        const bool work = live && !meta_bad(hd, ln);
+        const bool pre = ln + T > L;
+        const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
+        const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
+        const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
+        const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
+        const float *r_dt = reinterpret_cast<const float *>(rb + lay.rdt_off);
+        float *cb = s_cb + pb * T * KM, *w = s_w + pb * HPI * T * KM, *dec = s_decay + pb * HPI * T;
+        float *wf = s_wf + pb * HPI * KM, *fdec = s_fdec + pb * HPI, *rt = s_rt + pb * HPI * T * P;
+        consumer_sync<NC>();                             // every warp is done with item kk-2's arrays
+        if (work) {
+            // drafts' x and dt rows into the ring (per head, read by no other CTA)
+            const int hd2 = pre ? (hd + ln) % L : hd, ln2 = pre ? 0 : ln;
+            for (int idx = ctid; idx < HPI * T * CX + HPI * T; idx += NC) {
+                if (idx < HPI * T * CX) {
+                    const int hh = idx / (T * CX), rr = idx - hh * T * CX, i = rr / CX, c = rr - i * CX;
+                    const size_t bh = (size_t)b * H + h0 + hh;
+                    const int slot = (hd2 + ln2 + i) % L;
+                    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.rec_x) + (bh * L + slot) * P + c * 8) =
+                        *reinterpret_cast<const uint4 *>(r_x + (hh * KM + ln + i) * P + c * 8);
+                } else {
+                    const int rr = idx - HPI * T * CX, hh = rr / T, i = rr - hh * T;
+                    const size_t bh = (size_t)b * H + h0 + hh;
+                    a.rec_dt[bh * L + (hd2 + ln2 + i) % L] = r_dt[hh * KM + ln + i];
+                }
+            }
+            // B_j . C_i for every draft i and record j <= len + i, one warp per pair
+            for (int pr = cw; pr < T * KM; pr += NC / 32) {
+                const int i = pr / KM, j = pr - i * KM;
+                if (j > ln + i) continue;
+                float acc = 0.0f;
+#pragma unroll
+                for (int n = lane; n < N; n += 32) acc = fmaf(bf16_at(r_B, j * N + n), bf16_at(r_C, i * N + n), acc);
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (lane == 0) cb[i * KM + j] = acc;
+            }
+            // query weights exp(A sum(dt after j, up to len+i)) dt_j and decays exp(A S_i)
+            for (int idx = ctid; idx < HPI * T * KM; idx += NC) {
+                const int hh = idx / (T * KM), rr = idx - hh * T * KM, i = rr / KM, j = rr - i * KM;
+                const float *dth = r_dt + hh * KM;
+                if (j <= ln + i) w[idx] = expf(s_A[h0 + hh] * suffix_sum(dth, j, ln + i)) * dth[j];
+            }
+            for (int idx = ctid; idx < HPI * T; idx += NC) {
+                const int hh = idx / T, i = idx - hh * T;
+                dec[idx] = expf(s_A[h0 + hh] * suffix_sum(r_dt + hh * KM, -1, ln + i));
+            }
+            if (pre) {
+                // fold weights over the buffered records only, the flush's arithmetic
+                for (int idx = ctid; idx < HPI * (ln + 1); idx += NC) {
+                    const int hh = idx / (ln + 1), j = idx - hh * (ln + 1);
+                    const float *dth = r_dt + hh * KM;
+                    if (j < ln) wf[hh * KM + j] = expf(s_A[h0 + hh] * suffix_sum(dth, j, ln - 1)) * dth[j];
+                    else fdec[hh] = expf(s_A[h0 + hh] * suffix_sum(dth, -1, ln - 1));
+                }
+            }
+        }
+        consumer_sync<NC>();                             // cb, w, dec, wf of item kk
+        if (work) {
+            // record terms of this warp's rows: lane = (head hh, draft i)
+            const int hh = lane / TQ, i = lane % TQ;
+            if (i < T) {
+                const float *wh = w + (hh * T + i) * KM, *ci = cb + i * KM;
+                const uint16_t *xh = r_x + hh * KM * P;
+                float acc[VPT];
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) acc[v] = 0.0f;
+                for (int j = 0; j <= ln + i; ++j) {
+                    const float c = wh[j] * ci[j];
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) acc[v] = fmaf(c, bf16_at(xh, j * P + cw + RSTEP * v), acc[v]);
+                }
+                const float dh = s_D[h0 + hh];
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) {
+                    const int row = cw + RSTEP * v;
+                    rt[(hh * T + i) * P + row] = fmaf(dh, bf16_at(xh, (ln + i) * P + row), acc[v]);
+                }
+            }
+        }
+        __syncwarp();
+    };
+
+    prep_item(0);
+    for (int k = 0; k < n_my; ++k) {
+        const int r = k % RB, pb = k & 1;
+        const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
+        const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+        const bool work = live && !meta_bad(hd, ln);
+        const bool pre = work && (ln + T > L);
+        const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
+        const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
+        const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
+        const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
+        const float *dec = s_decay + pb * HPI * T, *rt = s_rt + pb * HPI * T * P;
+        const float *wf = s_wf + pb * HPI * KM, *fdec = s_fdec + pb * HPI;
+        float4 cfr[TQ];
+#pragma unroll
+        for (int i = 0; i < TQ; ++i)
+            cfr[i] = i < T ? make_float4(bf16_at(r_C, i * N + col4 * 4 + 0), bf16_at(r_C, i * N + col4 * 4 + 1),
+                                         bf16_at(r_C, i * N + col4 * 4 + 2), bf16_at(r_C, i * N + col4 * 4 + 3))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int hh = 0; hh < HPI; ++hh) {
+            const int t = k * HPI + hh, s = t % S;
+            if (live && !pwait(full + s, (uint32_t)((t / S) & 1), s_abort)) {
+                live = false;
+                *s_abort = 1;
+            }
+            const float4 *stg = reinterpret_cast<const float4 *>(stages + s * lay.stage_bytes);
+            float4 hv[VPT];
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) hv[v] = stg[ctid + v * NC];
+            mbar_arrive(empty + s);                      // this thread is done with the stage
+            if (hh == 0 && k + 1 < n_my) prep_item(k + 1);   // overlaps the tiles in flight
+            if (!work) continue;
+            const int h = h0 + hh;
+            const size_t tile = ((size_t)b * H + h) * P;
+            // T x 8 row dot products reduced across the warp: lane ends with (draft, row)
+            float part[TQ * VPT];
+#pragma unroll
+            for (int i = 0; i < TQ; ++i) {
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) {
+                    float d = hv[v].x * cfr[i].x;
+                    d = fmaf(hv[v].y, cfr[i].y, d);
+                    d = fmaf(hv[v].z, cfr[i].z, d);
+                    d = fmaf(hv[v].w, cfr[i].w, d);
+                    part[i * VPT + v] = d;
+                }
+            }
+            group_reduce<G4, TQ * VPT>(part);
+            {
+                const int vi = reduced_index<G4, TQ * VPT>(0);
+                const int i = vi / VPT, row = cw + RSTEP * (vi - i * VPT);
+                if (i < T)
+                    a.y[(((size_t)b * T + i) * H + h) * P + row] =
+                        fmaf(dec[hh * T + i], part[0], rt[(hh * T + i) * P + row]);
+            }
+            if (pre) {
+                // fold the buffered records into this warp's rows (the flush's arithmetic)
+                const float *wh = wf + hh * KM;
+                const uint16_t *xh = r_x + hh * KM * P;
+                for (int idx = lane; idx < ln * VPT; idx += 32) {
+                    const int j = idx / VPT, v = idx - j * VPT, row = cw + RSTEP * v;
+                    s_wx[j * P + row] = wh[j] * bf16_at(xh, j * P + row);
+                }
+                __syncwarp();
+                unsigned long long acc01[VPT], acc23[VPT];
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) acc01[v] = acc23[v] = 0ull;
+                for (int j = 0; j < ln; ++j) {
+                    const uint2 braw = *reinterpret_cast<const uint2 *>(r_B + j * N + col4 * 4);
+                    const unsigned long long b01 = f2pack(bf16lo(braw.x), bf16hi(braw.x));
+                    const unsigned long long b23 = f2pack(bf16lo(braw.y), bf16hi(braw.y));
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) {
+                        const float c = s_wx[j * P + cw + RSTEP * v];
+                        const unsigned long long cc = f2pack(c, c);
+                        acc01[v] = fma2(cc, b01, acc01[v]);
+                        acc23[v] = fma2(cc, b23, acc23[v]);
+                    }
+                }
+                const unsigned long long dd = f2pack(fdec[hh], fdec[hh]);
+                float4 *ckp = reinterpret_cast<float4 *>(a.ckpt + tile * N);
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) {
+                    const int row = cw + RSTEP * v;
+                    float4 o;
+                    f2unpack(fma2(dd, f2pack(hv[v].x, hv[v].y), acc01[v]), o.x, o.y);
+                    f2unpack(fma2(dd, f2pack(hv[v].z, hv[v].w), acc23[v]), o.z, o.w);
+                    st_stream(ckp + ctid + v * NC, o);
+                    if (a.read_copy) {
+                        float m = fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w)));
+                        m = group_max<G4>(m);
+                        float scale, inv;
+                        e4m3_row_scale(m, scale, inv);
+                        reinterpret_cast<uint32_t *>(a.ckpt_q + tile * N)[ctid + v * NC] =
+                            e4m3_pack4(__fmul_rn(o.x, inv), __fmul_rn(o.y, inv), __fmul_rn(o.z, inv),
+                                       __fmul_rn(o.w, inv));
+                        if (lane == 0) a.ckpt_scale[tile + row] = scale;
+                    }
+                }
+                __syncwarp();                            // s_wx is rewritten for the next head
+            }
+        }
+        mbar_arrive(rempty + r);                         // record buffer r may be refilled
+    }
+    if (ctid == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
+}
+
+// After the verify kernel: the drafts' B and C rows (shared by the heads of a
+// group) go to the last T slots of each sequence's ring, whose pointers the
+// verify kernel has already committed.
+__global__ void verify_bc_epilogue(const M2Args a) {
+    const int b = blockIdx.x;
+    const int hd = a.ring_head[b], ln = a.ring_len[b], L = a.L, T = a.T, G = a.G, N = a.N;
+    if (hd < 0 || hd >= L || ln < T || ln > L) return;
+    const int CB = N / 8;
+    const int total = 2 * T * G * CB;
+    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+        const bool isC = idx >= T * G * CB;
+        const int rr = isC ? idx - T * G * CB : idx;
+        const int i = rr / (G * CB), r2 = rr - i * G * CB, g = r2 / CB, c = r2 - g * CB;
+        uint16_t *dst = static_cast<uint16_t *>(isC ? a.rec_C : a.rec_B);
+        if (dst == nullptr) continue;
+        const uint16_t *src = static_cast<const uint16_t *>(isC ? a.Cin : a.Bin);
+        const int slot = (hd + ln - T + i) % L;
+        *reinterpret_cast<uint4 *>(dst + ((((size_t)b * G + g) * L + slot) * N + c * 8)) =
+            __ldcg(reinterpret_cast<const uint4 *>(src + ((((size_t)b * T + i) * G + g) * N + c * 8)));
+    }
+}
+
+}  // namespace rssm

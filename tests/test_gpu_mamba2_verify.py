@@ -216,3 +216,60 @@ def test_snapshot_slot_bounds_and_select():
     assert slot.cpu().tolist() == [3, 1, 1] and err.item() == 0
     rs.conventional_select(slot, 4, torch.tensor([5, 0, -1], dtype=torch.int32, device="cuda"), err)
     assert slot.cpu().tolist() == [3, 1, 1] and err.item() == rs.DEVERR_ROLLBACK
+
+
+@pytest.mark.parametrize("T,L", [(1, 8), (3, 8), (4, 8), (4, 16)])
+def test_persistent_verify_variants(T, L):
+    """Serving head shape at batch 128 (the persistent verify): 1-4 drafts, rings
+    of 8 (pre-flush every couple of steps) and 16; outputs against the oracle,
+    ring pointers of all sequences and the live records bit-exact."""
+    shape = gen.Mamba2Shape(batch=128, nheads=128, headdim=64, dstate=128, ngroups=8, L=L)
+    h0 = gen.mamba2_random_state(shape, 500 + T)
+    v = VerifyRun(shape, 500 + T, T, h0=h0, sample=[0, 77, 127], conventional=False)
+    del h0
+    for t in range(14):
+        v.verify_step(t, gen.accepted_counts(shape.batch, T, 500 + T, t))
+        if t % 4 == 3:
+            v.r.check_records(seqs=[0, 77, 127])
+
+
+def test_persistent_mixed_decode_verify():
+    """Persistent decode and persistent verify on the same cache, interleaved,
+    including decodes that meet a ring a verify left full."""
+    shape = gen.Mamba2Shape(batch=128, nheads=128, headdim=64, dstate=128, ngroups=8, L=8)
+    h0 = gen.mamba2_random_state(shape, 612)
+    v = VerifyRun(shape, 612, 4, h0=h0, sample=[5, 120], conventional=False)
+    del h0
+    rng = np.random.default_rng(3)
+    for t in range(30):
+        if t % 3 == 1:
+            acc = rng.integers(0, 5, size=shape.batch).astype(np.int32)
+            acc[::7] = 4
+            v.verify_step(40_000 + t, acc)
+        else:
+            v.r.decode(50_000 + t)
+        if t % 5 == 0:
+            v.r.check_records(seqs=[5, 120])
+
+
+def test_persistent_verify_fp8_copy_preflush():
+    """With an FP8 read copy, a pre-flushing verify rebuilds the copy of the new
+    checkpoint (every code within half an E4M3 step of the FP32 value)."""
+    from tests.m2_runner import M2Run
+    shape = gen.Mamba2Shape(batch=128, nheads=128, headdim=64, dstate=128, ngroups=8, L=4)
+    h0 = gen.mamba2_random_state(shape, 71)
+    r = M2Run(shape, 71, h0=h0, read_copy=1, sample=[9], conventional=False)
+    del h0
+    v = VerifyRun.__new__(VerifyRun)
+    from ssm_decode_state_gb300 import replayssm as rs
+    v.rs, v.r, v.T, v.shape, v.pool = rs, r, 3, shape, None
+    for t in range(4):
+        v.verify_step(t, gen.accepted_counts(shape.batch, 3, 71, t))
+    ck = r.cache.ckpt[:8].cpu().numpy().astype(np.float64)
+    sc = r.cache.ckpt_scale[:8].cpu().numpy().astype(np.float64)
+    codes = r.cache.ckpt_q[:8].cpu().numpy()
+    sign = np.where(codes & 0x80, -1.0, 1.0)
+    e, m = (codes >> 3) & 0xF, codes & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e.astype(np.float64) - 7))
+    dq = sign * mag * sc[..., None]
+    assert np.all(np.abs(dq - ck) <= 2.0 ** -4 * np.abs(ck) + 2.0 ** -10 * sc[..., None] + 1e-6 * np.abs(ck))

@@ -45,8 +45,9 @@ __device__ __forceinline__ void unpack_chunk(uint4 c, bool bf16, float *out) {
 // partner.  On return:
 //   V <= G: v[0] holds the group sum of value index (lane % G) / (G / V);
 //   V >  G: v[i] (i < V/G) holds the group sum of value (lane % G) * (V/G) + i.
-template <int O, int C, int V>
+template <int O, int C, int V, bool kMax = false>
 struct GroupReduce {
+    static __device__ __forceinline__ float op(float a, float b) { return kMax ? fmaxf(a, b) : a + b; }
     static __device__ __forceinline__ void run(float (&v)[V], int lane) {
         if constexpr (O >= 1) {
             if constexpr (C > 1) {
@@ -55,12 +56,12 @@ struct GroupReduce {
                 for (int i = 0; i < C / 2; ++i) {
                     const float send = up ? v[i] : v[i + C / 2];
                     const float keep = up ? v[i + C / 2] : v[i];
-                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+                    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, O));
                 }
-                GroupReduce<O / 2, C / 2, V>::run(v, lane);
+                GroupReduce<O / 2, C / 2, V, kMax>::run(v, lane);
             } else {
-                v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-                GroupReduce<O / 2, 1, V>::run(v, lane);
+                v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], O));
+                GroupReduce<O / 2, 1, V, kMax>::run(v, lane);
             }
         }
     }
@@ -69,6 +70,12 @@ struct GroupReduce {
 template <int G, int V>
 __device__ __forceinline__ void group_reduce(float (&v)[V]) {
     GroupReduce<G / 2, V, V>::run(v, threadIdx.x & 31);
+}
+
+// The same exchange pattern with max instead of sum (same result placement).
+template <int G, int V>
+__device__ __forceinline__ void group_reduce_max(float (&v)[V]) {
+    GroupReduce<G / 2, V, V, true>::run(v, threadIdx.x & 31);
 }
 
 // Value index of v[i] after group_reduce<G, V>, and whether this lane is the
@@ -126,6 +133,31 @@ __device__ __forceinline__ float4 e4m3_unpack4(uint32_t w) {
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// Four E4M3 codes (byte i = column i) as two pairs of bfloat16 values, even
+// columns (0, 2) and odd columns (1, 3), each 2^-120 times the code's value:
+// the code's exponent and mantissa bits become the low exponent bits and the
+// top mantissa bits of a bfloat16 (normal codes read as normal bfloat16 with
+// the bias 120 too large, subnormal codes as bfloat16 subnormals with the same
+// offset), integer operations only.  Never given NaN codes (the encoder
+// saturates to the largest finite value).
+__device__ __forceinline__ void e4m3_to_bf16_pairs(uint32_t w, uint32_t &even, uint32_t &odd) {
+    even = ((w & 0x007f007fu) << 4) | ((w << 8) & 0x80008000u);
+    odd = ((w & 0x7f007f00u) >> 4) | (w & 0x80008000u);
+}
+
+// acc + a.lo * c.lo + a.hi * c.hi: bfloat16 pairs, products exact, FP32
+// accumulation (mixed-precision fma of sm_100 and later).
+__device__ __forceinline__ float fma_bf16_pair(uint32_t a, uint32_t c, float acc) {
+    asm("{ .reg .b16 al, ah, cl, ch;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {cl, ch}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, cl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, ah, ch, %0; }"
+        : "+f"(acc)
+        : "r"(a), "r"(c));
+    return acc;
+}
+
 // Per-row read-copy scale: scale = amax/448 and inv = 448/amax, each one
 // correctly rounded float32 division; a zero row (or one whose inverse
 // overflows) is stored as zero codes with scale 1.
@@ -138,6 +170,29 @@ __device__ __forceinline__ void e4m3_row_scale(float amax, float &scale, float &
     }
 }
 
+// Read-copy codes of V rows held by one warp, 32 lanes per row (lane i holds
+// columns 4i..4i+3 of every row).  The row maxima go through one transposed
+// exchange, each lane derives scale and inverse for the row it ends up with
+// (row (lane / (32/V))), and the inverses are broadcast back: two divisions
+// per lane instead of two per row per lane.  Codes and scales are the same
+// as per-row e4m3_row_scale + e4m3_pack4.  On return q[v] holds this lane's
+// four codes of row v and row_scale the scale of row (lane / (32/V)).
+template <int V>
+__device__ __forceinline__ void e4m3_quantize_rows(const float4 (&o)[V], uint32_t (&q)[V], float &row_scale) {
+    static_assert(V <= 32 && (V & (V - 1)) == 0, "rows per warp");
+    float m[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) m[v] = fmaxf(fmaxf(fabsf(o[v].x), fabsf(o[v].y)), fmaxf(fabsf(o[v].z), fabsf(o[v].w)));
+    group_reduce_max<32, V>(m);
+    float inv;
+    e4m3_row_scale(m[0], row_scale, inv);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const float iv = __shfl_sync(0xffffffffu, inv, v * (32 / V));
+        q[v] = e4m3_pack4(__fmul_rn(o[v].x, iv), __fmul_rn(o[v].y, iv), __fmul_rn(o[v].z, iv), __fmul_rn(o[v].w, iv));
+    }
+}
+
 // ------------------------------------------------------------------ the ring
 
 // Sum of dt[j+1 .. e] accumulated from the newest record backwards (j = -1:
@@ -145,6 +200,7 @@ __device__ __forceinline__ void e4m3_row_scale(float amax, float &scale, float &
 // one order, so fused and standalone flushes agree bit for bit.
 __device__ __forceinline__ float suffix_sum(const float *dt, int j, int e) {
     float s = 0.0f;
+#pragma unroll 4
     for (int m = e; m > j; --m) s += dt[m];
     return s;
 }
@@ -194,6 +250,14 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// The same copy with the default L2 policy (for data that is read again soon).
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -213,11 +277,14 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Wait for phase `parity` of an mbarrier, giving up after ~2 s (returns
 // false); a copy that never lands must not hang the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t it = 0; it < (1u << 26); ++it) {
+    uint64_t t0 = 0;                                   // the clock is read only in long waits
+    for (uint32_t it = 1; it <= (1u << 26); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && global_ns() - t0 > 2000000000ull) return false;
+        if ((it & 255u) == 0) {
+            const uint64_t now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > 2000000000ull) return false;
+        }
     }
     return false;
 }

@@ -58,7 +58,7 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
     if (s != RSSM_OK) return s;
     M2Args a = args;
     void *params[] = {&a, &pc};
-    const int threads = persist_threads(64 * 128 / 4 / VPT);
+    const int threads = persist_decode_threads(64 * 128 / 4 / VPT);
     if (cudaLaunchKernel(k, dim3(grid), dim3(threads), params, smem, st) != cudaSuccess) return RSSM_ERR_CUDA;
     return launch_status();
 }

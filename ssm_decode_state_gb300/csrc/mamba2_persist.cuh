@@ -2,34 +2,30 @@
 // serving-shape path: headdim 64, dstate 128, bf16 token inputs).
 //
 // One CTA per SM walks a static list of work items; an item is HPI heads of
-// one group of one sequence.  The CTA has two producer warps and eight
-// consumer warps that never meet at a CTA-wide barrier:
+// one group of one sequence.  At kernel start every thread block reads the
+// ring pointers of all its items (and the last reader of a sequence commits
+// the new ones); after that the warps never meet at a CTA-wide barrier:
 //
-//  * record warp (warp 1): for each item in order, lane 0 reads the ring
-//    pointers of the item's sequence, publishes them on the item's "meta"
-//    mbarrier and arrives on that sequence's counter; all 32 lanes copy the
-//    item's records (x of its heads, dt, the group's B, the current C) into a
-//    ring of record buffers with cp.async, whose completion lands on the
-//    buffer's "full" mbarrier.  It runs up to RB items ahead of the consumers.
-//  * tile warp (warp 0, one lane): streams the checkpoint of each head (P x N
-//    floats, or its FP8 read copy on non-flush steps) into an S-stage ring of
-//    shared-memory tiles with one-dimensional bulk copies (the TMA engine),
-//    each completing on the stage's "full" mbarrier as transaction bytes.  It
-//    waits only for a stage to be freed (or, once per item, for the item's
-//    ring pointers), so the stages are refilled as soon as they drain.
-//  * consumer warps (warps 2..9): per item, B_j . C_t and the decay weights
-//    (one named barrier among the consumers), then the record term of the
-//    rows each warp owns; per head tile, each warp reads its own 8 rows, frees
-//    the stage, reduces the row dot products with C_t across its lanes and
-//    writes y = exp(A S) (h_c . C_t) + record term directly; on flush steps it
-//    folds h_c <- exp(A S) h_c + sum_j w_j x_j B_j^T into its rows and stores
-//    them (and the FP8 copy).  At the end of the item it appends the token's
-//    records and frees the record buffer.
+//  * tile warp (warp 0, one lane): streams the checkpoint into an S-stage ring
+//    of shared-memory buffers with one-dimensional bulk copies (the TMA
+//    engine), completing on the stage's "full" mbarrier as transaction bytes:
+//    one FP32 head tile (P x N) per stage, or on non-flush steps of a cache
+//    with a read copy the FP8 codes and row scales of Q8 heads per stage.
+//  * record warp (warp 1): copies each item's records (the used ring slots of
+//    x and B are at most two contiguous runs each, plus the current token's x,
+//    B and C, by bulk copy; dt words by cp.async) into a ring of RB record
+//    buffers, RB items ahead of the consumers.
+//  * preparation warps (warps 2 + NC/32 and up): per item, ahead of the
+//    consumers, append the token to the ring, B_j . C_t, the decay weights and
+//    the record term of every row, into triple-buffered item arrays handed
+//    over through mbarriers.
+//  * consumer warps (warps 2..): per stage, each warp reads its own rows,
+//    frees the stage, reduces the row dot products with C_t across its lanes
+//    and writes y = exp(A S) (h_c . C_t) + record term; on flush steps it folds
+//    h_c <- exp(A S) h_c + sum_j w_j x_j B_j^T into its rows and stores them
+//    (and the FP8 copy).
 //
 // Every wait is bounded (~2 s, then RSSM_DEVERR_TIMEOUT and an orderly exit).
-// The CTA that sees the last arrival of a sequence commits its ring pointers;
-// an item can never see a committed value, because the commit needs its own
-// arrival, which happens right after its read.
 #pragma once
 
 #include "mamba2_replay.cuh"
@@ -47,23 +43,33 @@ struct PersistCfg {
 
 // Threads of a CTA: NC consumers + the tile warp and the record warp.
 constexpr int persist_threads(int nc) { return nc + 64; }
+// The decode kernel adds two item-preparation warps after the consumers.
+constexpr int kPrepThreads = 64;
+constexpr int persist_decode_threads(int nc) { return nc + 64 + kPrepThreads; }
 
 // Byte layout of the persistent kernel's shared memory.
+// Heads whose FP8 codes share one stage (one wait, one release).
+__host__ __device__ constexpr int persist_q8(int hpi) { return hpi >= 4 ? 4 : hpi; }
+
 struct PSmem {
     int stage_bytes, stages_off;
     int full_off, empty_off, rfull_off, rempty_off;
     int rec_off, rx_off, rB_off, rC_off, rdt_off, rec_bytes;
     int meta_off, cb_off, w_off, decay_off, rt_off, wx_off, ad_off, flag_off, total;
+    int pfull_off, pempty_off, wcb_off, sfx_off;
     __host__ __device__ PSmem(int P, int N, int L, int HPI, int S, int RB, int H, int MY) {
         const int KM = L + 1;
         auto up = [](int v, int a) { return (v + a - 1) / a * a; };
-        stage_bytes = P * N * 4;
+        // one FP32 tile, or the codes and row scales of persist_q8(HPI) heads
+        stage_bytes = P * N * 4 > persist_q8(HPI) * (P * N + P * 4) ? P * N * 4 : persist_q8(HPI) * (P * N + P * 4);
         int o = 0;
         stages_off = o; o += S * stage_bytes;
         full_off = o;   o += 8 * S;
         empty_off = o;  o += 8 * S;
         rfull_off = o;  o += 8 * RB;
         rempty_off = o; o += 8 * RB;
+        pfull_off = o;  o += 8 * 3;
+        pempty_off = o; o += 8 * 3;
         o = up(o, 128);
         // one record buffer: x [HPI][KM][P] bf16, B [KM][N] bf16, C [N] bf16, dt [HPI][KM] f32
         rx_off = 0;
@@ -78,6 +84,8 @@ struct PSmem {
         decay_off = o; o += up(3 * HPI * 4, 16);            // [3][HPI]
         rt_off = o;    o += up(3 * HPI * P * 4, 16);        // [3][HPI][P] (rows owned per warp)
         wx_off = o;    o += up(KM * P * 4, 16);             // [KM][P]  (rows owned per warp)
+        wcb_off = o;   o += up(3 * HPI * KM * 4, 16);       // [3][HPI][KM]  w_j (B_j . C_t)
+        sfx_off = o;   o += up(HPI * (KM + 1) * 4, 16);     // [HPI][KM + 1] suffix sums (prep only)
         ad_off = o;    o += up(2 * H * 4, 16);              // A[H], D[H]
         flag_off = o;  o += 16;
         total = o;
@@ -100,6 +108,9 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
 }
 
+// Named barrier among the item-preparation warps only.
+__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kPrepThreads) : "memory"); }
+
 // Packed pair of float32 (one 64-bit register) and the sm_100+ two-wide fma:
 // each lane of the pair is an ordinary fused multiply-add, rounded once.
 __device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
@@ -119,25 +130,29 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
 
 // Bounded wait that also gives up as soon as another warp has aborted.
 __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t it = 0; it < (1u << 26); ++it) {
+    // The clock is read only once a wait has polled 256 times: reading it is
+    // slow, and short waits sit on the path that hands a stage to the consumers.
+    uint64_t t0 = 0;
+    for (uint32_t it = 1; it <= (1u << 26); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if ((it & 255u) == 0) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > 2000000000ull) return false;
+            const uint64_t now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > 2000000000ull) return false;
         }
     }
     return false;
 }
 
 template <int N, int P, int VPT, int HPI>
-__global__ void __launch_bounds__(persist_threads(P * N / 4 / VPT), 1)
+__global__ void __launch_bounds__(persist_decode_threads(P * N / 4 / VPT), 1)
 m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     constexpr int kPConsumers = P * N / 4 / VPT;         // consumer threads
     constexpr int G4 = N / 4;                            // lanes per row
     constexpr int RSTEP = kPConsumers / G4;              // rows between a thread's consecutive float4s
     constexpr int CX = P / 8, CB = N / 8;                // 16-byte chunks per x / B row
+    constexpr int Q8 = persist_q8(HPI);                  // heads per stage of FP8 codes
     static_assert(G4 == 32, "a warp owns whole rows");
     extern __shared__ __align__(128) unsigned char smraw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -157,6 +172,10 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     float *s_wx = reinterpret_cast<float *>(smraw + lay.wx_off);
     float *s_A = reinterpret_cast<float *>(smraw + lay.ad_off), *s_D = s_A + H;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smraw + lay.flag_off);
+    uint64_t *pfull = reinterpret_cast<uint64_t *>(smraw + lay.pfull_off);
+    uint64_t *pempty = reinterpret_cast<uint64_t *>(smraw + lay.pempty_off);
+    float *s_wcb = reinterpret_cast<float *>(smraw + lay.wcb_off);
+    float *s_sfx = reinterpret_cast<float *>(smraw + lay.sfx_off);
 
     const int grid = gridDim.x;
     const int n_my = (pc.items - (int)blockIdx.x + grid - 1) / grid;
@@ -168,15 +187,22 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         return (bg % G) * hpg + c * HPI;
     };
     auto meta_bad = [&](int hd, int ln) { return hd < 0 || hd >= L || ln < 0 || ln > L; };
+    // a non-flush item of a cache with a read copy streams the FP8 codes, Q8 heads
+    // per stage; every other item streams FP32 tiles, one head per stage
+    auto fp8_item = [&](int hd, int ln) { return q8 && !meta_bad(hd, ln) && ln + 1 < L; };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, kPConsumers);
+            mbar_init(empty + s, kPConsumers / 32);       // one arrival per consumer warp
         }
         for (int r = 0; r < RB; ++r) {
             mbar_init(rfull + r, 33);                    // 32 cp.async arrivals + lane 0's release
-            mbar_init(rempty + r, kPConsumers);
+            mbar_init(rempty + r, kPConsumers / 32);
+        }
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(pfull + i, kPrepThreads / 32);     // one arrival per preparation warp
+            mbar_init(pempty + i, kPConsumers / 32);
         }
         *s_abort = 0;
         fence_mbar_init();
@@ -214,24 +240,27 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         if (lane != 0) return;
         const uint64_t pol = l2_evict_first_policy();
         bool ok = true;
-        int issued = 0;
+        int issued = 0;                                  // stage units issued so far
         for (int k = 0; k < n_my && ok; ++k) {
             const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
-            const bool fp32_tile = meta_bad(hd, ln) || !q8 || (ln + 1 >= L);
+            const bool f8 = fp8_item(hd, ln);
             const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
-            for (int hh = 0; hh < HPI; ++hh) {
-                const int t = k * HPI + hh, s = t % S;
+            const int nu = f8 ? HPI / Q8 : HPI;
+            for (int uu = 0; uu < nu; ++uu) {
+                const int t = issued, s = t % S;
                 if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort);
                 if (!ok) break;
                 unsigned char *dst = stages + s * lay.stage_bytes;
-                const size_t tile = ((size_t)b * H + h0 + hh) * P;
-                if (fp32_tile) {
+                if (!f8) {
+                    const size_t tile = ((size_t)b * H + h0 + uu) * P;
                     mbar_arrive_expect_tx(full + s, P * N * 4);
                     bulk_g2s(dst, a.ckpt + tile * N, P * N * 4, full + s, pol);
                 } else {
-                    mbar_arrive_expect_tx(full + s, P * N + P * 4);
-                    bulk_g2s(dst, a.ckpt_q + tile * N, P * N, full + s, pol);
-                    bulk_g2s(dst + P * N, a.ckpt_scale + tile, P * 4, full + s, pol);
+                    // Q8 consecutive heads: their codes, then their row scales
+                    const size_t tile = ((size_t)b * H + h0 + uu * Q8) * P;
+                    mbar_arrive_expect_tx(full + s, Q8 * (P * N + P * 4));
+                    bulk_g2s(dst, a.ckpt_q + tile * N, Q8 * P * N, full + s, pol);
+                    bulk_g2s(dst + Q8 * P * N, a.ckpt_scale + tile, Q8 * P * 4, full + s, pol);
                 }
                 issued = t + 1;
             }
@@ -254,47 +283,198 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         const uint16_t *iB = static_cast<const uint16_t *>(a.Bin);
         const uint16_t *iC = static_cast<const uint16_t *>(a.Cin);
         bool ok = true;
-        for (int k = 0; k < n_my; ++k) {
+        int k = 0;
+        for (; k < n_my; ++k) {
             const int r = k % RB;
             if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const int it = item_of(k), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
             const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
-            if (!meta_bad(hd, ln)) {
-                // records: list position j < ln is ring slot (hd + j) mod L, j = ln the current token
+            const bool good = !meta_bad(hd, ln);
+            if (good) {
+                // records: list position j < ln is ring slot (hd + j) mod L, j = ln the current
+                // token.  The used slots of a ring are at most two contiguous runs, copied
+                // whole (x and B rows) by the TMA engine; dt words go by cp.async.
                 unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
                 const int nrec = ln + 1;
-                for (int row = lane / CX; row < HPI * nrec; row += 32 / CX) {
-                    const int hh = row / nrec, j = row - hh * nrec, c = lane % CX;
-                    const size_t bh = (size_t)b * H + h0 + hh;
-                    const uint16_t *src = j < ln ? rx + ((bh * L + (hd + j) % L) * P + c * 8) : ix + (bh * P + c * 8);
-                    cp_async16(rb + lay.rx_off + ((hh * KM + j) * P + c * 8) * 2, src);
+                const int run1 = ln < L - hd ? ln : L - hd, run2 = ln - run1;
+                if (lane == 0) mbar_arrive_expect_tx(rfull + r, (uint32_t)((HPI * nrec * P + nrec * N + N) * 2));
+                __syncwarp();
+                if (lane < HPI) {
+                    const size_t bh = (size_t)b * H + h0 + lane;
+                    unsigned char *dx = rb + lay.rx_off + lane * KM * P * 2;
+                    if (run1) bulk_g2s(dx, rx + (bh * L + hd) * P, run1 * P * 2, rfull + r);
+                    if (run2) bulk_g2s(dx + run1 * P * 2, rx + bh * L * P, run2 * P * 2, rfull + r);
+                    bulk_g2s(dx + ln * P * 2, ix + bh * P, P * 2, rfull + r);
+                } else if (lane == HPI) {
+                    const size_t bg = (size_t)b * G + g;
+                    unsigned char *dB = rb + lay.rB_off;
+                    if (run1) bulk_g2s(dB, rB + (bg * L + hd) * N, run1 * N * 2, rfull + r);
+                    if (run2) bulk_g2s(dB + run1 * N * 2, rB + bg * L * N, run2 * N * 2, rfull + r);
+                    bulk_g2s(dB + ln * N * 2, iB + bg * N, N * 2, rfull + r);
+                } else if (lane == HPI + 1) {
+                    bulk_g2s(rb + lay.rC_off, iC + ((size_t)b * G + g) * N, N * 2, rfull + r);
                 }
-                for (int idx = lane; idx < nrec * CB; idx += 32) {
-                    const int j = idx / CB, c = idx - j * CB;
-                    const uint16_t *src = j < ln ? rB + ((((size_t)b * G + g) * L + (hd + j) % L) * N + c * 8)
-                                                 : iB + (((size_t)b * G + g) * N + c * 8);
-                    cp_async16(rb + lay.rB_off + (j * N + c * 8) * 2, src);
-                }
-                if (lane < CB) cp_async16(rb + lay.rC_off + lane * 16, iC + (((size_t)b * G + g) * N + lane * 8));
                 for (int idx = lane; idx < HPI * nrec; idx += 32) {
                     const int hh = idx / nrec, j = idx - hh * nrec;
                     const size_t bh = (size_t)b * H + h0 + hh;
-                    cp_async4(rb + lay.rdt_off + (hh * KM + j) * 4, j < ln ? a.rec_dt + bh * L + (hd + j) % L : a.dt + bh);
+                    const int slot = hd + j < L ? hd + j : hd + j - L;
+                    cp_async4(rb + lay.rdt_off + (hh * KM + j) * 4, j < ln ? a.rec_dt + bh * L + slot : a.dt + bh);
                 }
             }
             cp_async_arrive_noinc(rfull + r);
-            if (lane == 0) mbar_arrive(rfull + r);
+            if (lane == 0 && !good) mbar_arrive(rfull + r);   // with good metadata lane 0 arrived above
         }
         cp_async_wait_all();
-        if (!ok) {
-            if (lane == 0) {
-                *s_abort = 1;
-                flag_error(a.err, RSSM_DEVERR_TIMEOUT);
-            }
-            return;
+        // the record copies of the last items may still be in flight: the CTA must
+        // not end before they land (bounded waits; the consumers normally saw them)
+        if (lane == 0)
+            for (int kk = k - RB < 0 ? 0 : k - RB; kk < k; ++kk) mbar_wait(rfull + kk % RB, (uint32_t)((kk / RB) & 1));
+        if (!ok && lane == 0) {
+            *s_abort = 1;
+            flag_error(a.err, RSSM_DEVERR_TIMEOUT);
         }
+        return;
+    }
+
+    if (warp >= 2 + kPConsumers / 32) {
+        // ============================ item-preparation warps ============================
+        // Per item, ahead of the consumers: append the token to the ring, B_j . C_t,
+        // the decay weights, and the record term of every row of every head.  Item
+        // arrays are triple-buffered (ia = item % 3); pempty says the consumers are
+        // done with a buffer, pfull hands a prepared one over.
+        const int ptid = tid - 64 - kPConsumers, pw = ptid >> 5;
+        bool live = true;
+        for (int kk = 0; kk < n_my; ++kk) {
+            const int r = kk % RB, ia = kk % 3;
+            const int it = item_of(kk), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
+            if (live && kk >= 3 && !pwait(pempty + ia, (uint32_t)(((kk / 3) - 1) & 1), s_abort)) {
+                live = false;
+                *s_abort = 1;
+            }
+            if (live && !pwait(rfull + r, (uint32_t)((kk / RB) & 1), s_abort)) {
+                live = false;
+                *s_abort = 1;
+            }
+            const int hd = s_meta[kk * 2 + 0], ln = s_meta[kk * 2 + 1];
+            const bool work = live && !meta_bad(hd, ln);
+            const int nrec = ln + 1;
+            const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
+            const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
+            const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
+            const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
+            const float *r_dt = reinterpret_cast<const float *>(rb + lay.rdt_off);
+            float *cb = s_cb + ia * KM, *w = s_w + ia * HPI * KM, *wcb = s_wcb + ia * HPI * KM;
+            float *dec = s_decay + ia * HPI, *rt = s_rt + ia * HPI * P;
+            if (work && ln + 1 < L) {
+                // a non-flush step appends the token to the ring, slot (hd + ln) mod L, which
+                // no one reads during this launch; the token is already in the record buffer
+                const int slot = hd + ln < L ? hd + ln : hd + ln - L;
+                const int nBC = (h0 % hpg == 0) ? 2 * CB : 0;   // the group's first chunk writes B and C
+                for (int idx = ptid; idx < HPI * CX + nBC + HPI; idx += kPrepThreads) {
+                    if (idx < HPI * CX) {
+                        const int hh = idx / CX, c = idx - hh * CX;
+                        const size_t bh = (size_t)b * H + h0 + hh;
+                        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.rec_x) + (bh * L + slot) * P + c * 8) =
+                            *reinterpret_cast<const uint4 *>(r_x + (hh * KM + ln) * P + c * 8);
+                    } else if (idx < HPI * CX + nBC) {
+                        const int rr = idx - HPI * CX;
+                        const bool isC = rr >= CB;
+                        const int c = isC ? rr - CB : rr;
+                        uint16_t *dst = static_cast<uint16_t *>(isC ? a.rec_C : a.rec_B);
+                        if (dst != nullptr)
+                            *reinterpret_cast<uint4 *>(dst + ((((size_t)b * G + g) * L + slot) * N + c * 8)) =
+                                *reinterpret_cast<const uint4 *>(isC ? r_C + c * 8 : r_B + ln * N + c * 8);
+                    } else {
+                        const int hh = idx - HPI * CX - nBC;
+                        a.rec_dt[((size_t)b * H + h0 + hh) * L + slot] = r_dt[hh * KM + ln];
+                    }
+                }
+            }
+            if (work) {
+                // suffix sums of dt per head, newest first (suffix_sum's order): one pass
+                // per head gives every S_j and the total
+                if (ptid < HPI) {
+                    const float *dth = r_dt + ptid * KM;
+                    float *sf = s_sfx + ptid * (KM + 1);
+                    float acc = 0.0f;
+                    for (int j = ln; j >= 0; --j) {
+                        sf[j] = acc;
+                        acc += dth[j];
+                    }
+                    sf[KM] = acc;
+                }
+                // B_j . C_t, a warp per record (lane-strided products, butterfly sum),
+                // four records at a time per warp
+                for (int jb = pw * 4; jb < nrec; jb += 8) {
+                    float acc[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[q] = 0.0f;
+                        const int j = jb + q < nrec ? jb + q : 0;
+#pragma unroll
+                        for (int n = lane; n < N; n += 32) acc[q] = fmaf(bf16_at(r_B, j * N + n), bf16_at(r_C, n), acc[q]);
+                    }
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+                    }
+                    if (lane < 4 && jb + lane < nrec) {
+                        float v = acc[0];
+#pragma unroll
+                        for (int q = 1; q < 4; ++q) v = lane == q ? acc[q] : v;
+                        cb[jb + lane] = v;
+                    }
+                }
+            }
+            prep_sync();                                 // S_j and B_j . C_t
+            if (work) {
+                // w_j = exp(A S_j) dt_j, w_j (B_j . C_t), and exp(A S) per head
+                for (int idx = ptid; idx < HPI * nrec; idx += kPrepThreads) {
+                    const int hh = idx / nrec, j = idx - hh * nrec;
+                    const float wv = expf(s_A[h0 + hh] * s_sfx[hh * (KM + 1) + j]) * r_dt[hh * KM + j];
+                    w[hh * KM + j] = wv;
+                    wcb[hh * KM + j] = wv * cb[j];
+                }
+                if (ptid < HPI) dec[ptid] = expf(s_A[h0 + ptid] * s_sfx[ptid * (KM + 1) + KM]);
+            }
+            prep_sync();                                 // w, w (B . C)
+            if (work) {
+                // record term of every row: 8 consecutive rows of one head per thread
+                for (int o = ptid; o < HPI * P / 8; o += kPrepThreads) {
+                    const int hh = o / (P / 8), r0 = (o - hh * (P / 8)) * 8;
+                    const uint16_t *xh = r_x + hh * KM * P + r0;
+                    const float *wc = wcb + hh * KM;
+                    float acc[8];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) acc[v] = 0.0f;
+                    for (int j = 0; j < nrec; ++j) {
+                        const float c = wc[j];
+                        const uint4 xr = *reinterpret_cast<const uint4 *>(xh + j * P);
+                        acc[0] = fmaf(c, bf16lo(xr.x), acc[0]);
+                        acc[1] = fmaf(c, bf16hi(xr.x), acc[1]);
+                        acc[2] = fmaf(c, bf16lo(xr.y), acc[2]);
+                        acc[3] = fmaf(c, bf16hi(xr.y), acc[3]);
+                        acc[4] = fmaf(c, bf16lo(xr.z), acc[4]);
+                        acc[5] = fmaf(c, bf16hi(xr.z), acc[5]);
+                        acc[6] = fmaf(c, bf16lo(xr.w), acc[6]);
+                        acc[7] = fmaf(c, bf16hi(xr.w), acc[7]);
+                    }
+                    const uint4 xl = *reinterpret_cast<const uint4 *>(xh + ln * P);
+                    const float Dh = s_D[h0 + hh];
+                    float4 *dst = reinterpret_cast<float4 *>(rt + hh * P + r0);
+                    dst[0] = make_float4(fmaf(Dh, bf16lo(xl.x), acc[0]), fmaf(Dh, bf16hi(xl.x), acc[1]),
+                                         fmaf(Dh, bf16lo(xl.y), acc[2]), fmaf(Dh, bf16hi(xl.y), acc[3]));
+                    dst[1] = make_float4(fmaf(Dh, bf16lo(xl.z), acc[4]), fmaf(Dh, bf16hi(xl.z), acc[5]),
+                                         fmaf(Dh, bf16lo(xl.w), acc[6]), fmaf(Dh, bf16hi(xl.w), acc[7]));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pfull + ia);      // item kk is prepared
+        }
+        if (ptid == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
         return;
     }
 
@@ -304,91 +484,20 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     const int col4 = lane;                               // this lane's 4 columns
     bool live = true;                                    // false once any wait gave up
 
-    // Item preparation, done by all consumers: wait for the item's records, append
-    // its token to the ring (non-flush steps), B_j . C_t, the decay weights and
-    // exp(A S) per head, then the record term of the rows each warp owns.  The
-    // item arrays are triple-buffered: item kk+1 is prepared right after the
-    // first tile of item kk, while the next tiles are still in flight.
-    auto prep_item = [&](int kk) {
-        const int r = kk % RB, ia = kk % 3;
-        const int it = item_of(kk), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
-        if (live && !pwait(rfull + r, (uint32_t)((kk / RB) & 1), s_abort)) {
-            live = false;
-            *s_abort = 1;
-        }
-        const int hd = s_meta[kk * 2 + 0], ln = s_meta[kk * 2 + 1];
-        const bool work = live && !meta_bad(hd, ln);
-        const int nrec = ln + 1;
-        const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
-        const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
-        const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
-        const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
-        const float *r_dt = reinterpret_cast<const float *>(rb + lay.rdt_off);
-        float *cb = s_cb + ia * KM, *w = s_w + ia * HPI * KM, *dec = s_decay + ia * HPI;
-        if (work && ln + 1 < L) {
-            // a non-flush step appends the token to the ring, slot (hd + ln) mod L, which
-            // no one reads during this launch; the token is already in the record buffer
-            const int slot = (hd + ln) % L;
-            const int nBC = (h0 % hpg == 0) ? 2 * CB : 0;   // the group's first chunk writes B and C
-            for (int idx = ctid; idx < HPI * CX + nBC + HPI; idx += kPConsumers) {
-                if (idx < HPI * CX) {
-                    const int hh = idx / CX, c = idx - hh * CX;
-                    const size_t bh = (size_t)b * H + h0 + hh;
-                    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.rec_x) + (bh * L + slot) * P + c * 8) =
-                        *reinterpret_cast<const uint4 *>(r_x + (hh * KM + ln) * P + c * 8);
-                } else if (idx < HPI * CX + nBC) {
-                    const int rr = idx - HPI * CX;
-                    const bool isC = rr >= CB;
-                    const int c = isC ? rr - CB : rr;
-                    uint16_t *dst = static_cast<uint16_t *>(isC ? a.rec_C : a.rec_B);
-                    if (dst != nullptr)
-                        *reinterpret_cast<uint4 *>(dst + ((((size_t)b * G + g) * L + slot) * N + c * 8)) =
-                            *reinterpret_cast<const uint4 *>(isC ? r_C + c * 8 : r_B + ln * N + c * 8);
-                } else {
-                    const int hh = idx - HPI * CX - nBC;
-                    a.rec_dt[((size_t)b * H + h0 + hh) * L + slot] = r_dt[hh * KM + ln];
-                }
-            }
-        }
-        if (work) {
-            // B_j . C_t, one warp per record
-            for (int j = cw; j < nrec; j += kPConsumers / 32) {
-                float acc = 0.0f;
-#pragma unroll
-                for (int n = lane; n < N; n += 32) acc = fmaf(bf16_at(r_B, j * N + n), bf16_at(r_C, n), acc);
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (lane == 0) cb[j] = acc;
-            }
-            // decay weights per head: w_j = exp(A sum(dt after j)) dt_j, and exp(A S)
-            for (int idx = ctid; idx < HPI * KM; idx += kPConsumers) {
-                const int hh = idx / KM, j = idx - hh * KM;
-                const float *dth = r_dt + hh * KM;
-                if (j < nrec) w[idx] = expf(s_A[h0 + hh] * suffix_sum(dth, j, ln)) * dth[j];
-            }
-            if (ctid < HPI) dec[ctid] = expf(s_A[h0 + ctid] * suffix_sum(r_dt + ctid * KM, -1, ln));
-        }
-        consumer_sync<kPConsumers>();                    // cb, w, dec of item kk
-        if (work) {
-            // record term of the rows this warp owns, for every head of the item
-            float *rt = s_rt + ia * HPI * P;
-            for (int idx = lane; idx < HPI * VPT; idx += 32) {
-                const int hh = idx / VPT, v = idx - hh * VPT, row = cw + RSTEP * v;
-                const float *wh = w + hh * KM;
-                const uint16_t *xh = r_x + hh * KM * P;
-                float acc = 0.0f;
-                for (int j = 0; j < nrec; ++j) acc = fmaf(wh[j] * cb[j], bf16_at(xh, j * P + row), acc);
-                rt[hh * P + row] = fmaf(s_D[h0 + hh], bf16_at(xh, ln * P + row), acc);
-            }
-        }
-        __syncwarp();
-    };
-
-    prep_item(0);
+    int u = 0;                                           // stage units consumed so far
     for (int k = 0; k < n_my; ++k) {
         const int r = k % RB, ia = k % 3;
         const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
         const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+        // the item's records and its prepared arrays
+        if (live && !pwait(pfull + ia, (uint32_t)((k / 3) & 1), s_abort)) {
+            live = false;
+            *s_abort = 1;
+        }
+        if (live && !pwait(rfull + r, (uint32_t)((k / RB) & 1), s_abort)) {
+            live = false;
+            *s_abort = 1;
+        }
         const bool work = live && !meta_bad(hd, ln);
         const bool fold = work && (ln + 1 >= L);
         const int nrec = ln + 1;
@@ -399,41 +508,9 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         const float *w = s_w + ia * HPI * KM, *dec = s_decay + ia * HPI, *rt = s_rt + ia * HPI * P;
         const float4 cfr = make_float4(bf16_at(r_C, col4 * 4 + 0), bf16_at(r_C, col4 * 4 + 1),
                                        bf16_at(r_C, col4 * 4 + 2), bf16_at(r_C, col4 * 4 + 3));
-        for (int hh = 0; hh < HPI; ++hh) {
-            const int t = k * HPI + hh, s = t % S;
-            if (live && !pwait(full + s, (uint32_t)((t / S) & 1), s_abort)) {
-                live = false;
-                *s_abort = 1;
-            }
-            const unsigned char *stg = stages + s * lay.stage_bytes;
-            float4 hv[VPT];
-            if (q8 && work && !fold) {
-                const uint32_t *q = reinterpret_cast<const uint32_t *>(stg);
-                const float *sc = reinterpret_cast<const float *>(stg + P * N);
-#pragma unroll
-                for (int v = 0; v < VPT; ++v) {
-                    const float4 d = e4m3_unpack4(q[ctid + v * kPConsumers]);
-                    const float sv = sc[cw + RSTEP * v];
-                    hv[v] = make_float4(d.x * sv, d.y * sv, d.z * sv, d.w * sv);
-                }
-            } else {
-#pragma unroll
-                for (int v = 0; v < VPT; ++v) hv[v] = reinterpret_cast<const float4 *>(stg)[ctid + v * kPConsumers];
-            }
-            mbar_arrive(empty + s);                      // this thread is done with the stage
-            if (hh == 0 && k + 1 < n_my) prep_item(k + 1);   // overlaps the tiles in flight
-            if (!work) continue;
-            const int h = h0 + hh;
-            const size_t tile = ((size_t)b * H + h) * P;
-            if (fold) {
-                const float *wh = w + hh * KM;
-                const uint16_t *xh = r_x + hh * KM * P;
-                for (int idx = lane; idx < nrec * VPT; idx += 32) {
-                    const int j = idx / VPT, v = idx - j * VPT, row = cw + RSTEP * v;
-                    s_wx[j * P + row] = wh[j] * bf16_at(xh, j * P + row);
-                }
-                __syncwarp();
-            }
+        // y of head hh from its FP32 tile: h_c . C_t (rows reduced across the warp),
+        // decayed, plus the record term
+        auto head_y = [&](int hh, const float4 (&hv)[VPT]) {
             float part[VPT];
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
@@ -446,51 +523,125 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             group_reduce<G4, VPT>(part);
             if (reduced_writer<G4, VPT>()) {
                 const int row = cw + RSTEP * reduced_index<G4, VPT>(0);
-                a.y[tile + row] = fmaf(dec[hh], part[0], rt[hh * P + row]);
+                a.y[((size_t)b * H + h0 + hh) * P + row] = fmaf(dec[hh], part[0], rt[hh * P + row]);
             }
-            if (fold) {
-                // rank-nrec update first (each B_j loaded once per lane), then the
-                // decayed checkpoint in one fma: the state is rounded once per flush
-                unsigned long long acc01[VPT], acc23[VPT];      // packed (x, y) and (z, w)
+        };
+        if (fp8_item(hd, ln)) {
+            // C_t of this lane's columns as bfloat16 pairs (0, 2) and (1, 3)
+            const uint2 craw = *reinterpret_cast<const uint2 *>(r_C + col4 * 4);
+            const uint32_t ce = __byte_perm(craw.x, craw.y, 0x5410), co = __byte_perm(craw.x, craw.y, 0x7632);
+            // FP8 codes, Q8 heads per stage: take every code and scale this thread
+            // needs, release the stage, then decode and reduce head by head
+            for (int uu = 0; uu < HPI / Q8; ++uu, ++u) {
+                const int s = u % S;
+                if (live && !pwait(full + s, (uint32_t)((u / S) & 1), s_abort)) {
+                    live = false;
+                    *s_abort = 1;
+                }
+                const unsigned char *stg = stages + s * lay.stage_bytes;
+                const uint32_t *q = reinterpret_cast<const uint32_t *>(stg);
+                const float *sc = reinterpret_cast<const float *>(stg + Q8 * P * N);
+                uint32_t qc[Q8][VPT];
+                float rsc[Q8];
 #pragma unroll
-                for (int v = 0; v < VPT; ++v) acc01[v] = acc23[v] = 0ull;
-                for (int j = 0; j < nrec; ++j) {
-                    const uint2 braw = *reinterpret_cast<const uint2 *>(r_B + j * N + col4 * 4);
-                    const unsigned long long b01 = f2pack(bf16lo(braw.x), bf16hi(braw.x));
-                    const unsigned long long b23 = f2pack(bf16lo(braw.y), bf16hi(braw.y));
+                for (int hq = 0; hq < Q8; ++hq) {
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) qc[hq][v] = q[hq * (P * N / 4) + ctid + v * kPConsumers];
+                    rsc[hq] = sc[hq * P + cw + RSTEP * reduced_index<G4, VPT>(0)];
+                }
+                __syncwarp();                            // the warp is done with the stage
+                if (lane == 0) mbar_arrive(empty + s);
+                if (!work) continue;
+#pragma unroll
+                for (int hq = 0; hq < Q8; ++hq) {
+                    // codes enter the dot at 2^-120 of their value; the row sum is scaled
+                    // back (exactly) and by the row scale after the warp reduction
+                    float part[VPT];
 #pragma unroll
                     for (int v = 0; v < VPT; ++v) {
-                        const float c = s_wx[j * P + cw + RSTEP * v];
-                        const unsigned long long cc = f2pack(c, c);
-                        acc01[v] = fma2(cc, b01, acc01[v]);
-                        acc23[v] = fma2(cc, b23, acc23[v]);
+                        uint32_t ev, od;
+                        e4m3_to_bf16_pairs(qc[hq][v], ev, od);
+                        part[v] = fma_bf16_pair(od, co, fma_bf16_pair(ev, ce, 0.0f));
+                    }
+                    group_reduce<G4, VPT>(part);
+                    if (reduced_writer<G4, VPT>()) {
+                        const int hh = uu * Q8 + hq, row = cw + RSTEP * reduced_index<G4, VPT>(0);
+                        a.y[((size_t)b * H + h0 + hh) * P + row] =
+                            fmaf(dec[hh], (part[0] * 0x1p120f) * rsc[hq], rt[hh * P + row]);
                     }
                 }
-                const float dk = dec[hh];
-                float4 *ckp = reinterpret_cast<float4 *>(a.ckpt + tile * N);
+            }
+        } else {
+            for (int hh = 0; hh < HPI; ++hh, ++u) {
+                const int s = u % S;
+                if (live && !pwait(full + s, (uint32_t)((u / S) & 1), s_abort)) {
+                    live = false;
+                    *s_abort = 1;
+                }
+                const float4 *stg = reinterpret_cast<const float4 *>(stages + s * lay.stage_bytes);
+                float4 hv[VPT];
 #pragma unroll
-                for (int v = 0; v < VPT; ++v) {
-                    const int row = cw + RSTEP * v;
-                    const unsigned long long dd = f2pack(dk, dk);
-                    float4 o;
-                    f2unpack(fma2(dd, f2pack(hv[v].x, hv[v].y), acc01[v]), o.x, o.y);
-                    f2unpack(fma2(dd, f2pack(hv[v].z, hv[v].w), acc23[v]), o.z, o.w);
-                    st_stream(ckp + ctid + v * kPConsumers, o);
-                    if (q8) {
-                        float m = fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w)));
-                        m = group_max<G4>(m);
-                        float scale, inv;
-                        e4m3_row_scale(m, scale, inv);
-                        reinterpret_cast<uint32_t *>(a.ckpt_q + tile * N)[ctid + v * kPConsumers] =
-                            e4m3_pack4(__fmul_rn(o.x, inv), __fmul_rn(o.y, inv), __fmul_rn(o.z, inv),
-                                       __fmul_rn(o.w, inv));
-                        if (lane == 0) a.ckpt_scale[tile + row] = scale;
+                for (int v = 0; v < VPT; ++v) hv[v] = stg[ctid + v * kPConsumers];
+                __syncwarp();                            // the warp is done with the stage
+                if (lane == 0) mbar_arrive(empty + s);
+                if (!work) continue;
+                const size_t tile = ((size_t)b * H + h0 + hh) * P;
+                if (fold) {
+                    const float *wh = w + hh * KM;
+                    const uint16_t *xh = r_x + hh * KM * P;
+                    for (int idx = lane; idx < nrec * VPT; idx += 32) {
+                        const int j = idx / VPT, v = idx - j * VPT, row = cw + RSTEP * v;
+                        s_wx[j * P + row] = wh[j] * bf16_at(xh, j * P + row);
                     }
+                    __syncwarp();
                 }
-                __syncwarp();                            // s_wx is rewritten for the next head
+                head_y(hh, hv);
+                if (fold) {
+                    // rank-nrec update first (each B_j loaded once per lane), then the
+                    // decayed checkpoint in one fma: the state is rounded once per flush
+                    unsigned long long acc01[VPT], acc23[VPT];      // packed (x, y) and (z, w)
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) acc01[v] = acc23[v] = 0ull;
+                    for (int j = 0; j < nrec; ++j) {
+                        const uint2 braw = *reinterpret_cast<const uint2 *>(r_B + j * N + col4 * 4);
+                        const unsigned long long b01 = f2pack(bf16lo(braw.x), bf16hi(braw.x));
+                        const unsigned long long b23 = f2pack(bf16lo(braw.y), bf16hi(braw.y));
+#pragma unroll
+                        for (int v = 0; v < VPT; ++v) {
+                            const float c = s_wx[j * P + cw + RSTEP * v];
+                            const unsigned long long cc = f2pack(c, c);
+                            acc01[v] = fma2(cc, b01, acc01[v]);
+                            acc23[v] = fma2(cc, b23, acc23[v]);
+                        }
+                    }
+                    const float dk = dec[hh];
+                    const unsigned long long dd = f2pack(dk, dk);
+                    float4 *ckp = reinterpret_cast<float4 *>(a.ckpt + tile * N);
+                    float4 o[VPT];
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) {
+                        f2unpack(fma2(dd, f2pack(hv[v].x, hv[v].y), acc01[v]), o[v].x, o[v].y);
+                        f2unpack(fma2(dd, f2pack(hv[v].z, hv[v].w), acc23[v]), o[v].z, o[v].w);
+                        st_stream(ckp + ctid + v * kPConsumers, o[v]);
+                    }
+                    if (q8) {
+                        uint32_t q[VPT];
+                        float rs;
+                        e4m3_quantize_rows<VPT>(o, q, rs);
+                        uint32_t *ckq = reinterpret_cast<uint32_t *>(a.ckpt_q + tile * N);
+#pragma unroll
+                        for (int v = 0; v < VPT; ++v) ckq[ctid + v * kPConsumers] = q[v];
+                        if (reduced_writer<32, VPT>()) a.ckpt_scale[tile + cw + RSTEP * reduced_index<32, VPT>(0)] = rs;
+                    }
+                    __syncwarp();                        // s_wx is rewritten for the next head
+                }
             }
         }
-        mbar_arrive(rempty + r);                         // record buffer r may be refilled
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(rempty + r);                     // record buffer r may be refilled
+            mbar_arrive(pempty + ia);                    // and the item arrays ia
+        }
     }
     if (ctid == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
 }

@@ -108,11 +108,11 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, NC);
+            mbar_init(empty + s, NC / 32);       // one arrival per consumer warp
         }
         for (int r = 0; r < RB; ++r) {
             mbar_init(rfull + r, 33);                    // 32 cp.async arrivals + lane 0's release
-            mbar_init(rempty + r, NC);
+            mbar_init(rempty + r, NC / 32);
         }
         *s_abort = 0;
         fence_mbar_init();
@@ -354,7 +354,8 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             float4 hv[VPT];
 #pragma unroll
             for (int v = 0; v < VPT; ++v) hv[v] = stg[ctid + v * NC];
-            mbar_arrive(empty + s);                      // this thread is done with the stage
+            __syncwarp();                                // the warp is done with the stage
+            if (lane == 0) mbar_arrive(empty + s);
             if (hh == 0 && k + 1 < n_my) prep_item(k + 1);   // overlaps the tiles in flight
             if (!work) continue;
             const int h = h0 + hh;
@@ -406,28 +407,27 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
                 }
                 const unsigned long long dd = f2pack(fdec[hh], fdec[hh]);
                 float4 *ckp = reinterpret_cast<float4 *>(a.ckpt + tile * N);
+                float4 o[VPT];
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
-                    const int row = cw + RSTEP * v;
-                    float4 o;
-                    f2unpack(fma2(dd, f2pack(hv[v].x, hv[v].y), acc01[v]), o.x, o.y);
-                    f2unpack(fma2(dd, f2pack(hv[v].z, hv[v].w), acc23[v]), o.z, o.w);
-                    st_stream(ckp + ctid + v * NC, o);
-                    if (a.read_copy) {
-                        float m = fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w)));
-                        m = group_max<G4>(m);
-                        float scale, inv;
-                        e4m3_row_scale(m, scale, inv);
-                        reinterpret_cast<uint32_t *>(a.ckpt_q + tile * N)[ctid + v * NC] =
-                            e4m3_pack4(__fmul_rn(o.x, inv), __fmul_rn(o.y, inv), __fmul_rn(o.z, inv),
-                                       __fmul_rn(o.w, inv));
-                        if (lane == 0) a.ckpt_scale[tile + row] = scale;
-                    }
+                    f2unpack(fma2(dd, f2pack(hv[v].x, hv[v].y), acc01[v]), o[v].x, o[v].y);
+                    f2unpack(fma2(dd, f2pack(hv[v].z, hv[v].w), acc23[v]), o[v].z, o[v].w);
+                    st_stream(ckp + ctid + v * NC, o[v]);
+                }
+                if (a.read_copy) {
+                    uint32_t q[VPT];
+                    float rs;
+                    e4m3_quantize_rows<VPT>(o, q, rs);
+                    uint32_t *ckq = reinterpret_cast<uint32_t *>(a.ckpt_q + tile * N);
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) ckq[ctid + v * NC] = q[v];
+                    if (reduced_writer<32, VPT>()) a.ckpt_scale[tile + cw + RSTEP * reduced_index<32, VPT>(0)] = rs;
                 }
                 __syncwarp();                            // s_wx is rewritten for the next head
             }
         }
-        mbar_arrive(rempty + r);                         // record buffer r may be refilled
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rempty + r);          // record buffer r may be refilled
     }
     if (ctid == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
 }

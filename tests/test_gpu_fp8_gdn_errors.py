@@ -241,3 +241,41 @@ def test_persistent_fp8_small_batch():
     dq = sign * mag * sc[..., None]
     bound = 2.0 ** -4 * np.abs(ck) + 2.0 ** -10 * sc[..., None] + 1e-6 * np.abs(ck)
     assert np.all(np.abs(dq - ck) <= bound)
+
+
+@pytest.mark.parametrize("batch", [64, 128])
+def test_persistent_fp8_decodes_every_code_exactly(batch):
+    """The FP8 read path decodes every finite E4M3 code exactly.  The copy is
+    written directly: row (b, h, p) column n holds code (row index + 3n) mod 256
+    (the two NaN codes replaced by 0), row scales are powers of two, C_t is
+    one-hot on a column per (b, g), x_t = 0 and dt = 0, so y must equal the
+    code's value times the row scale bit for bit (batch 64 takes 4 heads per
+    work item, one stage per item; 128 takes 8 heads, two stages per item)."""
+    from oracle.fp8 import e4m3_decode
+    from ssm_decode_state_gb300 import replayssm as rs
+    Bt, H, P, N, G, L = batch, 128, 64, 128, 8, 16
+    dims = rs.mamba2_dims(Bt, H, P, N, G, L, read_copy=1)
+    cache = rs.mamba2_cache(dims, torch.full((H,), -0.5), torch.zeros(H))
+    rows = np.arange(Bt * H * P, dtype=np.int64).reshape(Bt, H, P, 1)
+    codes = ((rows + 3 * np.arange(N).reshape(1, 1, 1, N)) % 256).astype(np.uint8)
+    codes[(codes == 0x7F) | (codes == 0xFF)] = 0
+    scale = (2.0 ** ((np.arange(P) % 7) - 3)).astype(np.float32)
+    scale = np.broadcast_to(scale, (Bt, H, P)).copy()
+    cache.ckpt_q.copy_(torch.from_numpy(codes))
+    cache.ckpt_scale.copy_(torch.from_numpy(scale))
+    n0 = (np.arange(Bt).reshape(Bt, 1) * 5 + np.arange(G).reshape(1, G) * 11) % N      # [b, g]
+    C = np.zeros((Bt, G, N), np.float32)
+    C[np.arange(Bt)[:, None], np.arange(G)[None, :], n0] = 1.0
+    rng = np.random.default_rng(5)
+    Bm = rng.standard_normal((Bt, G, N)).astype(np.float32)
+    dt = torch.zeros(Bt, H, device="cuda")
+    x = torch.zeros(Bt, H, P, dtype=torch.bfloat16, device="cuda")
+    y = rs.decode(cache, dt, x, to_dev(Bm, torch.bfloat16), to_dev(C, torch.bfloat16))
+    torch.cuda.synchronize()
+    assert int(cache.err.item()) == 0
+    g_of_h = np.arange(H) // (H // G)
+    col = n0[:, g_of_h]                                                      # [b, h]
+    picked = np.take_along_axis(codes, col[:, :, None, None].repeat(P, axis=2), axis=3)[..., 0]
+    expect = e4m3_decode(picked) * scale
+    assert len(np.unique(picked)) == 254
+    np.testing.assert_array_equal(y.cpu().numpy().astype(np.float64), expect)

@@ -1,0 +1,395 @@
+// Persistent, warp-specialised replay decode of the gated delta rule at the
+// serving head shape (dk = dv = 128, bf16 token inputs), with the fused flush.
+//
+// One CTA per SM walks a static list of work items, one (sequence, head)
+// each; its dv x dk FP32 state streams through shared memory as two stages
+// of 64 rows.  The ring pointers of every item are read (and committed by the
+// last reader of each sequence) at kernel start; after that:
+//
+//  * tile warp (warp 0, one lane): bulk copies (TMA engine) of the state,
+//    one 64-row half per stage, into an S-stage ring.
+//  * record warp (warp 1): per item, the used ring slots of k and v (at most
+//    two contiguous runs each) and the token's q, k, v by bulk copy, alpha
+//    and beta by cp.async, into a ring of RB record buffers.
+//  * preparation warps (two, after the consumers), alternate items, ahead of
+//    the consumers: append the token to the ring; run the backward chain
+//    u = q, d_j = k_j . u, u <- alpha_j (u - beta_j d_j k_j) (newest record
+//    first), which leaves u_0 and the record term sum_j beta_j d_j v_j[r] of
+//    every row, into item buffers handed over through mbarriers.
+//  * consumer warps (eight): per stage, each warp reads its own 8 rows, frees
+//    the stage, reduces the row dot products with u_0 across its lanes and
+//    writes o[r] = S_c[r] . u_0 + record term; on the flush step it folds the
+//    records into its rows, oldest first, s <- alpha_j s + beta_j (v_j[r] -
+//    alpha_j (s . k_j)) k_j (the arithmetic of the per-tile kernel), and
+//    stores them.
+//
+// Every wait is bounded (~2 s, then RSSM_DEVERR_TIMEOUT and an orderly exit).
+#pragma once
+
+#include "persist_common.cuh"
+
+namespace rssm {
+
+struct GPArgs {
+    int H, L, items, max_my, stages, recbufs;
+    float *ckpt;
+    uint16_t *rec_k, *rec_v;
+    float *rec_alpha, *rec_beta;
+    int32_t *ring_head, *ring_len, *arrive;
+    uint32_t *err;
+    const uint16_t *q, *k, *v;
+    const float *alpha, *beta;
+    float *o;
+};
+
+constexpr int kGdnRows = 64;     // state rows per stage
+constexpr int kGdnBufs = 4;      // prepared-item buffers
+
+// Byte layout of the kernel's shared memory.
+struct GPSmem {
+    int stage_bytes, stages_off, full_off, empty_off, rfull_off, rempty_off, pfull_off, pempty_off;
+    int rk_off, rv_off, rq_off, ral_off, rbe_off, rec_bytes, rec_off;
+    int meta_off, u_off, rt_off, flag_off, total;
+    __host__ __device__ GPSmem(int DK, int DV, int L, int S, int RB, int MY) {
+        const int KM = L + 1;
+        auto up = [](int v, int a) { return (v + a - 1) / a * a; };
+        stage_bytes = kGdnRows * DK * 4;
+        int o = 0;
+        stages_off = o; o += S * stage_bytes;
+        full_off = o;   o += 8 * S;
+        empty_off = o;  o += 8 * S;
+        rfull_off = o;  o += 8 * RB;
+        rempty_off = o; o += 8 * RB;
+        pfull_off = o;  o += 8 * kGdnBufs;
+        pempty_off = o; o += 8 * kGdnBufs;
+        o = up(o, 128);
+        // one record buffer: k [KM][DK] bf16, v [KM][DV] bf16, q [DK] bf16, alpha, beta [KM] f32
+        rk_off = 0;
+        rv_off = up(KM * DK * 2, 16);
+        rq_off = rv_off + up(KM * DV * 2, 16);
+        ral_off = rq_off + up(DK * 2, 16);
+        rbe_off = ral_off + up(KM * 4, 16);
+        rec_bytes = up(rbe_off + KM * 4, 128);
+        rec_off = o;  o += RB * rec_bytes;
+        meta_off = o; o += up(MY * 8, 16);                  // [items of this CTA][head, len]
+        u_off = o;    o += up(kGdnBufs * DK * 4, 16);       // u_0 per prepared item
+        rt_off = o;   o += up(kGdnBufs * DV * 4, 16);       // record term per prepared item
+        flag_off = o; o += 16;
+        total = o;
+    }
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persistent(const GPArgs a) {
+    constexpr int NC = 256, VPT = 8, G4 = DK / 4, RSTEP = NC / G4, NU = DV / kGdnRows;
+    static_assert(G4 == 32 && NC * VPT * 4 == kGdnRows * DK && DV % kGdnRows == 0, "serving shape");
+    constexpr int CK = DK / 8, CV = DV / 8;              // 16-byte chunks per k / v row
+    extern __shared__ __align__(128) unsigned char smraw[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int L = a.L, H = a.H, S = a.stages, RB = a.recbufs;
+    const GPSmem lay(DK, DV, L, S, RB, a.max_my);
+    unsigned char *stages = smraw + lay.stages_off;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smraw + lay.full_off);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + lay.empty_off);
+    uint64_t *rfull = reinterpret_cast<uint64_t *>(smraw + lay.rfull_off);
+    uint64_t *rempty = reinterpret_cast<uint64_t *>(smraw + lay.rempty_off);
+    uint64_t *pfull = reinterpret_cast<uint64_t *>(smraw + lay.pfull_off);
+    uint64_t *pempty = reinterpret_cast<uint64_t *>(smraw + lay.pempty_off);
+    int *s_meta = reinterpret_cast<int *>(smraw + lay.meta_off);
+    float *s_u = reinterpret_cast<float *>(smraw + lay.u_off);
+    float *s_rt = reinterpret_cast<float *>(smraw + lay.rt_off);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smraw + lay.flag_off);
+
+    const int grid = gridDim.x;
+    const int n_my = (a.items - (int)blockIdx.x + grid - 1) / grid;
+    auto item_of = [&](int k) { return (int)blockIdx.x + k * grid; };   // item = b * H + h
+    auto meta_bad = [&](int hd, int ln) { return hd < 0 || hd >= L || ln < 0 || ln > L; };
+    auto rec = [&](int r) { return smraw + lay.rec_off + r * lay.rec_bytes; };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, NC / 32);               // one arrival per consumer warp
+        }
+        for (int r = 0; r < RB; ++r) {
+            mbar_init(rfull + r, 33);                    // 32 cp.async arrivals + lane 0's
+            mbar_init(rempty + r, NC / 32);
+        }
+        for (int i = 0; i < kGdnBufs; ++i) {
+            mbar_init(pfull + i, 1);                     // the preparing warp's lane 0
+            mbar_init(pempty + i, NC / 32);
+        }
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    // Ring pointers of every item of this CTA, read once; the thread that sees
+    // a sequence's last arrival commits the new ones (every item of the
+    // sequence, in every CTA, has read them by then).
+    for (int k = tid; k < n_my; k += blockDim.x) {
+        const int it = item_of(k), b = it / H;
+        const int hd = __ldcg(a.ring_head + b), ln = __ldcg(a.ring_len + b);
+        s_meta[k * 2 + 0] = hd;
+        s_meta[k * 2 + 1] = ln;
+        if (meta_bad(hd, ln) && it % H == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
+        __threadfence();
+        if (atomicAdd(a.arrive + b, 1) == H - 1) {
+            __threadfence();
+            if (!meta_bad(hd, ln)) {
+                const bool fold = ln + 1 >= L;
+                a.ring_head[b] = fold ? (hd + ln + 1) % L : hd;
+                a.ring_len[b] = fold ? 0 : ln + 1;
+            }
+            a.arrive[b] = 0;
+        }
+    }
+    __syncthreads();                                     // the only CTA-wide barrier
+    if (n_my <= 0) return;
+
+    if (warp == 0) {
+        // ================================= tile warp ==================================
+        if (lane != 0) return;
+        const uint64_t pol = l2_evict_first_policy();
+        bool ok = true;
+        int issued = 0;
+        for (int k = 0; k < n_my && ok; ++k) {
+            const size_t bh = (size_t)item_of(k);
+            for (int uu = 0; uu < NU; ++uu) {
+                const int t = issued, s = t % S;
+                if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort);
+                if (!ok) break;
+                mbar_arrive_expect_tx(full + s, lay.stage_bytes);
+                bulk_g2s(stages + s * lay.stage_bytes, a.ckpt + (bh * DV + uu * kGdnRows) * DK, lay.stage_bytes,
+                         full + s, pol);
+                issued = t + 1;
+            }
+        }
+        if (!ok) {
+            *s_abort = 1;
+            flag_error(a.err, RSSM_DEVERR_TIMEOUT);
+            for (int u = issued - S < 0 ? 0 : issued - S; u < issued; ++u)
+                mbar_wait(full + (u % S), (uint32_t)((u / S) & 1));
+        }
+        return;
+    }
+
+    if (warp == 1) {
+        // ================================ record warp =================================
+        bool ok = true;
+        int k = 0;
+        for (; k < n_my; ++k) {
+            const int r = k % RB;
+            if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const size_t bh = (size_t)item_of(k);
+            const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+            const bool good = !meta_bad(hd, ln);
+            if (good) {
+                // list position j < ln is ring slot (hd + j) mod L, j = ln the token
+                unsigned char *rb = rec(r);
+                const int nrec = ln + 1;
+                const int run1 = ln < L - hd ? ln : L - hd, run2 = ln - run1;
+                if (lane == 0) mbar_arrive_expect_tx(rfull + r, (uint32_t)((nrec * (DK + DV) + DK) * 2));
+                __syncwarp();
+                if (lane == 0) {
+                    unsigned char *d = rb + lay.rk_off;
+                    if (run1) bulk_g2s(d, a.rec_k + (bh * L + hd) * DK, run1 * DK * 2, rfull + r);
+                    if (run2) bulk_g2s(d + run1 * DK * 2, a.rec_k + bh * L * DK, run2 * DK * 2, rfull + r);
+                    bulk_g2s(d + ln * DK * 2, a.k + bh * DK, DK * 2, rfull + r);
+                } else if (lane == 1) {
+                    unsigned char *d = rb + lay.rv_off;
+                    if (run1) bulk_g2s(d, a.rec_v + (bh * L + hd) * DV, run1 * DV * 2, rfull + r);
+                    if (run2) bulk_g2s(d + run1 * DV * 2, a.rec_v + bh * L * DV, run2 * DV * 2, rfull + r);
+                    bulk_g2s(d + ln * DV * 2, a.v + bh * DV, DV * 2, rfull + r);
+                } else if (lane == 2) {
+                    bulk_g2s(rb + lay.rq_off, a.q + bh * DK, DK * 2, rfull + r);
+                }
+                for (int j = lane; j <= ln; j += 32) {
+                    const int slot = hd + j < L ? hd + j : hd + j - L;
+                    cp_async4(rb + lay.ral_off + j * 4, j < ln ? a.rec_alpha + bh * L + slot : a.alpha + bh);
+                    cp_async4(rb + lay.rbe_off + j * 4, j < ln ? a.rec_beta + bh * L + slot : a.beta + bh);
+                }
+            }
+            cp_async_arrive_noinc(rfull + r);
+            if (lane == 0 && !good) mbar_arrive(rfull + r);
+        }
+        cp_async_wait_all();
+        // the copies of the last items may still be in flight: wait (bounded)
+        if (lane == 0)
+            for (int kk = k - RB < 0 ? 0 : k - RB; kk < k; ++kk) mbar_wait(rfull + kk % RB, (uint32_t)((kk / RB) & 1));
+        if (!ok && lane == 0) {
+            *s_abort = 1;
+            flag_error(a.err, RSSM_DEVERR_TIMEOUT);
+        }
+        return;
+    }
+
+    if (warp >= 2 + NC / 32) {
+        // ============================ item-preparation warps ============================
+        const int pw = warp - 2 - NC / 32;               // 0 or 1: even or odd items
+        bool live = true;
+        for (int kk = pw; kk < n_my; kk += 2) {
+            const int r = kk % RB, ib = kk % kGdnBufs;
+            if (live && kk >= kGdnBufs && !pwait(pempty + ib, (uint32_t)(((kk / kGdnBufs) - 1) & 1), s_abort)) {
+                live = false;
+                *s_abort = 1;
+            }
+            if (live && !pwait(rfull + r, (uint32_t)((kk / RB) & 1), s_abort)) {
+                live = false;
+                *s_abort = 1;
+            }
+            const size_t bh = (size_t)item_of(kk);
+            const int hd = s_meta[kk * 2 + 0], ln = s_meta[kk * 2 + 1];
+            const bool work = live && !meta_bad(hd, ln);
+            const unsigned char *rb = rec(r);
+            const uint16_t *r_k = reinterpret_cast<const uint16_t *>(rb + lay.rk_off);
+            const uint16_t *r_v = reinterpret_cast<const uint16_t *>(rb + lay.rv_off);
+            const uint16_t *r_q = reinterpret_cast<const uint16_t *>(rb + lay.rq_off);
+            const float *r_al = reinterpret_cast<const float *>(rb + lay.ral_off);
+            const float *r_be = reinterpret_cast<const float *>(rb + lay.rbe_off);
+            if (work && ln + 1 < L) {
+                // a non-flush step appends the token to the ring, slot (hd + ln) mod L
+                const int slot = hd + ln < L ? hd + ln : hd + ln - L;
+                if (lane < CK) {
+                    *reinterpret_cast<uint4 *>(a.rec_k + (bh * L + slot) * DK + lane * 8) =
+                        *reinterpret_cast<const uint4 *>(r_k + ln * DK + lane * 8);
+                } else if (lane < CK + CV) {
+                    const int c = lane - CK;
+                    *reinterpret_cast<uint4 *>(a.rec_v + (bh * L + slot) * DV + c * 8) =
+                        *reinterpret_cast<const uint4 *>(r_v + ln * DV + c * 8);
+                }
+                if (lane == 0) {
+                    a.rec_alpha[bh * L + slot] = r_al[ln];
+                    a.rec_beta[bh * L + slot] = r_be[ln];
+                }
+            }
+            if (work) {
+                // backward chain from the newest record; lane holds columns lane + 32 m of u
+                // and rows lane + 32 m of the record term
+                constexpr int MK = DK / 32, MV = DV / 32;
+                float u[MK], racc[MV];
+#pragma unroll
+                for (int m = 0; m < MK; ++m) u[m] = bf16_at(r_q, lane + 32 * m);
+#pragma unroll
+                for (int m = 0; m < MV; ++m) racc[m] = 0.0f;
+                for (int j = ln; j >= 0; --j) {
+                    float d = 0.0f;
+#pragma unroll
+                    for (int m = 0; m < MK; ++m) d = fmaf(bf16_at(r_k, j * DK + lane + 32 * m), u[m], d);
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                    const float cf = r_be[j] * d, al = r_al[j];
+#pragma unroll
+                    for (int m = 0; m < MV; ++m) racc[m] = fmaf(cf, bf16_at(r_v, j * DV + lane + 32 * m), racc[m]);
+#pragma unroll
+                    for (int m = 0; m < MK; ++m) u[m] = al * fmaf(-cf, bf16_at(r_k, j * DK + lane + 32 * m), u[m]);
+                }
+#pragma unroll
+                for (int m = 0; m < MK; ++m) s_u[ib * DK + lane + 32 * m] = u[m];
+#pragma unroll
+                for (int m = 0; m < MV; ++m) s_rt[ib * DV + lane + 32 * m] = racc[m];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pfull + ib);      // item kk is prepared
+        }
+        if (lane == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
+        return;
+    }
+
+    // ================================ consumer warps =================================
+    const int ctid = tid - 64;                           // 0..255
+    const int cw = ctid >> 5;                            // owns rows cw + RSTEP * v of each stage
+    const int col4 = lane;                               // this lane's 4 columns
+    bool live = true;
+    int u = 0;                                           // stages consumed so far
+    for (int k = 0; k < n_my; ++k) {
+        const int r = k % RB, ib = k % kGdnBufs;
+        if (live && !pwait(pfull + ib, (uint32_t)((k / kGdnBufs) & 1), s_abort)) {
+            live = false;
+            *s_abort = 1;
+        }
+        if (live && !pwait(rfull + r, (uint32_t)((k / RB) & 1), s_abort)) {
+            live = false;
+            *s_abort = 1;
+        }
+        const size_t bh = (size_t)item_of(k);
+        const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+        const bool work = live && !meta_bad(hd, ln);
+        const bool fold = work && (ln + 1 >= L);
+        const int nrec = ln + 1;
+        const unsigned char *rb = rec(r);
+        const uint16_t *r_k = reinterpret_cast<const uint16_t *>(rb + lay.rk_off);
+        const uint16_t *r_v = reinterpret_cast<const uint16_t *>(rb + lay.rv_off);
+        const float *r_al = reinterpret_cast<const float *>(rb + lay.ral_off);
+        const float *r_be = reinterpret_cast<const float *>(rb + lay.rbe_off);
+        const float4 u0 = *reinterpret_cast<const float4 *>(s_u + ib * DK + col4 * 4);
+        const float *rt = s_rt + ib * DV;
+        for (int uu = 0; uu < NU; ++uu, ++u) {
+            const int s = u % S;
+            if (live && !pwait(full + s, (uint32_t)((u / S) & 1), s_abort)) {
+                live = false;
+                *s_abort = 1;
+            }
+            const float4 *stg = reinterpret_cast<const float4 *>(stages + s * lay.stage_bytes);
+            float4 hv[VPT];
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) hv[v] = stg[ctid + v * NC];
+            __syncwarp();                                // the warp is done with the stage
+            if (lane == 0) mbar_arrive(empty + s);
+            if (!work) continue;
+            // o = S_c . u_0 + record term
+            float part[VPT];
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                float d = hv[v].x * u0.x;
+                d = fmaf(hv[v].y, u0.y, d);
+                d = fmaf(hv[v].z, u0.z, d);
+                d = fmaf(hv[v].w, u0.w, d);
+                part[v] = d;
+            }
+            group_reduce<G4, VPT>(part);
+            if (reduced_writer<G4, VPT>()) {
+                const int row = uu * kGdnRows + cw + RSTEP * reduced_index<G4, VPT>(0);
+                a.o[bh * DV + row] = part[0] + rt[row];
+            }
+            if (fold) {
+                // sequential rank-one updates of every row, oldest record first
+                for (int j = 0; j < nrec; ++j) {
+                    const uint2 kraw = *reinterpret_cast<const uint2 *>(r_k + j * DK + col4 * 4);
+                    const float4 kj = make_float4(bf16lo(kraw.x), bf16hi(kraw.x), bf16lo(kraw.y), bf16hi(kraw.y));
+                    const float al = r_al[j], be = r_be[j];
+                    float d[VPT];
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) {
+                        float t = hv[v].x * kj.x;
+                        t = fmaf(hv[v].y, kj.y, t);
+                        t = fmaf(hv[v].z, kj.z, t);
+                        t = fmaf(hv[v].w, kj.w, t);
+                        d[v] = t;
+                    }
+                    group_allreduce<G4, VPT>(d);
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) {
+                        const float vr = bf16_at(r_v, j * DV + uu * kGdnRows + cw + RSTEP * v);
+                        const float c = be * fmaf(-al, d[v], vr);
+                        hv[v].x = fmaf(c, kj.x, al * hv[v].x);
+                        hv[v].y = fmaf(c, kj.y, al * hv[v].y);
+                        hv[v].z = fmaf(c, kj.z, al * hv[v].z);
+                        hv[v].w = fmaf(c, kj.w, al * hv[v].w);
+                    }
+                }
+                float4 *ck4 = reinterpret_cast<float4 *>(a.ckpt + (bh * DV + uu * kGdnRows) * DK);
+#pragma unroll
+                for (int v = 0; v < VPT; ++v) st_stream(ck4 + ctid + v * NC, hv[v]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(rempty + r);                     // record buffer r may be refilled
+            mbar_arrive(pempty + ib);                    // and the item buffer ib
+        }
+    }
+    if (ctid == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
+}
+
+}  // namespace rssm

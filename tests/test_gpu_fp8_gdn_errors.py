@@ -279,3 +279,107 @@ def test_persistent_fp8_decodes_every_code_exactly(batch):
     expect = e4m3_decode(picked) * scale
     assert len(np.unique(picked)) == 254
     np.testing.assert_array_equal(y.cpu().numpy().astype(np.float64), expect)
+
+
+# ------------------------------------------- persistent gated-delta decode
+
+class GDNPersistRun:
+    """Serving head shape (dk = dv = 128): replay decode, optional standalone
+    flushes, against the stepwise oracle on sampled sequences, with a per-
+    sequence ring model (head, len) and checks of the appended records."""
+
+    def __init__(self, batch, L, seed, sample):
+        from ssm_decode_state_gb300 import replayssm as rs
+        self.rs = rs
+        self.shape = gen.GDNShape(batch=batch, nheads=32, dk=128, dv=128, L=L)
+        self.seed, self.sample = seed, np.asarray(sample)
+        S0 = gen.gdn_random_state(self.shape, seed)
+        self.dims = rs.gdn_dims(batch, 32, 128, 128, L)
+        self.cache = rs.gdn_cache(self.dims, ckpt=to_dev(S0))
+        self.oracle = GDNStepwise(S0[self.sample])
+        self.head = np.zeros(batch, np.int64)
+        self.len = np.zeros(batch, np.int64)
+
+    def step(self, t):
+        L = self.shape.L
+        st = gen.gdn_step_inputs(self.shape, self.seed, t)
+        o = self.rs.gdn_decode(self.cache, *(to_dev(a, torch.bfloat16) for a in (st.q, st.k, st.v)),
+                               to_dev(st.alpha), to_dev(st.beta))
+        s = self.sample
+        oo = self.oracle.step(st.q[s], st.k[s], st.v[s], st.alpha[s], st.beta[s])
+        assert_close(o.cpu().numpy()[s], oo, f"gdn persistent o step {t}", RTOL_INPLACE)
+        fold = self.len + 1 >= L
+        slot = (self.head + self.len) % L
+        self.head = np.where(fold, (self.head + self.len + 1) % L, self.head)
+        self.len = np.where(fold, 0, self.len + 1)
+        np.testing.assert_array_equal(self.cache.ring_len.cpu().numpy(), self.len)
+        np.testing.assert_array_equal(self.cache.ring_head.cpu().numpy(), self.head)
+        assert int(self.cache.err.item()) == 0
+        # the token's records sit in the ring slot it was appended to (non-fold sequences)
+        bs = [b for b in s if not fold[b]]
+        if bs:
+            rk = self.cache.rec_k.cpu().float().numpy()
+            rv = self.cache.rec_v.cpu().float().numpy()
+            ra = self.cache.rec_alpha.cpu().numpy()
+            for b in bs:
+                np.testing.assert_array_equal(rk[b, :, slot[b]], bf16_round(st.k[b]))
+                np.testing.assert_array_equal(rv[b, :, slot[b]], bf16_round(st.v[b]))
+                np.testing.assert_array_equal(ra[b, :, slot[b]], st.alpha[b])
+        for i, b in enumerate(s):
+            if fold[b]:
+                e = rel_err(self.cache.ckpt[b].cpu().numpy(), self.oracle.S[i])
+                assert e <= RTOL_INPLACE, f"gdn checkpoint of seq {b} after step {t}: {e:.3e}"
+
+    def flush(self, mask):
+        self.rs.gdn_flush(self.cache, torch.tensor(mask, dtype=torch.uint8, device="cuda"))
+        m = np.asarray(mask, bool) & (self.len > 0)
+        self.head = np.where(m, (self.head + self.len) % self.shape.L, self.head)
+        self.len = np.where(m, 0, self.len)
+        np.testing.assert_array_equal(self.cache.ring_len.cpu().numpy(), self.len)
+        np.testing.assert_array_equal(self.cache.ring_head.cpu().numpy(), self.head)
+
+
+def bf16_round(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+@pytest.mark.parametrize("batch,L", [(16, 4), (16, 16), (40, 8)])
+def test_gdn_persistent_variants(batch, L):
+    """Persistent gated-delta decode (serving head shape) at batches of 512 and
+    1280 heads, rings of 4..16: outputs and folded checkpoints against the
+    oracle, ring pointers and appended records exact."""
+    r = GDNPersistRun(batch, L, 610 + L, sample=[0, batch // 2, batch - 1])
+    for t in range(2 * L + 3):
+        r.step(t)
+
+
+def test_gdn_persistent_with_standalone_flush():
+    """Persistent decodes around a masked standalone flush: the flushed and the
+    unflushed sequences then fold at different steps of the same launches."""
+    r = GDNPersistRun(16, 8, 77, sample=[0, 1, 5])
+    for t in range(3):
+        r.step(t)
+    r.flush([1, 0] * 8)
+    for i, b in enumerate(r.sample):
+        if b % 2 == 0:
+            assert rel_err(r.cache.ckpt[b].cpu().numpy(), r.oracle.S[i]) <= RTOL_INPLACE
+    for t in range(3, 14):
+        r.step(t)
+
+
+def test_gdn_persistent_bad_ring_pointers():
+    """A sequence with invalid ring pointers is flagged and left untouched by
+    the persistent kernel; the others proceed."""
+    r = GDNPersistRun(16, 8, 91, sample=[0])
+    r.step(0)
+    r.cache.ring_len[3] = 9                               # > L
+    before = r.cache.ckpt[3].clone()
+    rk = r.cache.rec_k[3].clone()
+    st = gen.gdn_step_inputs(r.shape, r.seed, 1)
+    r.rs.gdn_decode(r.cache, *(to_dev(a, torch.bfloat16) for a in (st.q, st.k, st.v)),
+                    to_dev(st.alpha), to_dev(st.beta))
+    torch.cuda.synchronize()
+    assert int(r.cache.err.item()) & r.rs.DEVERR_RING_META
+    assert r.cache.ring_len[3].item() == 9
+    assert torch.equal(r.cache.ckpt[3], before) and torch.equal(r.cache.rec_k[3], rk)
+    assert r.cache.ring_len[0].item() == 2 and not r.cache.arrive.any().item()

@@ -104,7 +104,7 @@ rssm_status launch_verify_persistent(const rssm_mamba2_dims *d, const M2Args &ar
     if (s != RSSM_OK) return s;
     M2Args a = args;
     void *params[] = {&a, &pc};
-    if (cudaLaunchKernel(k, dim3(grid), dim3(persist_threads(256)), params, smem, st) != cudaSuccess)
+    if (cudaLaunchKernel(k, dim3(grid), dim3(persist_decode_threads(256)), params, smem, st) != cudaSuccess)
         return RSSM_ERR_CUDA;
     if ((s = launch_status()) != RSSM_OK) return s;
     verify_bc_epilogue<<<d->batch, 128, 0, st>>>(a);

@@ -2,23 +2,27 @@
 //
 // Same pipeline as the persistent decode (mamba2_persist.cuh): one CTA per SM,
 // a tile warp streaming each head's FP32 checkpoint through shared-memory
-// stages with bulk copies, a record warp copying each item's records with
-// cp.async, and eight consumer warps that own whole rows.  Per item (HPI heads
-// of one group of one sequence) the records are the len buffered ones plus the
-// T drafts; draft i is scored against the checkpoint, the buffered records and
-// drafts 1..i:
+// stages with bulk copies, a record warp copying each item's records (ring
+// runs and the drafts, by bulk copy), two preparation warps and eight consumer
+// warps that own whole rows.  Per item (HPI heads of one group of one
+// sequence) the records are the len buffered ones plus the T drafts; draft i
+// is scored against the checkpoint, the buffered records and drafts 1..i:
 //   y_i = exp(A S_i) (h_c . C_i) + sum_{j <= len+i} exp(A (S_i - S_j)) dt_j (B_j . C_i) x_j + D x_i,
 // with S the running sum of dt over the records.  If len + T > L the buffered
 // records are first folded into the checkpoint (the pre-flush), with the same
 // arithmetic as a flush; the outputs are read from the unfolded checkpoint
 // plus all records, which is the same number.
 //
+// The preparation warps, ahead of the consumers, append the drafts' x and dt
+// rows to the ring and compute B_j . C_i, the query weights and decays, the
+// pre-flush fold weights and the record term of every (head, draft, row), into
+// triple-buffered item arrays handed over through mbarriers.
+//
 // Ring pointers are read once at kernel start and committed there by the
 // sequence's last arrival: pre-flush -> head <- (head + len) mod L, len <- T;
-// otherwise len <- len + T.  The drafts' x and dt rows (per head) are appended
-// by the consumers; the drafts' B and C rows are shared by the heads of a group
-// and, on a pre-flush, land on slots other CTAs may still be reading, so a
-// small epilogue kernel writes them after this one.
+// otherwise len <- len + T.  The drafts' B and C rows are shared by the heads
+// of a group and, on a pre-flush, land on slots other CTAs may still be
+// reading, so a small epilogue kernel writes them after this one.
 #pragma once
 
 #include "mamba2_persist.cuh"
@@ -28,9 +32,10 @@ namespace rssm {
 // Byte layout of the verify kernel's shared memory (T drafts, KM = L + T).
 struct VSmem {
     int stage_bytes, stages_off;
-    int full_off, empty_off, rfull_off, rempty_off;
+    int full_off, empty_off, rfull_off, rempty_off, pfull_off, pempty_off;
     int rec_off, rx_off, rB_off, rC_off, rdt_off, rec_bytes;
-    int meta_off, cb_off, w_off, decay_off, wf_off, fdec_off, rt_off, wx_off, ad_off, flag_off, total;
+    int meta_off, decay_off, wf_off, fdec_off, rt_off, cb_off, wcb_off, sfx_off, sff_off, wx_off, ad_off, flag_off;
+    int total;
     __host__ __device__ VSmem(int P, int N, int L, int T, int HPI, int S, int RB, int H, int MY) {
         const int KM = L + T;
         auto up = [](int v, int a) { return (v + a - 1) / a * a; };
@@ -41,6 +46,8 @@ struct VSmem {
         empty_off = o;  o += 8 * S;
         rfull_off = o;  o += 8 * RB;
         rempty_off = o; o += 8 * RB;
+        pfull_off = o;  o += 8 * 3;
+        pempty_off = o; o += 8 * 3;
         o = up(o, 128);
         // one record buffer: x [HPI][KM][P] bf16, B [KM][N] bf16, C [T][N] bf16, dt [HPI][KM] f32
         rx_off = 0;
@@ -50,13 +57,16 @@ struct VSmem {
         rec_bytes = up(rdt_off + HPI * KM * 4, 128);
         rec_off = o;   o += RB * rec_bytes;
         meta_off = o;  o += up(MY * 8, 16);                 // [items of this CTA][head, len]
-        // per-item arrays, double-buffered (two consumer barriers per item)
-        cb_off = o;    o += up(2 * T * KM * 4, 16);         // [2][T][KM]     B_j . C_i
-        w_off = o;     o += up(2 * HPI * T * KM * 4, 16);   // [2][HPI][T][KM] query weights
-        decay_off = o; o += up(2 * HPI * T * 4, 16);        // [2][HPI][T]    exp(A S_i)
-        wf_off = o;    o += up(2 * HPI * KM * 4, 16);       // [2][HPI][KM]   fold weights
-        fdec_off = o;  o += up(2 * HPI * 4, 16);            // [2][HPI]       fold decay
-        rt_off = o;    o += up(2 * HPI * T * P * 4, 16);    // [2][HPI][T][P] record terms
+        // prepared items, triple-buffered
+        decay_off = o; o += up(3 * HPI * T * 4, 16);        // [3][HPI][T]    exp(A S_i)
+        wf_off = o;    o += up(3 * HPI * KM * 4, 16);       // [3][HPI][KM]   fold weights
+        fdec_off = o;  o += up(3 * HPI * 4, 16);            // [3][HPI]       fold decay
+        rt_off = o;    o += up(3 * HPI * T * P * 4, 16);    // [3][HPI][T][P] record terms
+        // the preparation warps' own scratch
+        cb_off = o;    o += up(T * KM * 4, 16);             // [T][KM]        B_j . C_i
+        wcb_off = o;   o += up(HPI * T * KM * 4, 16);       // [HPI][T][KM]   w_ij (B_j . C_i)
+        sfx_off = o;   o += up(HPI * T * KM * 4, 16);       // [HPI][T][KM]   query suffix sums
+        sff_off = o;   o += up(HPI * KM * 4, 16);           // [HPI][KM]      fold suffix sums
         wx_off = o;    o += up(KM * P * 4, 16);             // [KM][P] fold coefficients (rows owned per warp)
         ad_off = o;    o += up(2 * H * 4, 16);              // A[H], D[H]
         flag_off = o;  o += 16;
@@ -65,12 +75,12 @@ struct VSmem {
 };
 
 template <int N, int P, int VPT, int HPI>
-__global__ void __launch_bounds__(persist_threads(P * N / 4 / VPT), 1)
+__global__ void __launch_bounds__(persist_decode_threads(P * N / 4 / VPT), 1)
 m2_verify_persistent(const M2Args a, const PersistCfg pc) {
     constexpr int NC = P * N / 4 / VPT;                  // consumer threads
     constexpr int G4 = N / 4;                            // lanes per row
     constexpr int RSTEP = NC / G4;                       // rows between a thread's consecutive float4s
-    constexpr int CX = P / 8, CB = N / 8;                // 16-byte chunks per x / B row
+    constexpr int CX = P / 8;                            // 16-byte chunks per x row
     constexpr int TQ = 4;                                // draft slots in registers (T <= 4)
     static_assert(G4 == 32, "a warp owns whole rows");
     static_assert(HPI * TQ == 32 && TQ * VPT == 32, "one (head, draft) pair per lane");
@@ -84,9 +94,13 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
     uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + lay.empty_off);
     uint64_t *rfull = reinterpret_cast<uint64_t *>(smraw + lay.rfull_off);
     uint64_t *rempty = reinterpret_cast<uint64_t *>(smraw + lay.rempty_off);
+    uint64_t *pfull = reinterpret_cast<uint64_t *>(smraw + lay.pfull_off);
+    uint64_t *pempty = reinterpret_cast<uint64_t *>(smraw + lay.pempty_off);
     int *s_meta = reinterpret_cast<int *>(smraw + lay.meta_off);
     float *s_cb = reinterpret_cast<float *>(smraw + lay.cb_off);
-    float *s_w = reinterpret_cast<float *>(smraw + lay.w_off);
+    float *s_wcb = reinterpret_cast<float *>(smraw + lay.wcb_off);
+    float *s_sfx = reinterpret_cast<float *>(smraw + lay.sfx_off);
+    float *s_sff = reinterpret_cast<float *>(smraw + lay.sff_off);
     float *s_decay = reinterpret_cast<float *>(smraw + lay.decay_off);
     float *s_wf = reinterpret_cast<float *>(smraw + lay.wf_off);
     float *s_fdec = reinterpret_cast<float *>(smraw + lay.fdec_off);
@@ -113,6 +127,10 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
         for (int r = 0; r < RB; ++r) {
             mbar_init(rfull + r, 33);                    // 32 cp.async arrivals + lane 0's release
             mbar_init(rempty + r, NC / 32);
+        }
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(pfull + i, kPrepThreads / 32);     // one arrival per preparation warp
+            mbar_init(pempty + i, NC / 32);
         }
         *s_abort = 0;
         fence_mbar_init();
@@ -179,48 +197,209 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
         const uint16_t *iB = static_cast<const uint16_t *>(a.Bin);
         const uint16_t *iC = static_cast<const uint16_t *>(a.Cin);
         bool ok = true;
-        for (int k = 0; k < n_my; ++k) {
+        int k = 0;
+        for (; k < n_my; ++k) {
             const int r = k % RB;
             if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const int it = item_of(k), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
             const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
-            if (!meta_bad(hd, ln)) {
+            const bool good = !meta_bad(hd, ln);
+            if (good) {
+                // buffered records: at most two contiguous runs of ring slots; drafts: one
+                // row each from the inputs; all by bulk copy, dt words by cp.async
                 unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
                 const int nrec = ln + T;
-                for (int row = lane / CX; row < HPI * nrec; row += 32 / CX) {
-                    const int hh = row / nrec, j = row - hh * nrec, c = lane % CX;
-                    const size_t bh = (size_t)b * H + h0 + hh;
-                    const uint16_t *src = j < ln ? rx + ((bh * L + (hd + j) % L) * P + c * 8)
-                                                 : ix + ((((size_t)b * T + (j - ln)) * H + h0 + hh) * P + c * 8);
-                    cp_async16(rb + lay.rx_off + ((hh * KM + j) * P + c * 8) * 2, src);
-                }
-                for (int idx = lane; idx < nrec * CB; idx += 32) {
-                    const int j = idx / CB, c = idx - j * CB;
-                    const uint16_t *src = j < ln ? rB + ((((size_t)b * G + g) * L + (hd + j) % L) * N + c * 8)
-                                                 : iB + ((((size_t)b * T + (j - ln)) * G + g) * N + c * 8);
-                    cp_async16(rb + lay.rB_off + (j * N + c * 8) * 2, src);
-                }
-                for (int idx = lane; idx < T * CB; idx += 32) {
-                    const int i = idx / CB, c = idx - i * CB;
-                    cp_async16(rb + lay.rC_off + (i * N + c * 8) * 2, iC + ((((size_t)b * T + i) * G + g) * N + c * 8));
+                const int run1 = ln < L - hd ? ln : L - hd, run2 = ln - run1;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(rfull + r, (uint32_t)((HPI * nrec * P + nrec * N + T * N) * 2));
+                __syncwarp();
+                if (lane < HPI) {
+                    const size_t bh = (size_t)b * H + h0 + lane;
+                    unsigned char *dx = rb + lay.rx_off + lane * KM * P * 2;
+                    if (run1) bulk_g2s(dx, rx + (bh * L + hd) * P, run1 * P * 2, rfull + r);
+                    if (run2) bulk_g2s(dx + run1 * P * 2, rx + bh * L * P, run2 * P * 2, rfull + r);
+                    for (int i = 0; i < T; ++i)
+                        bulk_g2s(dx + (ln + i) * P * 2, ix + (((size_t)b * T + i) * H + h0 + lane) * P, P * 2, rfull + r);
+                } else if (lane == HPI) {
+                    const size_t bg = (size_t)b * G + g;
+                    unsigned char *dB = rb + lay.rB_off;
+                    if (run1) bulk_g2s(dB, rB + (bg * L + hd) * N, run1 * N * 2, rfull + r);
+                    if (run2) bulk_g2s(dB + run1 * N * 2, rB + bg * L * N, run2 * N * 2, rfull + r);
+                    for (int i = 0; i < T; ++i)
+                        bulk_g2s(dB + (ln + i) * N * 2, iB + (((size_t)b * T + i) * G + g) * N, N * 2, rfull + r);
+                } else if (lane == HPI + 1) {
+                    for (int i = 0; i < T; ++i)
+                        bulk_g2s(rb + lay.rC_off + i * N * 2, iC + (((size_t)b * T + i) * G + g) * N, N * 2, rfull + r);
                 }
                 for (int idx = lane; idx < HPI * nrec; idx += 32) {
                     const int hh = idx / nrec, j = idx - hh * nrec;
                     const size_t bh = (size_t)b * H + h0 + hh;
+                    const int slot = hd + j < L ? hd + j : hd + j - L;
                     cp_async4(rb + lay.rdt_off + (hh * KM + j) * 4,
-                              j < ln ? a.rec_dt + bh * L + (hd + j) % L : a.dt + ((size_t)b * T + (j - ln)) * H + h0 + hh);
+                              j < ln ? a.rec_dt + bh * L + slot : a.dt + ((size_t)b * T + (j - ln)) * H + h0 + hh);
                 }
             }
             cp_async_arrive_noinc(rfull + r);
-            if (lane == 0) mbar_arrive(rfull + r);
+            if (lane == 0 && !good) mbar_arrive(rfull + r);   // with good metadata lane 0 arrived above
         }
         cp_async_wait_all();
+        // the record copies of the last items may still be in flight: wait (bounded)
+        if (lane == 0)
+            for (int kk = k - RB < 0 ? 0 : k - RB; kk < k; ++kk) mbar_wait(rfull + kk % RB, (uint32_t)((kk / RB) & 1));
         if (!ok && lane == 0) {
             *s_abort = 1;
             flag_error(a.err, RSSM_DEVERR_TIMEOUT);
         }
+        return;
+    }
+
+    if (warp >= 2 + NC / 32) {
+        // ============================ item-preparation warps ============================
+        const int ptid = tid - 64 - NC, pw = ptid >> 5;
+        bool live = true;
+        for (int kk = 0; kk < n_my; ++kk) {
+            const int r = kk % RB, ia = kk % 3;
+            const int it = item_of(kk), b = item_b(it), h0 = item_h0(it);
+            if (live && kk >= 3 && !pwait(pempty + ia, (uint32_t)(((kk / 3) - 1) & 1), s_abort)) {
+                live = false;
+                *s_abort = 1;
+            }
+            if (live && !pwait(rfull + r, (uint32_t)((kk / RB) & 1), s_abort)) {
+                live = false;
+                *s_abort = 1;
+            }
+            const int hd = s_meta[kk * 2 + 0], ln = s_meta[kk * 2 + 1];
+            const bool work = live && !meta_bad(hd, ln);
+            const bool pre = ln + T > L;
+            const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
+            const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
+            const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
+            const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
+            const float *r_dt = reinterpret_cast<const float *>(rb + lay.rdt_off);
+            float *dec = s_decay + ia * HPI * T, *rt = s_rt + ia * HPI * T * P;
+            float *wf = s_wf + ia * HPI * KM, *fdec = s_fdec + ia * HPI;
+            if (work) {
+                // drafts' x and dt rows into the ring (per head, read by no other CTA)
+                const int hd2 = pre ? (hd + ln) % L : hd, ln2 = pre ? 0 : ln;
+                for (int idx = ptid; idx < HPI * T * CX + HPI * T; idx += kPrepThreads) {
+                    if (idx < HPI * T * CX) {
+                        const int hh = idx / (T * CX), rr = idx - hh * T * CX, i = rr / CX, c = rr - i * CX;
+                        const size_t bh = (size_t)b * H + h0 + hh;
+                        const int slot = (hd2 + ln2 + i) % L;
+                        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.rec_x) + (bh * L + slot) * P + c * 8) =
+                            *reinterpret_cast<const uint4 *>(r_x + (hh * KM + ln + i) * P + c * 8);
+                    } else {
+                        const int rr = idx - HPI * T * CX, hh = rr / T, i = rr - hh * T;
+                        const size_t bh = (size_t)b * H + h0 + hh;
+                        a.rec_dt[bh * L + (hd2 + ln2 + i) % L] = r_dt[hh * KM + ln + i];
+                    }
+                }
+                // suffix sums of dt, newest first (suffix_sum's order): one pass per
+                // (head, draft) up to len + i gives that draft's S_ij and its decay;
+                // one pass per head over the buffered records gives the fold's
+                if (ptid < HPI * T) {
+                    const int hh = ptid / T, i = ptid - hh * T;
+                    const float *dth = r_dt + hh * KM;
+                    float *sf = s_sfx + (hh * T + i) * KM;
+                    float acc = 0.0f;
+                    for (int j = ln + i; j >= 0; --j) {
+                        sf[j] = acc;
+                        acc += dth[j];
+                    }
+                    dec[hh * T + i] = expf(s_A[h0 + hh] * acc);
+                } else if (pre && ptid < HPI * T + HPI) {
+                    const int hh = ptid - HPI * T;
+                    const float *dth = r_dt + hh * KM;
+                    float *sf = s_sff + hh * KM;
+                    float acc = 0.0f;
+                    for (int j = ln - 1; j >= 0; --j) {
+                        sf[j] = acc;
+                        acc += dth[j];
+                    }
+                    fdec[hh] = expf(s_A[h0 + hh] * acc);
+                }
+                // B_j . C_i for every draft i and record j <= len + i: a warp per pair
+                // (lane-strided products, butterfly sum), four pairs at a time per warp
+                for (int pb0 = pw * 4; pb0 < T * KM; pb0 += 8) {
+                    float acc[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int pr = pb0 + q, i = pr / KM, j = pr - i * KM;
+                        const bool valid = pr < T * KM && j <= ln + i;
+                        acc[q] = 0.0f;
+                        const int jj = valid ? j : 0, ii = valid ? i : 0;
+#pragma unroll
+                        for (int n = lane; n < N; n += 32)
+                            acc[q] = fmaf(bf16_at(r_B, jj * N + n), bf16_at(r_C, ii * N + n), acc[q]);
+                    }
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+                    }
+                    if (lane < 4) {
+                        const int pr = pb0 + lane, i = pr / KM, j = pr - i * KM;
+                        float v = acc[0];
+#pragma unroll
+                        for (int q = 1; q < 4; ++q) v = lane == q ? acc[q] : v;
+                        if (pr < T * KM && j <= ln + i) s_cb[pr] = v;
+                    }
+                }
+            }
+            prep_sync();                                 // suffix sums and B . C
+            if (work) {
+                // query weights times B_j . C_i, and the pre-flush fold weights
+                for (int idx = ptid; idx < HPI * T * KM; idx += kPrepThreads) {
+                    const int hh = idx / (T * KM), rr = idx - hh * T * KM, i = rr / KM, j = rr - i * KM;
+                    if (j <= ln + i) {
+                        const float wv = expf(s_A[h0 + hh] * s_sfx[idx]) * r_dt[hh * KM + j];
+                        s_wcb[idx] = wv * s_cb[i * KM + j];
+                    }
+                }
+                if (pre) {
+                    for (int idx = ptid; idx < HPI * ln; idx += kPrepThreads) {
+                        const int hh = idx / ln, j = idx - hh * ln;
+                        wf[hh * KM + j] = expf(s_A[h0 + hh] * s_sff[hh * KM + j]) * r_dt[hh * KM + j];
+                    }
+                }
+            }
+            prep_sync();                                 // w (B . C)
+            if (work) {
+                // record terms: 8 consecutive rows of one (head, draft) per thread
+                for (int o = ptid; o < HPI * T * (P / 8); o += kPrepThreads) {
+                    const int hi = o / (P / 8), r0 = (o - hi * (P / 8)) * 8, hh = hi / T, i = hi - hh * T;
+                    const uint16_t *xh = r_x + hh * KM * P + r0;
+                    const float *wc = s_wcb + hi * KM;
+                    float acc[8];
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) acc[v] = 0.0f;
+                    for (int j = 0; j <= ln + i; ++j) {
+                        const float c = wc[j];
+                        const uint4 xr = *reinterpret_cast<const uint4 *>(xh + j * P);
+                        acc[0] = fmaf(c, bf16lo(xr.x), acc[0]);
+                        acc[1] = fmaf(c, bf16hi(xr.x), acc[1]);
+                        acc[2] = fmaf(c, bf16lo(xr.y), acc[2]);
+                        acc[3] = fmaf(c, bf16hi(xr.y), acc[3]);
+                        acc[4] = fmaf(c, bf16lo(xr.z), acc[4]);
+                        acc[5] = fmaf(c, bf16hi(xr.z), acc[5]);
+                        acc[6] = fmaf(c, bf16lo(xr.w), acc[6]);
+                        acc[7] = fmaf(c, bf16hi(xr.w), acc[7]);
+                    }
+                    const uint4 xl = *reinterpret_cast<const uint4 *>(xh + (ln + i) * P);
+                    const float dh = s_D[h0 + hh];
+                    float4 *dst = reinterpret_cast<float4 *>(rt + hi * P + r0);
+                    dst[0] = make_float4(fmaf(dh, bf16lo(xl.x), acc[0]), fmaf(dh, bf16hi(xl.x), acc[1]),
+                                         fmaf(dh, bf16lo(xl.y), acc[2]), fmaf(dh, bf16hi(xl.y), acc[3]));
+                    dst[1] = make_float4(fmaf(dh, bf16lo(xl.z), acc[4]), fmaf(dh, bf16hi(xl.z), acc[5]),
+                                         fmaf(dh, bf16lo(xl.w), acc[6]), fmaf(dh, bf16hi(xl.w), acc[7]));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pfull + ia);      // item kk is prepared
+        }
+        if (ptid == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
         return;
     }
 
@@ -230,105 +409,17 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
     const int col4 = lane;                               // this lane's 4 columns
     bool live = true;
 
-    // Preparation of item kk (all consumers): wait for its records; after every
-    // warp is past item kk-2 (barrier 1) fill the double-buffered item arrays:
-    // draft appends (x, dt), B_j . C_i, query weights and decays, fold weights on a
-    // pre-flush; after barrier 2, the record terms of the rows each warp owns.
-    auto prep_item = [&](int kk) {
-        const int r = kk % RB, pb = kk & 1;
-        const int it = item_of(kk), b = item_b(it), h0 = item_h0(it);
-        if (live && !pwait(rfull + r, (uint32_t)((kk / RB) & 1), s_abort)) {
+    for (int k = 0; k < n_my; ++k) {
+        const int r = k % RB, ia = k % 3;
+        const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
+        if (live && !pwait(pfull + ia, (uint32_t)((k / 3) & 1), s_abort)) {
             live = false;
             *s_abort = 1;
         }
-        const int hd = s_meta[kk * 2 + 0], ln = s_meta[kk * 2 + 1];
-        const bool work = live && !meta_bad(hd, ln);
-        const bool pre = ln + T > L;
-        const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
-        const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
-        const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
-        const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
-        const float *r_dt = reinterpret_cast<const float *>(rb + lay.rdt_off);
-        float *cb = s_cb + pb * T * KM, *w = s_w + pb * HPI * T * KM, *dec = s_decay + pb * HPI * T;
-        float *wf = s_wf + pb * HPI * KM, *fdec = s_fdec + pb * HPI, *rt = s_rt + pb * HPI * T * P;
-        consumer_sync<NC>();                             // every warp is done with item kk-2's arrays
-        if (work) {
-            // drafts' x and dt rows into the ring (per head, read by no other CTA)
-            const int hd2 = pre ? (hd + ln) % L : hd, ln2 = pre ? 0 : ln;
-            for (int idx = ctid; idx < HPI * T * CX + HPI * T; idx += NC) {
-                if (idx < HPI * T * CX) {
-                    const int hh = idx / (T * CX), rr = idx - hh * T * CX, i = rr / CX, c = rr - i * CX;
-                    const size_t bh = (size_t)b * H + h0 + hh;
-                    const int slot = (hd2 + ln2 + i) % L;
-                    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.rec_x) + (bh * L + slot) * P + c * 8) =
-                        *reinterpret_cast<const uint4 *>(r_x + (hh * KM + ln + i) * P + c * 8);
-                } else {
-                    const int rr = idx - HPI * T * CX, hh = rr / T, i = rr - hh * T;
-                    const size_t bh = (size_t)b * H + h0 + hh;
-                    a.rec_dt[bh * L + (hd2 + ln2 + i) % L] = r_dt[hh * KM + ln + i];
-                }
-            }
-            // B_j . C_i for every draft i and record j <= len + i, one warp per pair
-            for (int pr = cw; pr < T * KM; pr += NC / 32) {
-                const int i = pr / KM, j = pr - i * KM;
-                if (j > ln + i) continue;
-                float acc = 0.0f;
-#pragma unroll
-                for (int n = lane; n < N; n += 32) acc = fmaf(bf16_at(r_B, j * N + n), bf16_at(r_C, i * N + n), acc);
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (lane == 0) cb[i * KM + j] = acc;
-            }
-            // query weights exp(A sum(dt after j, up to len+i)) dt_j and decays exp(A S_i)
-            for (int idx = ctid; idx < HPI * T * KM; idx += NC) {
-                const int hh = idx / (T * KM), rr = idx - hh * T * KM, i = rr / KM, j = rr - i * KM;
-                const float *dth = r_dt + hh * KM;
-                if (j <= ln + i) w[idx] = expf(s_A[h0 + hh] * suffix_sum(dth, j, ln + i)) * dth[j];
-            }
-            for (int idx = ctid; idx < HPI * T; idx += NC) {
-                const int hh = idx / T, i = idx - hh * T;
-                dec[idx] = expf(s_A[h0 + hh] * suffix_sum(r_dt + hh * KM, -1, ln + i));
-            }
-            if (pre) {
-                // fold weights over the buffered records only, the flush's arithmetic
-                for (int idx = ctid; idx < HPI * (ln + 1); idx += NC) {
-                    const int hh = idx / (ln + 1), j = idx - hh * (ln + 1);
-                    const float *dth = r_dt + hh * KM;
-                    if (j < ln) wf[hh * KM + j] = expf(s_A[h0 + hh] * suffix_sum(dth, j, ln - 1)) * dth[j];
-                    else fdec[hh] = expf(s_A[h0 + hh] * suffix_sum(dth, -1, ln - 1));
-                }
-            }
+        if (live && !pwait(rfull + r, (uint32_t)((k / RB) & 1), s_abort)) {
+            live = false;
+            *s_abort = 1;
         }
-        consumer_sync<NC>();                             // cb, w, dec, wf of item kk
-        if (work) {
-            // record terms of this warp's rows: lane = (head hh, draft i)
-            const int hh = lane / TQ, i = lane % TQ;
-            if (i < T) {
-                const float *wh = w + (hh * T + i) * KM, *ci = cb + i * KM;
-                const uint16_t *xh = r_x + hh * KM * P;
-                float acc[VPT];
-#pragma unroll
-                for (int v = 0; v < VPT; ++v) acc[v] = 0.0f;
-                for (int j = 0; j <= ln + i; ++j) {
-                    const float c = wh[j] * ci[j];
-#pragma unroll
-                    for (int v = 0; v < VPT; ++v) acc[v] = fmaf(c, bf16_at(xh, j * P + cw + RSTEP * v), acc[v]);
-                }
-                const float dh = s_D[h0 + hh];
-#pragma unroll
-                for (int v = 0; v < VPT; ++v) {
-                    const int row = cw + RSTEP * v;
-                    rt[(hh * T + i) * P + row] = fmaf(dh, bf16_at(xh, (ln + i) * P + row), acc[v]);
-                }
-            }
-        }
-        __syncwarp();
-    };
-
-    prep_item(0);
-    for (int k = 0; k < n_my; ++k) {
-        const int r = k % RB, pb = k & 1;
-        const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
         const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
         const bool work = live && !meta_bad(hd, ln);
         const bool pre = work && (ln + T > L);
@@ -336,8 +427,8 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
         const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
         const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
         const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
-        const float *dec = s_decay + pb * HPI * T, *rt = s_rt + pb * HPI * T * P;
-        const float *wf = s_wf + pb * HPI * KM, *fdec = s_fdec + pb * HPI;
+        const float *dec = s_decay + ia * HPI * T, *rt = s_rt + ia * HPI * T * P;
+        const float *wf = s_wf + ia * HPI * KM, *fdec = s_fdec + ia * HPI;
         float4 cfr[TQ];
 #pragma unroll
         for (int i = 0; i < TQ; ++i)
@@ -356,7 +447,6 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             for (int v = 0; v < VPT; ++v) hv[v] = stg[ctid + v * NC];
             __syncwarp();                                // the warp is done with the stage
             if (lane == 0) mbar_arrive(empty + s);
-            if (hh == 0 && k + 1 < n_my) prep_item(k + 1);   // overlaps the tiles in flight
             if (!work) continue;
             const int h = h0 + hh;
             const size_t tile = ((size_t)b * H + h) * P;
@@ -427,7 +517,10 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(rempty + r);          // record buffer r may be refilled
+        if (lane == 0) {
+            mbar_arrive(rempty + r);                     // record buffer r may be refilled
+            mbar_arrive(pempty + ia);                    // and the item arrays ia
+        }
     }
     if (ctid == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
 }

@@ -42,6 +42,7 @@ METRIC = "replay SSM decode tokens/s/layer at B=256; achieved HBM GB/s vs GB300 
 UNIT = "seq*tok/s/layer"
 POOL = 32                       # distinct per-step input sets kept on the device
 KERNEL_SOURCES = ["ssm_decode_state_gb300/csrc/mamba2_persist.cuh",
+                  "ssm_decode_state_gb300/csrc/persist_common.cuh",
                   "ssm_decode_state_gb300/csrc/common.cuh"]
 
 

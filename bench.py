@@ -374,7 +374,10 @@ def run_sweep(args):
     print(json.dumps({"sweep": out}), flush=True)
 
 
-def measure_rows(rs, dev, steps, warmup):
+ROWS = ("fp8", "verify", "gdn")
+
+
+def measure_rows(rs, dev, steps, warmup, which=ROWS):
     """The other hot-path rows, each on its own workload shape: FP8-read decode
     (batch 256), speculative verify + rollback (batch 512, T = 4) against the
     snapshot-per-draft path, Gated DeltaNet decode (batch 256) against its
@@ -384,120 +387,124 @@ def measure_rows(rs, dev, steps, warmup):
     wl = gen.workloads()
     out = {}
     stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl["mamba2_fp8read_b256"].seed)
 
     def dev_step(st):
         return (torch.from_numpy(st.dt).to(dev), torch.from_numpy(st.x).to(torch.bfloat16).to(dev),
                 torch.from_numpy(st.B).to(torch.bfloat16).to(dev), torch.from_numpy(st.C).to(torch.bfloat16).to(dev))
 
-    # ---- FP8 read copy, batch 256
-    w = wl["mamba2_fp8read_b256"]
-    sh = w.shape
-    prm = gen.mamba2_params(sh, w.seed)
-    dims = rs.mamba2_dims(sh.batch, sh.nheads, sh.headdim, sh.dstate, sh.ngroups, sh.L, read_copy=1)
-    g = torch.Generator(device=dev)
-    g.manual_seed(w.seed)
-    ck = torch.randn(sh.batch, sh.nheads, sh.headdim, sh.dstate, device=dev, generator=g).mul_(0.1)
-    cache = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D), ckpt=ck, device=dev)
-    rs.requant(cache)
-    pool = [dev_step(gen.mamba2_step_inputs(sh, prm, w.seed, t)) for t in range(8)]
-    y = torch.empty(sh.batch, sh.nheads, sh.headdim, device=dev)
-    for t in range(warmup):
-        rs.decode(cache, *pool[t % 8], y=y)
-    torch.cuda.synchronize(dev)
-    ln = int(cache.ring_len[0].item())
-    u = bm.mamba2_units(sh.nheads, sh.headdim, sh.dstate, sh.ngroups)
-    K = (steps // sh.L) * sh.L
-    alg = 0
-    for _ in range(K):
-        alg += bm.mamba2_replay_decode(u, ln, sh.L, read_copy=True) * sh.batch
-        ln = 0 if ln + 1 >= sh.L else ln + 1
-    ms = _timed(stream, lambda t: rs.decode(cache, *pool[t % 8], y=y), K)
-    assert int(cache.err.item()) == 0
-    out["fp8_read_decode_b256"] = {"us_per_step": round(ms * 1e3 / K, 1),
-                                   "seq_tok_s": round(sh.batch * K / (ms / 1e3), 1),
-                                   "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1)}
-    del cache, ck
+    if "fp8" in which:
+        # ---- FP8 read copy, batch 256
+        w = wl["mamba2_fp8read_b256"]
+        sh = w.shape
+        prm = gen.mamba2_params(sh, w.seed)
+        dims = rs.mamba2_dims(sh.batch, sh.nheads, sh.headdim, sh.dstate, sh.ngroups, sh.L, read_copy=1)
+        ck = torch.randn(sh.batch, sh.nheads, sh.headdim, sh.dstate, device=dev, generator=g).mul_(0.1)
+        cache = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D), ckpt=ck, device=dev)
+        rs.requant(cache)
+        pool = [dev_step(gen.mamba2_step_inputs(sh, prm, w.seed, t)) for t in range(8)]
+        y = torch.empty(sh.batch, sh.nheads, sh.headdim, device=dev)
+        for t in range(warmup):
+            rs.decode(cache, *pool[t % 8], y=y)
+        torch.cuda.synchronize(dev)
+        ln = int(cache.ring_len[0].item())
+        u = bm.mamba2_units(sh.nheads, sh.headdim, sh.dstate, sh.ngroups)
+        K = (steps // sh.L) * sh.L
+        alg = 0
+        for _ in range(K):
+            alg += bm.mamba2_replay_decode(u, ln, sh.L, read_copy=True) * sh.batch
+            ln = 0 if ln + 1 >= sh.L else ln + 1
+        ms = _timed(stream, lambda t: rs.decode(cache, *pool[t % 8], y=y), K)
+        assert int(cache.err.item()) == 0
+        out["fp8_read_decode_b256"] = {"us_per_step": round(ms * 1e3 / K, 1),
+                                       "seq_tok_s": round(sh.batch * K / (ms / 1e3), 1),
+                                       "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1)}
+        del cache, ck
 
-    # ---- verify T = 4 + rollback, batch 512, and the snapshot-per-draft path
-    w = wl["mamba2_verify_b512_T4"]
-    sh, T = w.shape, w.T
-    prm = gen.mamba2_params(sh, w.seed)
-    dims = rs.mamba2_dims(sh.batch, sh.nheads, sh.headdim, sh.dstate, sh.ngroups, sh.L)
-    ck = torch.randn(sh.batch, sh.nheads, sh.headdim, sh.dstate, device=dev, generator=g).mul_(0.1)
-    cache = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D), ckpt=ck, device=dev)
-    drafts = [dev_step(gen.mamba2_draft_inputs(sh, prm, w.seed, t, T)) for t in range(4)]
-    accs = [gen.accepted_counts(sh.batch, T, w.seed, t) for t in range(steps + warmup)]
-    accd = [torch.from_numpy(a).to(dev) for a in accs]
-    y = torch.empty(sh.batch, T, sh.nheads, sh.headdim, device=dev)
+    if "verify" in which:
+        # ---- verify T = 4 + rollback, batch 512, and the snapshot-per-draft path
+        w = wl["mamba2_verify_b512_T4"]
+        sh, T = w.shape, w.T
+        u = bm.mamba2_units(sh.nheads, sh.headdim, sh.dstate, sh.ngroups)
+        prm = gen.mamba2_params(sh, w.seed)
+        dims = rs.mamba2_dims(sh.batch, sh.nheads, sh.headdim, sh.dstate, sh.ngroups, sh.L)
+        ck = torch.randn(sh.batch, sh.nheads, sh.headdim, sh.dstate, device=dev, generator=g).mul_(0.1)
+        cache = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D), ckpt=ck, device=dev)
+        drafts = [dev_step(gen.mamba2_draft_inputs(sh, prm, w.seed, t, T)) for t in range(4)]
+        accs = [gen.accepted_counts(sh.batch, T, w.seed, t) for t in range(steps + warmup)]
+        accd = [torch.from_numpy(a).to(dev) for a in accs]
+        y = torch.empty(sh.batch, T, sh.nheads, sh.headdim, device=dev)
 
-    def vstep(t):
-        rs.verify(cache, *drafts[t % 4], y=y)
-        rs.rollback(cache, T, accd[t])
+        def vstep(t):
+            rs.verify(cache, *drafts[t % 4], y=y)
+            rs.rollback(cache, T, accd[t])
 
-    for t in range(warmup):
-        vstep(t)
-    torch.cuda.synchronize(dev)
-    lens = cache.ring_len.cpu().numpy().astype(np.int64)
-    alg = 0
-    for t in range(warmup, warmup + steps):
-        alg += sum(bm.mamba2_verify(u, int(l), T, sh.L) for l in lens)
-        lens = np.where(lens + T > sh.L, 0, lens) + T - (T - accs[t])
-    ms = _timed(stream, lambda t: vstep(warmup + t), steps)
-    assert int(cache.err.item()) == 0
-    row = {"us_per_step": round(ms * 1e3 / steps, 1), "seq_verify_s": round(sh.batch * steps / (ms / 1e3), 1),
-           "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1)}
-    del cache
-    pool_t = torch.empty((sh.batch, T + 1) + tuple(ck.shape[1:]), device=dev)
-    pool_t[:, 0] = ck
-    del ck
-    slot = torch.zeros(sh.batch, dtype=torch.int32, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    Ad = torch.from_numpy(prm.A).to(dev)
-    Dd = torch.from_numpy(prm.D).to(dev)
+        for t in range(warmup):
+            vstep(t)
+        torch.cuda.synchronize(dev)
+        lens = cache.ring_len.cpu().numpy().astype(np.int64)
+        alg = 0
+        for t in range(warmup, warmup + steps):
+            alg += sum(bm.mamba2_verify(u, int(l), T, sh.L) for l in lens)
+            lens = np.where(lens + T > sh.L, 0, lens) + T - (T - accs[t])
+        ms = _timed(stream, lambda t: vstep(warmup + t), steps)
+        assert int(cache.err.item()) == 0
+        row = {"us_per_step": round(ms * 1e3 / steps, 1), "seq_verify_s": round(sh.batch * steps / (ms / 1e3), 1),
+               "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1)}
+        del cache
+        pool_t = torch.empty((sh.batch, T + 1) + tuple(ck.shape[1:]), device=dev)
+        pool_t[:, 0] = ck
+        del ck
+        slot = torch.zeros(sh.batch, dtype=torch.int32, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        Ad = torch.from_numpy(prm.A).to(dev)
+        Dd = torch.from_numpy(prm.D).to(dev)
 
-    def cstep(t):
-        rs.conventional_verify(dims, pool_t, slot, Ad, Dd, *drafts[t % 4], err, y=y)
-        rs.conventional_select(slot, T, accd[t], err)
+        def cstep(t):
+            rs.conventional_verify(dims, pool_t, slot, Ad, Dd, *drafts[t % 4], err, y=y)
+            rs.conventional_select(slot, T, accd[t], err)
 
-    for t in range(warmup):
-        cstep(t)
-    ms_c = _timed(stream, lambda t: cstep(warmup + t), steps)
-    row["snapshot_us_per_step"] = round(ms_c * 1e3 / steps, 1)
-    row["snapshot_alg_GBps"] = round(bm.mamba2_conventional_verify(u, T) * sh.batch / (ms_c / steps / 1e3) / 1e9, 1)
-    row["replay_speedup"] = round(ms_c / ms, 3)
-    out["verify_T4_b512"] = row
-    del pool_t
+        for t in range(warmup):
+            cstep(t)
+        ms_c = _timed(stream, lambda t: cstep(warmup + t), steps)
+        row["snapshot_us_per_step"] = round(ms_c * 1e3 / steps, 1)
+        row["snapshot_alg_GBps"] = round(bm.mamba2_conventional_verify(u, T) * sh.batch / (ms_c / steps / 1e3) / 1e9, 1)
+        row["replay_speedup"] = round(ms_c / ms, 3)
+        out["verify_T4_b512"] = row
+        del pool_t
 
-    # ---- Gated DeltaNet, batch 256
-    w = wl["gdn_b256"]
-    sh = w.shape
-    dims = rs.gdn_dims(sh.batch, sh.nheads, sh.dk, sh.dv, sh.L)
-    S0 = torch.randn(sh.batch, sh.nheads, sh.dv, sh.dk, device=dev, generator=g).mul_(0.1)
-    cache = rs.gdn_cache(dims, ckpt=S0, device=dev)
-    state = S0.clone()
-    gp = []
-    for t in range(8):
-        st = gen.gdn_step_inputs(sh, w.seed, t)
-        gp.append(tuple(torch.from_numpy(a).to(torch.bfloat16).to(dev) for a in (st.q, st.k, st.v))
-                  + (torch.from_numpy(st.alpha).to(dev), torch.from_numpy(st.beta).to(dev)))
-    o = torch.empty(sh.batch, sh.nheads, sh.dv, device=dev)
-    for t in range(warmup):
-        rs.gdn_decode(cache, *gp[t % 8], o=o)
-    torch.cuda.synchronize(dev)
-    gu = bm.gdn_units(sh.nheads, sh.dk, sh.dv)
-    ln = int(cache.ring_len[0].item())
-    K = (steps // sh.L) * sh.L
-    alg = 0
-    for _ in range(K):
-        alg += bm.gdn_replay_decode(gu, ln, sh.L) * sh.batch
-        ln = 0 if ln + 1 >= sh.L else ln + 1
-    ms = _timed(stream, lambda t: rs.gdn_decode(cache, *gp[t % 8], o=o), K)
-    ms_c = _timed(stream, lambda t: rs.gdn_conventional_decode(dims, state, *gp[t % 8], o=o), K)
-    assert int(cache.err.item()) == 0
-    out["gdn_decode_b256"] = {"us_per_step": round(ms * 1e3 / K, 1), "seq_tok_s": round(sh.batch * K / (ms / 1e3), 1),
-                              "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1),
-                              "conventional_us_per_step": round(ms_c * 1e3 / K, 1),
-                              "replay_speedup": round(ms_c / ms, 3)}
+    if "gdn" in which:
+        # ---- Gated DeltaNet, batch 256
+        w = wl["gdn_b256"]
+        sh = w.shape
+        dims = rs.gdn_dims(sh.batch, sh.nheads, sh.dk, sh.dv, sh.L)
+        S0 = torch.randn(sh.batch, sh.nheads, sh.dv, sh.dk, device=dev, generator=g).mul_(0.1)
+        cache = rs.gdn_cache(dims, ckpt=S0, device=dev)
+        state = S0.clone()
+        gp = []
+        for t in range(8):
+            st = gen.gdn_step_inputs(sh, w.seed, t)
+            gp.append(tuple(torch.from_numpy(a).to(torch.bfloat16).to(dev) for a in (st.q, st.k, st.v))
+                      + (torch.from_numpy(st.alpha).to(dev), torch.from_numpy(st.beta).to(dev)))
+        o = torch.empty(sh.batch, sh.nheads, sh.dv, device=dev)
+        for t in range(warmup):
+            rs.gdn_decode(cache, *gp[t % 8], o=o)
+        torch.cuda.synchronize(dev)
+        gu = bm.gdn_units(sh.nheads, sh.dk, sh.dv)
+        ln = int(cache.ring_len[0].item())
+        K = (steps // sh.L) * sh.L
+        alg = 0
+        for _ in range(K):
+            alg += bm.gdn_replay_decode(gu, ln, sh.L) * sh.batch
+            ln = 0 if ln + 1 >= sh.L else ln + 1
+        ms = _timed(stream, lambda t: rs.gdn_decode(cache, *gp[t % 8], o=o), K)
+        ms_c = _timed(stream, lambda t: rs.gdn_conventional_decode(dims, state, *gp[t % 8], o=o), K)
+        assert int(cache.err.item()) == 0
+        out["gdn_decode_b256"] = {"us_per_step": round(ms * 1e3 / K, 1), "seq_tok_s": round(sh.batch * K / (ms / 1e3), 1),
+                                  "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1),
+                                  "conventional_us_per_step": round(ms_c * 1e3 / K, 1),
+                                  "replay_speedup": round(ms_c / ms, 3)}
     return out
 
 
@@ -539,6 +546,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the FP8 / verify / GDN rows")
     ap.add_argument("--row-steps", type=int, default=128)
+    ap.add_argument("--row", choices=ROWS, default="",
+                    help="run only this row (FP8-read decode, verify, GDN) and print it")
     ap.add_argument("--sweep", type=str, default="",
                     help="comma-separated batch sizes: replay vs conventional table instead of the bench line")
     args = ap.parse_args()
@@ -552,6 +561,15 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.row:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        from ssm_decode_state_gb300 import replayssm as rs
+        dev = torch.device("cuda", local_rank)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"rows": measure_rows(rs, dev, args.row_steps, args.warmup, (args.row,))}), flush=True)
         return
     if world > 1:
         import torch

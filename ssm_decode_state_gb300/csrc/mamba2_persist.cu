@@ -25,7 +25,9 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
         if ((long long)d->batch * d->nheads / c >= 12LL * sms || c == 1) { hpi = c; break; }
     }
     const long long items = (long long)d->batch * d->nheads / hpi;
-    if (items < 2LL * sms || items > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;
+    // every batch: at batches 1-2 (fewer items than SMs) the persistent kernel still
+    // beats the per-tile kernel (7.4 vs 15.0 us at batch 1, 9.0 vs 12.1 at batch 2)
+    if (items < 1 || items > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;
     const int grid = (int)(items < sms ? items : sms);
     const int max_my = (int)((items + grid - 1) / grid);   // ring pointers of these are kept in smem
     if (max_my > 2048) return RSSM_ERR_UNSUPPORTED;

@@ -489,33 +489,39 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 const uint32_t *q = reinterpret_cast<const uint32_t *>(stg);
                 const float *sc = reinterpret_cast<const float *>(stg + Q8 * P * N);
                 uint32_t qc[Q8][VPT];
-                float rsc[Q8];
 #pragma unroll
                 for (int hq = 0; hq < Q8; ++hq) {
 #pragma unroll
                     for (int v = 0; v < VPT; ++v) qc[hq][v] = q[hq * (P * N / 4) + ctid + v * kPConsumers];
-                    rsc[hq] = sc[hq * P + cw + RSTEP * reduced_index<G4, VPT>(0)];
+                }
+                // the row scale of the (head, row) this lane ends up with after the reduction
+                float rsv;
+                {
+                    const int vi = reduced_index<G4, Q8 * VPT>(0), hq = vi / VPT;
+                    rsv = sc[hq * P + cw + RSTEP * (vi - hq * VPT)];
                 }
                 __syncwarp();                            // the warp is done with the stage
                 if (lane == 0) mbar_arrive(empty + s);
                 if (!work) continue;
+                // codes enter the dot at 2^-120 of their value; the Q8 x 8 row sums of the
+                // stage go through one transposed reduction, then each is scaled back
+                // (exactly) and by its row scale
+                float part[Q8 * VPT];
 #pragma unroll
                 for (int hq = 0; hq < Q8; ++hq) {
-                    // codes enter the dot at 2^-120 of their value; the row sum is scaled
-                    // back (exactly) and by the row scale after the warp reduction
-                    float part[VPT];
 #pragma unroll
                     for (int v = 0; v < VPT; ++v) {
                         uint32_t ev, od;
                         e4m3_to_bf16_pairs(qc[hq][v], ev, od);
-                        part[v] = fma_bf16_pair(od, co, fma_bf16_pair(ev, ce, 0.0f));
+                        part[hq * VPT + v] = fma_bf16_pair(od, co, fma_bf16_pair(ev, ce, 0.0f));
                     }
-                    group_reduce<G4, VPT>(part);
-                    if (reduced_writer<G4, VPT>()) {
-                        const int hh = uu * Q8 + hq, row = cw + RSTEP * reduced_index<G4, VPT>(0);
-                        a.y[((size_t)b * H + h0 + hh) * P + row] =
-                            fmaf(dec[hh], (part[0] * 0x1p120f) * rsc[hq], rt[hh * P + row]);
-                    }
+                }
+                group_reduce<G4, Q8 * VPT>(part);
+                if (reduced_writer<G4, Q8 * VPT>()) {
+                    const int vi = reduced_index<G4, Q8 * VPT>(0), hq = vi / VPT;
+                    const int hh = uu * Q8 + hq, row = cw + RSTEP * (vi - hq * VPT);
+                    a.y[((size_t)b * H + h0 + hh) * P + row] =
+                        fmaf(dec[hh], (part[0] * 0x1p120f) * rsv, rt[hh * P + row]);
                 }
             }
         } else {

@@ -19,7 +19,7 @@
 //    consumers, append the token to the ring, B_j . C_t, the decay weights and
 //    the record term of every row, into triple-buffered item arrays handed
 //    over through mbarriers.
-//  * consumer warps (warps 2..): per stage, each warp reads its own rows,
+//  * consumer warps (warps 2..): per stage, each warp reads its own 8 rows,
 //    frees the stage, reduces the row dot products with C_t across its lanes
 //    and writes y = exp(A S) (h_c . C_t) + record term; on flush steps it folds
 //    h_c <- exp(A S) h_c + sum_j w_j x_j B_j^T into its rows and stores them
@@ -97,10 +97,9 @@ __global__ void __launch_bounds__(persist_decode_threads(P * N / 4 / VPT), 1)
 m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     constexpr int kPConsumers = P * N / 4 / VPT;         // consumer threads
     constexpr int G4 = N / 4;                            // lanes per row
-    constexpr int RSTEP = kPConsumers / G4;              // rows between a thread's consecutive float4s
     constexpr int CX = P / 8, CB = N / 8;                // 16-byte chunks per x / B row
     constexpr int Q8 = persist_q8(HPI);                  // heads per stage of FP8 codes
-    static_assert(G4 == 32, "a warp owns whole rows");
+    static_assert(G4 == 32 && VPT == 8 && kPConsumers / 32 * VPT == P, "a warp owns 8 whole consecutive rows");
     extern __shared__ __align__(128) unsigned char smraw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = a.L, H = a.H, G = a.G, hpg = a.hpg, KM = L + 1;
@@ -427,7 +426,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
 
     // ================================ consumer warps =================================
     const int ctid = tid - 64;                           // 0..255
-    const int cw = ctid >> 5;                            // consumer warp: owns rows cw + RSTEP * v
+    const int cw = ctid >> 5;                            // consumer warp: owns rows cw * VPT + v
     const int col4 = lane;                               // this lane's 4 columns
     bool live = true;                                    // false once any wait gave up
 
@@ -469,7 +468,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             }
             group_reduce<G4, VPT>(part);
             if (reduced_writer<G4, VPT>()) {
-                const int row = cw + RSTEP * reduced_index<G4, VPT>(0);
+                const int row = cw * VPT + reduced_index<G4, VPT>(0);
                 a.y[((size_t)b * H + h0 + hh) * P + row] = fmaf(dec[hh], part[0], rt[hh * P + row]);
             }
         };
@@ -492,13 +491,13 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
 #pragma unroll
                 for (int hq = 0; hq < Q8; ++hq) {
 #pragma unroll
-                    for (int v = 0; v < VPT; ++v) qc[hq][v] = q[hq * (P * N / 4) + ctid + v * kPConsumers];
+                    for (int v = 0; v < VPT; ++v) qc[hq][v] = q[hq * (P * N / 4) + (cw * VPT + v) * G4 + lane];
                 }
                 // the row scale of the (head, row) this lane ends up with after the reduction
                 float rsv;
                 {
                     const int vi = reduced_index<G4, Q8 * VPT>(0), hq = vi / VPT;
-                    rsv = sc[hq * P + cw + RSTEP * (vi - hq * VPT)];
+                    rsv = sc[hq * P + cw * VPT + (vi - hq * VPT)];
                 }
                 __syncwarp();                            // the warp is done with the stage
                 if (lane == 0) mbar_arrive(empty + s);
@@ -519,7 +518,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 group_reduce<G4, Q8 * VPT>(part);
                 if (reduced_writer<G4, Q8 * VPT>()) {
                     const int vi = reduced_index<G4, Q8 * VPT>(0), hq = vi / VPT;
-                    const int hh = uu * Q8 + hq, row = cw + RSTEP * (vi - hq * VPT);
+                    const int hh = uu * Q8 + hq, row = cw * VPT + (vi - hq * VPT);
                     a.y[((size_t)b * H + h0 + hh) * P + row] =
                         fmaf(dec[hh], (part[0] * 0x1p120f) * rsv, rt[hh * P + row]);
                 }
@@ -534,7 +533,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 const float4 *stg = reinterpret_cast<const float4 *>(stages + s * lay.stage_bytes);
                 float4 hv[VPT];
 #pragma unroll
-                for (int v = 0; v < VPT; ++v) hv[v] = stg[ctid + v * kPConsumers];
+                for (int v = 0; v < VPT; ++v) hv[v] = stg[(cw * VPT + v) * G4 + lane];
                 __syncwarp();                            // the warp is done with the stage
                 if (lane == 0) mbar_arrive(empty + s);
                 if (!work) continue;
@@ -543,7 +542,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                     const float *wh = w + hh * KM;
                     const uint16_t *xh = r_x + hh * KM * P;
                     for (int idx = lane; idx < nrec * VPT; idx += 32) {
-                        const int j = idx / VPT, v = idx - j * VPT, row = cw + RSTEP * v;
+                        const int j = idx / VPT, v = idx - j * VPT, row = cw * VPT + v;
                         s_wx[j * P + row] = wh[j] * bf16_at(xh, j * P + row);
                     }
                     __syncwarp();
@@ -559,10 +558,13 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                         const uint2 braw = *reinterpret_cast<const uint2 *>(r_B + j * N + col4 * 4);
                         const unsigned long long b01 = f2pack(bf16lo(braw.x), bf16hi(braw.x));
                         const unsigned long long b23 = f2pack(bf16lo(braw.y), bf16hi(braw.y));
+                        // the warp's 8 consecutive rows: two 16-byte broadcast loads
+                        const float4 wa = *reinterpret_cast<const float4 *>(s_wx + j * P + cw * VPT);
+                        const float4 wb = *reinterpret_cast<const float4 *>(s_wx + j * P + cw * VPT + 4);
+                        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
                         for (int v = 0; v < VPT; ++v) {
-                            const float c = s_wx[j * P + cw + RSTEP * v];
-                            const unsigned long long cc = f2pack(c, c);
+                            const unsigned long long cc = f2pack(wv[v], wv[v]);
                             acc01[v] = fma2(cc, b01, acc01[v]);
                             acc23[v] = fma2(cc, b23, acc23[v]);
                         }
@@ -575,7 +577,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                     for (int v = 0; v < VPT; ++v) {
                         f2unpack(fma2(dd, f2pack(hv[v].x, hv[v].y), acc01[v]), o[v].x, o[v].y);
                         f2unpack(fma2(dd, f2pack(hv[v].z, hv[v].w), acc23[v]), o[v].z, o[v].w);
-                        st_stream(ckp + ctid + v * kPConsumers, o[v]);
+                        st_stream(ckp + (cw * VPT + v) * G4 + lane, o[v]);
                     }
                     if (q8) {
                         uint32_t q[VPT];
@@ -583,8 +585,8 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                         e4m3_quantize_rows<VPT>(o, q, rs);
                         uint32_t *ckq = reinterpret_cast<uint32_t *>(a.ckpt_q + tile * N);
 #pragma unroll
-                        for (int v = 0; v < VPT; ++v) ckq[ctid + v * kPConsumers] = q[v];
-                        if (reduced_writer<32, VPT>()) a.ckpt_scale[tile + cw + RSTEP * reduced_index<32, VPT>(0)] = rs;
+                        for (int v = 0; v < VPT; ++v) ckq[(cw * VPT + v) * G4 + lane] = q[v];
+                        if (reduced_writer<32, VPT>()) a.ckpt_scale[tile + cw * VPT + reduced_index<32, VPT>(0)] = rs;
                     }
                     __syncwarp();                        // s_wx is rewritten for the next head
                 }

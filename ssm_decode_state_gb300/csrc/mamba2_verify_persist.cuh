@@ -320,43 +320,54 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
                     }
                     fdec[hh] = expf(s_A[h0 + hh] * acc);
                 }
-                // B_j . C_i for every draft i and record j <= len + i: a warp per pair
-                // (lane-strided products, butterfly sum), four pairs at a time per warp
-                for (int pb0 = pw * 4; pb0 < T * KM; pb0 += 8) {
-                    float acc[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int pr = pb0 + q, i = pr / KM, j = pr - i * KM;
-                        const bool valid = pr < T * KM && j <= ln + i;
-                        acc[q] = 0.0f;
-                        const int jj = valid ? j : 0, ii = valid ? i : 0;
-#pragma unroll
-                        for (int n = lane; n < N; n += 32)
-                            acc[q] = fmaf(bf16_at(r_B, jj * N + n), bf16_at(r_C, ii * N + n), acc[q]);
+                // B_j . C_i for every draft i and record j <= len + i (the valid pairs only,
+                // draft-major): 8 lanes per pair, 16 columns per lane as bf16 pairs, then a
+                // 3-level butterfly; each warp takes 4 pairs at a time
+                const int npairs = T * (ln + 1) + T * (T - 1) / 2;
+                for (int pb0 = pw * 4; pb0 < npairs; pb0 += 8) {
+                    const int pr = pb0 + (lane >> 3);
+                    const bool valid = pr < npairs;
+                    int i = 0, j = pr;
+                    while (valid && j >= ln + 1 + i) {
+                        j -= ln + 1 + i;
+                        ++i;
                     }
-#pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+                    float acc = 0.0f;
+                    if (valid) {
+                        const int c0 = (lane & 7) * 16;
+                        const uint4 b0 = *reinterpret_cast<const uint4 *>(r_B + j * N + c0);
+                        const uint4 b1 = *reinterpret_cast<const uint4 *>(r_B + j * N + c0 + 8);
+                        const uint4 q0 = *reinterpret_cast<const uint4 *>(r_C + i * N + c0);
+                        const uint4 q1 = *reinterpret_cast<const uint4 *>(r_C + i * N + c0 + 8);
+                        acc = fma_bf16_pair(b0.x, q0.x, acc);
+                        acc = fma_bf16_pair(b0.y, q0.y, acc);
+                        acc = fma_bf16_pair(b0.z, q0.z, acc);
+                        acc = fma_bf16_pair(b0.w, q0.w, acc);
+                        acc = fma_bf16_pair(b1.x, q1.x, acc);
+                        acc = fma_bf16_pair(b1.y, q1.y, acc);
+                        acc = fma_bf16_pair(b1.z, q1.z, acc);
+                        acc = fma_bf16_pair(b1.w, q1.w, acc);
                     }
-                    if (lane < 4) {
-                        const int pr = pb0 + lane, i = pr / KM, j = pr - i * KM;
-                        float v = acc[0];
-#pragma unroll
-                        for (int q = 1; q < 4; ++q) v = lane == q ? acc[q] : v;
-                        if (pr < T * KM && j <= ln + i) s_cb[pr] = v;
-                    }
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+                    if (valid && (lane & 7) == 0) s_cb[i * KM + j] = acc;
                 }
             }
             prep_sync();                                 // suffix sums and B . C
             if (work) {
-                // query weights times B_j . C_i, and the pre-flush fold weights
-                for (int idx = ptid; idx < HPI * T * KM; idx += kPrepThreads) {
-                    const int hh = idx / (T * KM), rr = idx - hh * T * KM, i = rr / KM, j = rr - i * KM;
-                    if (j <= ln + i) {
-                        const float wv = expf(s_A[h0 + hh] * s_sfx[idx]) * r_dt[hh * KM + j];
-                        s_wcb[idx] = wv * s_cb[i * KM + j];
+                // query weights times B_j . C_i (valid pairs only), and the pre-flush fold weights
+                const int npairs = T * (ln + 1) + T * (T - 1) / 2;
+                for (int idx = ptid; idx < HPI * npairs; idx += kPrepThreads) {
+                    const int hh = idx / npairs;
+                    int i = 0, j = idx - hh * npairs;
+                    while (j >= ln + 1 + i) {
+                        j -= ln + 1 + i;
+                        ++i;
                     }
+                    const int e = (hh * T + i) * KM + j;
+                    const float wv = expf(s_A[h0 + hh] * s_sfx[e]) * r_dt[hh * KM + j];
+                    s_wcb[e] = wv * s_cb[i * KM + j];
                 }
                 if (pre) {
                     for (int idx = ptid; idx < HPI * ln; idx += kPrepThreads) {

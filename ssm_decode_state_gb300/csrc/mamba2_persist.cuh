@@ -351,28 +351,30 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                     }
                     sf[KM] = acc;
                 }
-                // B_j . C_t, a warp per record (lane-strided products, butterfly sum),
-                // four records at a time per warp
+                // B_j . C_t: 8 lanes per record, 16 columns per lane as bf16 pairs, then a
+                // 3-level butterfly; each warp takes 4 records at a time
                 for (int jb = pw * 4; jb < nrec; jb += 8) {
-                    float acc[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[q] = 0.0f;
-                        const int j = jb + q < nrec ? jb + q : 0;
-#pragma unroll
-                        for (int n = lane; n < N; n += 32) acc[q] = fmaf(bf16_at(r_B, j * N + n), bf16_at(r_C, n), acc[q]);
+                    const int j = jb + (lane >> 3);
+                    float acc = 0.0f;
+                    if (j < nrec) {
+                        const int c0 = (lane & 7) * 16;
+                        const uint4 b0 = *reinterpret_cast<const uint4 *>(r_B + j * N + c0);
+                        const uint4 b1 = *reinterpret_cast<const uint4 *>(r_B + j * N + c0 + 8);
+                        const uint4 q0 = *reinterpret_cast<const uint4 *>(r_C + c0);
+                        const uint4 q1 = *reinterpret_cast<const uint4 *>(r_C + c0 + 8);
+                        acc = fma_bf16_pair(b0.x, q0.x, acc);
+                        acc = fma_bf16_pair(b0.y, q0.y, acc);
+                        acc = fma_bf16_pair(b0.z, q0.z, acc);
+                        acc = fma_bf16_pair(b0.w, q0.w, acc);
+                        acc = fma_bf16_pair(b1.x, q1.x, acc);
+                        acc = fma_bf16_pair(b1.y, q1.y, acc);
+                        acc = fma_bf16_pair(b1.z, q1.z, acc);
+                        acc = fma_bf16_pair(b1.w, q1.w, acc);
                     }
-#pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
-                    }
-                    if (lane < 4 && jb + lane < nrec) {
-                        float v = acc[0];
-#pragma unroll
-                        for (int q = 1; q < 4; ++q) v = lane == q ? acc[q] : v;
-                        cb[jb + lane] = v;
-                    }
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+                    if (j < nrec && (lane & 7) == 0) cb[j] = acc;
                 }
             }
             prep_sync();                                 // S_j and B_j . C_t

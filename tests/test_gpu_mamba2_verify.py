@@ -273,3 +273,25 @@ def test_persistent_verify_fp8_copy_preflush():
     mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e.astype(np.float64) - 7))
     dq = sign * mag * sc[..., None]
     assert np.all(np.abs(dq - ck) <= 2.0 ** -4 * np.abs(ck) + 2.0 ** -10 * sc[..., None] + 1e-6 * np.abs(ck))
+
+
+def test_persistent_verify_bad_ring_pointers():
+    """Serving head shape at batch 128 (the persistent verify): a sequence with
+    invalid ring pointers is flagged and left untouched (checkpoint, records,
+    pointers); the other sequences take their drafts."""
+    from ssm_decode_state_gb300 import replayssm as rs
+    from tests.m2_runner import M2Run
+    shape = gen.Mamba2Shape(batch=128, nheads=128, headdim=64, dstate=128, ngroups=8, L=8)
+    r = M2Run(shape, 17, h0=gen.mamba2_random_state(shape, 17), sample=[0], conventional=False)
+    r.decode(0)
+    r.cache.ring_head[5] = 8                               # >= L
+    before = r.cache.ckpt[5].clone()
+    rx = r.cache.rec_x[5].clone()
+    d = gen.mamba2_draft_inputs(shape, r.params, 17, 1, 4)
+    rs.verify(r.cache, to_dev(d.dt), to_dev(d.x, torch.bfloat16), to_dev(d.B, torch.bfloat16),
+              to_dev(d.C, torch.bfloat16))
+    torch.cuda.synchronize()
+    assert int(r.cache.err.item()) & rs.DEVERR_RING_META
+    assert r.cache.ring_head[5].item() == 8 and r.cache.ring_len[5].item() == 1
+    assert torch.equal(r.cache.ckpt[5], before) and torch.equal(r.cache.rec_x[5], rx)
+    assert r.cache.ring_len[0].item() == 5 and not r.cache.arrive.any().item()

@@ -90,6 +90,7 @@ def _decode(rs, dims, cache, x=FAKE):
 
 def test_null_and_shape_errors(rs):
     assert _decode(rs, None, _cache(rs)) == 1
+    assert _decode(rs, _m2(rs, batch=0), _cache(rs)) == 3          # empty batch: rejected, nothing enqueued
     assert _decode(rs, _m2(rs, dstate=48), _cache(rs)) == 3
     assert _decode(rs, _m2(rs, headdim=12), _cache(rs)) == 3
     assert _decode(rs, _m2(rs, nheads=6, ngroups=4), _cache(rs)) == 3

@@ -47,12 +47,20 @@ def test_dstate_headdim_variants(N, P):
     _run(shape, 5, 20, h0=h0)
 
 
-def test_batch_one_split_rows():
-    """Batch 1 at the serving head shape: the rows of a head are split over
-    several CTAs to fill the GPU."""
+def test_batch_one_serving_shape():
+    """Batch 1 at the serving head shape: the persistent kernel with one head per
+    work item and fewer CTAs than SMs."""
     shape = gen.Mamba2Shape(batch=1, nheads=128, headdim=64, dstate=128, ngroups=8, L=16)
     h0 = gen.mamba2_random_state(shape, 9)
     _run(shape, 9, 34, h0=h0)
+
+
+def test_batch_one_split_rows():
+    """Batch 1 at a shape the per-tile kernel serves (headdim 128, dstate 64):
+    the rows of a head are split over several CTAs to fill the GPU."""
+    shape = gen.Mamba2Shape(batch=1, nheads=16, headdim=128, dstate=64, ngroups=4, L=8)
+    h0 = gen.mamba2_random_state(shape, 19)
+    _run(shape, 19, 20, h0=h0)
 
 
 def test_serving_shape_b256_sampled():

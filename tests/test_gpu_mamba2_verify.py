@@ -218,7 +218,7 @@ def test_snapshot_slot_bounds_and_select():
     assert slot.cpu().tolist() == [3, 1, 1] and err.item() == rs.DEVERR_ROLLBACK
 
 
-@pytest.mark.parametrize("T,L", [(1, 8), (3, 8), (4, 8), (4, 16)])
+@pytest.mark.parametrize("T,L", [(1, 8), (3, 8), (4, 8), (4, 16), (4, 4)])
 def test_persistent_verify_variants(T, L):
     """Serving head shape at batch 128 (the persistent verify): 1-4 drafts, rings
     of 8 (pre-flush every couple of steps) and 16; outputs against the oracle,

@@ -42,3 +42,28 @@ class GDNStepwise:
         """One decode token for every sequence; returns o [b, H, dv]."""
         self.S, o = self._update(self.S, q, k, v, alpha, beta)
         return o
+
+    def verify(self, q, k, v, alpha, beta):
+        """Score T draft tokens per sequence (inputs [b, T, H, ...]) without
+        committing: draft i is decoded on top of drafts 1..i, as speculative
+        decoding scores them (AT Pulse, Technical analysis: output-only
+        evaluation of the drafts; rollback keeps the accepted prefix).
+
+        Returns (o [b, T, H, dv], states) where states[i] is the state after
+        drafts 1..i+1; ``accept`` keeps one of them per sequence."""
+        T = np.asarray(alpha).shape[1]
+        S = self.S
+        outs, states = [], []
+        for i in range(T):
+            S, o = self._update(S, q[:, i], k[:, i], v[:, i], alpha[:, i], beta[:, i])
+            outs.append(o)
+            states.append(S)
+        return np.stack(outs, axis=1), states
+
+    def accept(self, states, accepted) -> None:
+        """Keep, per sequence, the state after its accepted prefix (0 = unchanged)."""
+        new = self.S.copy()
+        for b, a in enumerate(np.asarray(accepted)):
+            if a > 0:
+                new[b] = states[a - 1][b]
+        self.S = new

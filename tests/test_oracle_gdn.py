@@ -98,3 +98,56 @@ def test_unrolled_u_chain():
                     acc += beta[j, bb, h] * d * v[j, bb, h]
                     u = alpha[j, bb, h] * (u - beta[j, bb, h] * k[j, bb, h] * d)
                 np.testing.assert_allclose(o[bb, h], S0[bb, h] @ u + acc, rtol=1e-11, atol=1e-12)
+
+
+def _draft_batch(rng, b=3, H=2, dk=6, dv=5, T=4):
+    S0, q, k, v, alpha, beta = _rand(rng, b=b, H=H, dk=dk, dv=dv, T=T)
+    # [T, b, ...] -> [b, T, ...]
+    sw = lambda a: np.swapaxes(a, 0, 1)  # noqa: E731
+    return S0, sw(q), sw(k), sw(v), sw(alpha), sw(beta)
+
+
+def test_verify_equals_sequential_steps_and_commits_nothing():
+    """Draft i's output is the output of decoding drafts 1..i one by one; the
+    oracle's state is untouched until accept."""
+    rng = np.random.default_rng(31)
+    S0, q, k, v, alpha, beta = _draft_batch(rng)
+    m = GDNStepwise(S0)
+    o, states = m.verify(q, k, v, alpha, beta)
+    np.testing.assert_array_equal(m.S, S0)
+    ref = GDNStepwise(S0)
+    for i in range(q.shape[1]):
+        oi = ref.step(q[:, i], k[:, i], v[:, i], alpha[:, i], beta[:, i])
+        np.testing.assert_allclose(o[:, i], oi, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(states[i], ref.S, rtol=1e-13, atol=1e-14)
+
+
+def test_verify_accept_prefix_matches_dense_products():
+    """Accepting a drafts leaves S_0 (prod_i A_i) + (written terms) of exactly
+    those a drafts, built here from dense (I - beta k k^T) products; a = 0
+    keeps the state."""
+    rng = np.random.default_rng(32)
+    S0, q, k, v, alpha, beta = _draft_batch(rng, b=4, T=3)
+    m = GDNStepwise(S0)
+    _, states = m.verify(q, k, v, alpha, beta)
+    accepted = np.array([0, 1, 3, 2])
+    m.accept(states, accepted)
+    for b, a in enumerate(accepted):
+        for h in range(S0.shape[1]):
+            S = S0[b, h].copy()
+            for i in range(a):
+                kk = k[b, i, h][:, None]
+                M = np.eye(S.shape[1]) - beta[b, i, h] * (kk @ kk.T)
+                S = alpha[b, i, h] * S @ M + beta[b, i, h] * v[b, i, h][:, None] @ kk.T
+            np.testing.assert_allclose(m.S[b, h], S, rtol=1e-12, atol=1e-13)
+
+
+def test_verify_single_draft_is_step():
+    rng = np.random.default_rng(33)
+    S0, q, k, v, alpha, beta = _draft_batch(rng, T=1)
+    a, b_ = GDNStepwise(S0), GDNStepwise(S0)
+    o, states = a.verify(q, k, v, alpha, beta)
+    a.accept(states, np.ones(S0.shape[0], int))
+    ob = b_.step(q[:, 0], k[:, 0], v[:, 0], alpha[:, 0], beta[:, 0])
+    np.testing.assert_array_equal(o[:, 0], ob)
+    np.testing.assert_array_equal(a.S, b_.S)

@@ -98,3 +98,30 @@ def test_gdn_pins_catch(monkeypatch, mutant):
     gdn_mod.GDNStepwise._orig = gdn_mod.GDNStepwise._update
     monkeypatch.setattr(gdn_mod.GDNStepwise, "_update", mutant)
     assert _run_pins(gdn_pins) > 0
+
+
+def _gdn_verify_mutants():
+    def drafts_not_causal(self, q, k, v, alpha, beta):
+        T = np.asarray(alpha).shape[1]
+        outs, states = [], []
+        for i in range(T):                       # every draft scored from the checkpoint alone
+            S, o = self._update(self.S, q[:, i], k[:, i], v[:, i], alpha[:, i], beta[:, i])
+            outs.append(o)
+            states.append(S)
+        return np.stack(outs, axis=1), states
+
+    def accept_off_by_one(self, states, accepted):
+        new = self.S.copy()
+        for b, a in enumerate(np.asarray(accepted)):
+            if a > 0:
+                new[b] = states[min(a, len(states) - 1)][b]
+        self.S = new
+
+    return [("verify", drafts_not_causal), ("accept", accept_off_by_one)]
+
+
+@pytest.mark.parametrize("mutant", _gdn_verify_mutants(), ids=lambda m: m[1].__name__)
+def test_gdn_verify_pins_catch(monkeypatch, mutant):
+    attr, fn = mutant
+    monkeypatch.setattr(gdn_mod.GDNStepwise, attr, fn)
+    assert _run_pins(gdn_pins) > 0

@@ -280,6 +280,35 @@ rssm_status replayssm_gdn_decode(const rssm_gdn_dims *dims, const rssm_gdn_cache
 rssm_status replayssm_gdn_flush(const rssm_gdn_dims *dims, const rssm_gdn_cache *cache,
                                 const uint8_t *mask, void *stream);
 
+/*
+ * GDN speculative verify (AT Pulse, Technical analysis: the drafts are scored by
+ * output-only evaluation from the checkpoint and the buffered inputs; Capabilities
+ * and access: the method's kernels cover speculative decoding): draft i of each
+ * sequence is scored causally from the checkpoint, the buffered records and drafts
+ * 1..i, i.e. o_i = S_c u_0 + sum_j beta_j (k_j . u_j) v_j with the backward chain
+ * started from q_i at draft i.  Nothing is folded on account of the drafts; when
+ * ring_len + T > L the buffered records are first folded into the checkpoint (the
+ * pre-flush) so that the T drafts fit.  The drafts' records are appended and
+ * ring_len grows by T (a second, small kernel writes them after the first, because
+ * on a pre-flush they land on slots the first still reads).
+ * T in 1..8 and T <= L; q, k [batch][T][nheads][dk] bf16; v [batch][T][nheads][dv]
+ * bf16; alpha, beta [batch][T][nheads] f32; o [batch][T][nheads][dv] f32.
+ * Errors: RSSM_ERR_RING for T out of range, otherwise as replayssm_gdn_decode.
+ */
+rssm_status replayssm_gdn_verify(const rssm_gdn_dims *dims, const rssm_gdn_cache *cache, int32_t T,
+                                 const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                 const float *alpha, const float *beta, float *o, void *stream);
+
+/*
+ * GDN rollback after a verify of T drafts (AT Pulse, Technical analysis: rollback is
+ * a buffer-pointer move): ring_len[b] -= T - accepted[b], accepted [batch] int32 in
+ * 0..T on the device.  A sequence whose accepted count is out of range, or whose ring
+ * holds fewer than T - accepted records, is left as it is and RSSM_DEVERR_ROLLBACK is
+ * set in the error word.
+ */
+rssm_status replayssm_gdn_rollback(const rssm_gdn_dims *dims, const rssm_gdn_cache *cache, int32_t T,
+                                   const int32_t *accepted, void *stream);
+
 /* GDN conventional in-place decode of state [batch][nheads][dv][dk] f32. */
 rssm_status replayssm_gdn_conventional_decode(const rssm_gdn_dims *dims, float *state,
                                               const uint16_t *q, const uint16_t *k,

@@ -22,7 +22,7 @@ namespace {
 enum { gDecode = 0, gFlush = 2 };
 
 struct GArgs {
-    int H, DK, DV, L, R, split;
+    int H, DK, DV, L, R, split, T;
     float *ckpt;
     uint16_t *rec_k, *rec_v;
     float *rec_alpha, *rec_beta;
@@ -258,6 +258,220 @@ __global__ void __launch_bounds__(256) gdn_replay_kernel(const GArgs a) {
     }
 }
 
+// Speculative verify of T drafts.  Records j < len come from the ring, j = len + i is
+// draft i (from the inputs).  Warp i runs draft i's backward chain from q_i at record
+// len + i; every row's dot products with the T vectors u_0 are reduced once the
+// checkpoint tile is in registers; a pre-flush folds the len buffered records into
+// the rows (the flush's arithmetic) and stores them.  The last CTA of a sequence
+// commits its ring pointers; gdn_verify_append writes the drafts' records afterwards.
+struct GVSmem {
+    int al, be, coef, k, v, q, u, o, total;
+    __host__ __device__ GVSmem(int L, int T, int R, int DK) {
+        const int KM = L + T;
+        int off = 0;
+        auto take = [&off](int n) { const int at = off; off += (n + 3) & ~3; return at; };
+        al = take(KM); be = take(KM); coef = take(T * KM);
+        k = take(KM * DK); v = take(KM * R);
+        q = take(T * DK); u = take(T * DK); o = take(T * R);
+        total = off;
+    }
+};
+
+template <int DK, int VPT>
+__global__ void __launch_bounds__(256) gdn_verify_kernel(const GArgs a) {
+    constexpr int G4 = DK / 4;
+    extern __shared__ float4 smem4[];
+    float *sm = reinterpret_cast<float *>(smem4);
+    const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.y;
+    const int h = blockIdx.x / a.split, sp = blockIdx.x - h * a.split;
+    const int R = a.R, L = a.L, H = a.H, DV = a.DV, T = a.T;
+    const int p0 = sp * R;
+
+    const int head = a.ring_head[b], len = a.ring_len[b];
+    if (head < 0 || head >= L || len < 0 || len > L) {
+        if (blockIdx.x == 0 && tid == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
+        return;
+    }
+    const bool pre = len + T > L;
+    const int nrec = len + T, KM = L + T;
+
+    const size_t tile = ((size_t)b * H + h) * DV + p0;
+    float4 *ck4 = reinterpret_cast<float4 *>(a.ckpt + tile * DK);
+    float4 hv[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) hv[v] = ld_stream(ck4 + tid + v * nthr);
+
+    const GVSmem lay(L, T, R, DK);
+    float *s_al = sm + lay.al, *s_be = sm + lay.be, *s_coef = sm + lay.coef;
+    float *s_k = sm + lay.k, *s_v = sm + lay.v, *s_q = sm + lay.q, *s_u = sm + lay.u, *s_o = sm + lay.o;
+
+    // ---- stage the records (ring slots, then the drafts) and the drafts' q
+    const size_t bh = (size_t)b * H + h;
+    const int ck = DK / 8, cv = R / 8;
+    const int nk = nrec * ck, nv = nrec * cv, nq = T * ck, total = nk + nv + nq;
+    for (int idx = tid; idx < total; idx += nthr) {
+        const uint16_t *src;
+        float *dst;
+        if (idx < nk) {
+            const int j = idx / ck, c = idx - j * ck;
+            src = j < len ? a.rec_k + ((bh * L + (head + j) % L) * DK + c * 8)
+                          : a.k + ((((size_t)b * T + (j - len)) * H + h) * DK + c * 8);
+            dst = s_k + j * DK + c * 8;
+        } else if (idx < nk + nv) {
+            const int m = idx - nk, j = m / cv, c = m - j * cv;
+            src = j < len ? a.rec_v + ((bh * L + (head + j) % L) * DV + p0 + c * 8)
+                          : a.v + ((((size_t)b * T + (j - len)) * H + h) * DV + p0 + c * 8);
+            dst = s_v + j * R + c * 8;
+        } else {
+            const int m = idx - nk - nv, i = m / ck, c = m - i * ck;
+            src = a.q + ((((size_t)b * T + i) * H + h) * DK + c * 8);
+            dst = s_q + i * DK + c * 8;
+        }
+        put8(dst, __ldcg(reinterpret_cast<const uint4 *>(src)));
+    }
+    for (int j = tid; j < nrec; j += nthr) {
+        if (j < len) {
+            const size_t r = bh * L + (head + j) % L;
+            s_al[j] = __ldcg(a.rec_alpha + r);
+            s_be[j] = __ldcg(a.rec_beta + r);
+        } else {
+            const size_t r = ((size_t)b * T + (j - len)) * H + h;
+            s_al[j] = __ldcg(a.alpha + r);
+            s_be[j] = __ldcg(a.beta + r);
+        }
+    }
+    __syncthreads();
+
+    // ---- backward chains, one warp per draft: u_0 and beta_j (k_j . u_j)
+    for (int i = warp; i < T; i += nthr / 32) {
+        constexpr int M = (DK + 31) / 32;
+        float u[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const int c = lane + 32 * m;
+            u[m] = c < DK ? s_q[i * DK + c] : 0.0f;
+        }
+        for (int j = len + i; j >= 0; --j) {
+            float d = 0.0f;
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const int c = lane + 32 * m;
+                if (c < DK) d = fmaf(s_k[j * DK + c], u[m], d);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            const float cf = s_be[j] * d;
+            if (lane == 0) s_coef[i * KM + j] = cf;
+            const float al = s_al[j];
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const int c = lane + 32 * m;
+                if (c < DK) u[m] = al * fmaf(-cf, s_k[j * DK + c], u[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const int c = lane + 32 * m;
+            if (c < DK) s_u[i * DK + c] = u[m];
+        }
+    }
+    __syncthreads();
+
+    // ---- checkpoint contraction with every draft's u_0 (before a pre-flush changes hv)
+    const int col4 = tid % G4, row0 = tid / G4, rstep = nthr / G4;
+    for (int i = 0; i < T; ++i) {
+        const float4 u0 = *reinterpret_cast<const float4 *>(s_u + i * DK + col4 * 4);
+        float part[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            float d = hv[v].x * u0.x;
+            d = fmaf(hv[v].y, u0.y, d);
+            d = fmaf(hv[v].z, u0.z, d);
+            d = fmaf(hv[v].w, u0.w, d);
+            part[v] = d;
+        }
+        group_reduce<G4, VPT>(part);
+        if (reduced_writer<G4, VPT>()) {
+            constexpr int NV = (VPT <= G4) ? 1 : VPT / G4;
+#pragma unroll
+            for (int kk = 0; kk < NV; ++kk) s_o[i * R + row0 + reduced_index<G4, VPT>(kk) * rstep] = part[kk];
+        }
+    }
+    // ---- pre-flush: fold the len buffered records into every row, oldest first
+    if (pre) {
+        for (int j = 0; j < len; ++j) {
+            const float4 kj = *reinterpret_cast<const float4 *>(s_k + j * DK + col4 * 4);
+            const float al = s_al[j], be = s_be[j];
+            float d[VPT];
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                float t = hv[v].x * kj.x;
+                t = fmaf(hv[v].y, kj.y, t);
+                t = fmaf(hv[v].z, kj.z, t);
+                t = fmaf(hv[v].w, kj.w, t);
+                d[v] = t;
+            }
+            group_allreduce<G4, VPT>(d);
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const float c = be * fmaf(-al, d[v], s_v[j * R + row0 + v * rstep]);
+                hv[v].x = fmaf(c, kj.x, al * hv[v].x);
+                hv[v].y = fmaf(c, kj.y, al * hv[v].y);
+                hv[v].z = fmaf(c, kj.z, al * hv[v].z);
+                hv[v].w = fmaf(c, kj.w, al * hv[v].w);
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) st_stream(ck4 + tid + v * nthr, hv[v]);
+    }
+    __syncthreads();
+
+    // ---- outputs: o_i[r] = S_c[r] . u_0(i) + sum_{j <= len + i} coef_ij v_j[r]
+    for (int idx = tid; idx < T * R; idx += nthr) {
+        const int i = idx / R, r = idx - i * R;
+        float acc = s_o[i * R + r];
+        for (int j = 0; j <= len + i; ++j) acc = fmaf(s_coef[i * KM + j], s_v[j * R + r], acc);
+        a.o[(((size_t)b * T + i) * H + h) * DV + p0 + r] = acc;
+    }
+
+    // ---- the last CTA of the sequence commits its ring pointers
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(a.arrive + b, 1) == (int)gridDim.x - 1) {
+            __threadfence();
+            a.ring_head[b] = pre ? (head + len) % L : head;
+            a.ring_len[b] = (pre ? 0 : len) + T;
+            a.arrive[b] = 0;
+        }
+    }
+}
+
+// After gdn_verify_kernel: the T drafts' records of every (sequence, head) go to
+// the last T slots of the ring, whose pointers the verify has committed.
+__global__ void gdn_verify_append(const GArgs a) {
+    const int bh = blockIdx.x, b = bh / a.H, h = bh - b * a.H;
+    const int hd = a.ring_head[b], ln = a.ring_len[b], L = a.L, T = a.T, DK = a.DK, DV = a.DV;
+    if (hd < 0 || hd >= L || ln < T || ln > L) return;
+    const int ck = DK / 8, cv = DV / 8;
+    for (int idx = threadIdx.x; idx < T * (ck + cv + 1); idx += blockDim.x) {
+        const int i = idx / (ck + cv + 1), c = idx - i * (ck + cv + 1);
+        const int slot = (hd + ln - T + i) % L;
+        const size_t src = ((size_t)b * T + i) * a.H + h, dst = (size_t)bh * L + slot;
+        if (c < ck) {
+            *reinterpret_cast<uint4 *>(a.rec_k + dst * DK + c * 8) =
+                __ldcg(reinterpret_cast<const uint4 *>(a.k + src * DK + c * 8));
+        } else if (c < ck + cv) {
+            *reinterpret_cast<uint4 *>(a.rec_v + dst * DV + (c - ck) * 8) =
+                __ldcg(reinterpret_cast<const uint4 *>(a.v + src * DV + (c - ck) * 8));
+        } else {
+            a.rec_alpha[dst] = __ldcg(a.alpha + src);
+            a.rec_beta[dst] = __ldcg(a.beta + src);
+        }
+    }
+}
+
 // Conventional in-place step: per row d = s . k; s <- alpha s + beta (v_r -
 // alpha d) k; o_r = s . q.
 template <int DK, int VPT>
@@ -346,6 +560,14 @@ template <int MODE>
 void *pick_replay(int DK, int vpt) {
 #define RSSM_PICK(NN) \
     if (DK == NN) return vpt == 8 ? (void *)gdn_replay_kernel<MODE, NN, 8> : (void *)gdn_replay_kernel<MODE, NN, 2>;
+    RSSM_PICK(16) RSSM_PICK(32) RSSM_PICK(64) RSSM_PICK(128)
+#undef RSSM_PICK
+    return nullptr;
+}
+
+void *pick_verify(int DK, int vpt) {
+#define RSSM_PICK(NN) \
+    if (DK == NN) return vpt == 8 ? (void *)gdn_verify_kernel<NN, 8> : (void *)gdn_verify_kernel<NN, 2>;
     RSSM_PICK(16) RSSM_PICK(32) RSSM_PICK(64) RSSM_PICK(128)
 #undef RSSM_PICK
     return nullptr;
@@ -453,6 +675,37 @@ extern "C" rssm_status replayssm_gdn_flush(const rssm_gdn_dims *d, const rssm_gd
     a.mask = mask;
     const size_t smem = (size_t)GSmem(d->L, g.R, d->dk).total * sizeof(float);
     return launch(pick_replay<gFlush>(d->dk, g.vpt), d, a, g, smem, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" rssm_status replayssm_gdn_verify(const rssm_gdn_dims *d, const rssm_gdn_cache *c, int32_t T,
+                                            const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                            const float *alpha, const float *beta, float *o, void *stream) {
+    rssm_status s = check(d);
+    if (s != RSSM_OK) return s;
+    if ((s = check_cache(c)) != RSSM_OK) return s;
+    if (T < 1 || T > kMaxT || T > d->L) return RSSM_ERR_RING;
+    if (!q || !k || !v || !alpha || !beta || !o) return RSSM_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return RSSM_ERR_ALIGN;
+    TileGeom g;
+    if (!choose_geom(d->batch, d->nheads, d->dv, d->dk, g)) return RSSM_ERR_UNSUPPORTED;
+    GArgs a = make_args(d, g);
+    set_cache(a, c);
+    a.T = T; a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.o = o;
+    const size_t smem = (size_t)GVSmem(d->L, T, g.R, d->dk).total * sizeof(float);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((s = launch(pick_verify(d->dk, g.vpt), d, a, g, smem, st)) != RSSM_OK) return s;
+    gdn_verify_append<<<d->batch * d->nheads, 128, 0, st>>>(a);
+    return launch_status();
+}
+
+extern "C" rssm_status replayssm_gdn_rollback(const rssm_gdn_dims *d, const rssm_gdn_cache *c, int32_t T,
+                                              const int32_t *accepted, void *stream) {
+    rssm_status s = check(d);
+    if (s != RSSM_OK) return s;
+    if (!c || !c->ring_head || !c->ring_len || !c->err || !accepted) return RSSM_ERR_NULL;
+    if (T < 1 || T > kMaxT || T > d->L) return RSSM_ERR_RING;
+    return rssm::launch_ring_rollback(d->batch, d->L, T, accepted, c->ring_head, c->ring_len, c->err,
+                                      static_cast<cudaStream_t>(stream));
 }
 
 extern "C" rssm_status replayssm_gdn_conventional_decode(const rssm_gdn_dims *d, float *state, const uint16_t *q,

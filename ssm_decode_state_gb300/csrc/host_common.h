@@ -75,4 +75,8 @@ inline bool choose_geom(int batch, int heads, int rows, int cols, TileGeom &g, i
     return g.split > 0;
 }
 
+// Device-side ring rollback shared by the Mamba-2 and GDN caches (launch only).
+rssm_status launch_ring_rollback(int batch, int L, int T, const int32_t *accepted, int32_t *ring_head,
+                                 int32_t *ring_len, uint32_t *err, cudaStream_t st);
+
 }  // namespace rssm

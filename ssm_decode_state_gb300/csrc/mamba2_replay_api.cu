@@ -106,6 +106,16 @@ __global__ void requant_kernel(const float *ckpt, uint8_t *q, float *scale, long
 }
 
 }  // namespace
+
+// Rollback of ring_len by T - accepted[b] on the device (Mamba-2 and GDN caches
+// share the ring metadata).
+rssm_status launch_ring_rollback(int batch, int L, int T, const int32_t *accepted, int32_t *ring_head,
+                                 int32_t *ring_len, uint32_t *err, cudaStream_t st) {
+    const int thr = 128;
+    rollback_kernel<<<(batch + thr - 1) / thr, thr, 0, st>>>(batch, L, T, accepted, ring_head, ring_len, err);
+    return launch_status();
+}
+
 }  // namespace rssm
 
 using namespace rssm;
@@ -168,10 +178,8 @@ extern "C" rssm_status replayssm_rollback(const rssm_mamba2_dims *d, const rssm_
     if (!c) return RSSM_ERR_NULL;
     if (!c->ring_head || !c->ring_len || !c->err || !accepted) return RSSM_ERR_NULL;
     if (T < 1 || T > d->L || T > kMaxT) return RSSM_ERR_RING;
-    const int thr = 128;
-    rollback_kernel<<<(d->batch + thr - 1) / thr, thr, 0, static_cast<cudaStream_t>(stream)>>>(
-        d->batch, d->L, T, accepted, c->ring_head, c->ring_len, c->err);
-    return launch_status();
+    return launch_ring_rollback(d->batch, d->L, T, accepted, c->ring_head, c->ring_len, c->err,
+                                static_cast<cudaStream_t>(stream));
 }
 
 extern "C" rssm_status replayssm_requant(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c,

@@ -191,15 +191,24 @@ def _l2norm_f32(a: np.ndarray) -> np.ndarray:
     return (a / n).astype(np.float32)
 
 
-def gdn_step_inputs(shape: GDNShape, seed: int, step: int) -> GDNStep:
-    r = _rng(seed, _STREAM_STEP, step)
-    b, H = shape.batch, shape.nheads
-    q = round_bf16(_l2norm_f32(r.standard_normal((b, H, shape.dk), dtype=np.float32)))
-    k = round_bf16(_l2norm_f32(r.standard_normal((b, H, shape.dk), dtype=np.float32)))
-    v = round_bf16(r.standard_normal((b, H, shape.dv), dtype=np.float32))
-    alpha = np.exp(-_softplus(r.standard_normal((b, H)))).astype(np.float32)
-    beta = (1.0 / (1.0 + np.exp(-r.standard_normal((b, H))))).astype(np.float32)
+def _gdn_tokens(shape: GDNShape, r, lead: tuple) -> GDNStep:
+    H = shape.nheads
+    q = round_bf16(_l2norm_f32(r.standard_normal(lead + (H, shape.dk), dtype=np.float32)))
+    k = round_bf16(_l2norm_f32(r.standard_normal(lead + (H, shape.dk), dtype=np.float32)))
+    v = round_bf16(r.standard_normal(lead + (H, shape.dv), dtype=np.float32))
+    alpha = np.exp(-_softplus(r.standard_normal(lead + (H,)))).astype(np.float32)
+    beta = (1.0 / (1.0 + np.exp(-r.standard_normal(lead + (H,))))).astype(np.float32)
     return GDNStep(q=q, k=k, v=v, alpha=alpha, beta=beta)
+
+
+def gdn_step_inputs(shape: GDNShape, seed: int, step: int) -> GDNStep:
+    """One token per sequence: q, k [b, H, dk], v [b, H, dv], alpha, beta [b, H]."""
+    return _gdn_tokens(shape, _rng(seed, _STREAM_STEP, step), (shape.batch,))
+
+
+def gdn_draft_inputs(shape: GDNShape, seed: int, step: int, T: int) -> GDNStep:
+    """T draft tokens per sequence: q, k [b, T, H, dk], v [b, T, H, dv], alpha, beta [b, T, H]."""
+    return _gdn_tokens(shape, _rng(seed, _STREAM_DRAFT, step), (shape.batch, T))
 
 
 # --------------------------------------------------------------------------
@@ -209,7 +218,7 @@ def gdn_step_inputs(shape: GDNShape, seed: int, step: int) -> GDNStep:
 @dataclass
 class Workload:
     name: str
-    kind: str                  # "mamba2" | "mamba2_fp8" | "mamba2_verify" | "gdn"
+    kind: str                  # "mamba2" | "mamba2_fp8" | "mamba2_verify" | "gdn" | "gdn_verify"
     shape: object
     steps: int
     seed: int
@@ -240,4 +249,10 @@ def workloads() -> dict[str, Workload]:
             "gdn_b256", "gdn",
             GDNShape(batch=256, nheads=32, dk=128, dv=128, L=16),
             steps=256, seed=1004),
+        # the first next row: Gated DeltaNet speculative verify of 4 drafts on the
+        # batch-256 GDN layer (the verify step of the Mamba-2 verify workload, on GDN)
+        "gdn_verify_b256_T4": Workload(
+            "gdn_verify_b256_T4", "gdn_verify",
+            GDNShape(batch=256, nheads=32, dk=128, dv=128, L=16),
+            steps=200, seed=1005, T=4),
     }

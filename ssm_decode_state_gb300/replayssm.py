@@ -24,8 +24,8 @@ _lib = ctypes.CDLL(_LIB_PATH)
 EXPORTS = [
     "replayssm_decode", "replayssm_decode_noalloc", "replayssm_flush", "replayssm_verify", "replayssm_rollback",
     "replayssm_requant", "replayssm_conventional_decode", "replayssm_conventional_verify",
-    "replayssm_conventional_select", "replayssm_gdn_decode", "replayssm_gdn_flush",
-    "replayssm_gdn_conventional_decode", "replayssm_status_string", "replayssm_version",
+    "replayssm_conventional_select", "replayssm_gdn_decode", "replayssm_gdn_flush", "replayssm_gdn_verify",
+    "replayssm_gdn_rollback", "replayssm_gdn_conventional_decode", "replayssm_status_string", "replayssm_version",
 ]
 
 DEVERR_RING_META = 0x1
@@ -73,6 +73,8 @@ _sig = {
     "replayssm_conventional_select": [_I, _P, _I, _P, _P, _P],
     "replayssm_gdn_decode": [_P, _P, _P, _P, _P, _P, _P, _P, _P],
     "replayssm_gdn_flush": [_P, _P, _P, _P],
+    "replayssm_gdn_verify": [_P, _P, _I, _P, _P, _P, _P, _P, _P, _P],
+    "replayssm_gdn_rollback": [_P, _P, _I, _P, _P],
     "replayssm_gdn_conventional_decode": [_P, _P, _P, _P, _P, _P, _P, _P, _P],
 }
 for _name, _args in _sig.items():
@@ -282,6 +284,26 @@ def gdn_decode(cache: GDNCache, q, k, v, alpha, beta, o=None, stream=None) -> to
 def gdn_flush(cache: GDNCache, mask=None, stream=None) -> None:
     cs = cache.c_struct()
     _check(_lib.replayssm_gdn_flush(ctypes.byref(cache.dims), ctypes.byref(cs), _ptr(mask), _stream(stream)))
+
+
+def gdn_verify(cache: GDNCache, q, k, v, alpha, beta, o=None, stream=None) -> torch.Tensor:
+    """Score T drafts per sequence (q, k [b, T, H, dk], v [b, T, H, dv], alpha, beta
+    [b, T, H]); returns o [b, T, H, dv].  Appends the drafts' records."""
+    d = cache.dims
+    T = alpha.shape[1]
+    if o is None:
+        o = torch.empty(d.batch, T, d.nheads, d.dv, dtype=torch.float32, device=q.device)
+    cs = cache.c_struct()
+    _check(_lib.replayssm_gdn_verify(ctypes.byref(d), ctypes.byref(cs), T, _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(alpha), _ptr(beta), _ptr(o), _stream(stream)))
+    return o
+
+
+def gdn_rollback(cache: GDNCache, T: int, accepted, stream=None) -> None:
+    """Keep accepted[b] of the T drafts of the last verify (int32 device tensor)."""
+    cs = cache.c_struct()
+    _check(_lib.replayssm_gdn_rollback(ctypes.byref(cache.dims), ctypes.byref(cs), T, _ptr(accepted),
+                                       _stream(stream)))
 
 
 def gdn_conventional_decode(dims: GDNDims, state, q, k, v, alpha, beta, o=None, stream=None) -> torch.Tensor:

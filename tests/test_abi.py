@@ -132,3 +132,11 @@ def test_gdn_checks(rs):
                                     FAKE, FAKE, None) == 2
     assert lib.replayssm_gdn_conventional_decode(ctypes.byref(d), None, FAKE, FAKE, FAKE, FAKE,
                                                  FAKE, FAKE, None) == 1
+    d4 = rs.GDNDims(2, 4, 64, 64, 4)
+    for T in (0, 5, 9):                          # draft counts outside 1..min(L, 8)
+        assert lib.replayssm_gdn_verify(ctypes.byref(d4), ctypes.byref(c), T, FAKE, FAKE, FAKE, FAKE,
+                                        FAKE, FAKE, None) == 4
+        assert lib.replayssm_gdn_rollback(ctypes.byref(d4), ctypes.byref(c), T, FAKE, None) == 4
+    assert lib.replayssm_gdn_verify(ctypes.byref(d4), ctypes.byref(c2), 2, FAKE, FAKE, FAKE, FAKE,
+                                    FAKE, FAKE, None) == 2
+    assert lib.replayssm_gdn_rollback(ctypes.byref(d4), ctypes.byref(c), 2, None, None) == 1

@@ -408,7 +408,7 @@ def run_sweep(args):
     print(json.dumps({"sweep": out}), flush=True)
 
 
-ROWS = ("fp8", "verify", "gdn")
+ROWS = ("fp8", "verify", "gdn", "gdn_verify")
 
 
 def measure_rows(rs, dev, steps, warmup, which=ROWS):
@@ -539,6 +539,49 @@ def measure_rows(rs, dev, steps, warmup, which=ROWS):
                                   "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1),
                                   "conventional_us_per_step": round(ms_c * 1e3 / K, 1),
                                   "replay_speedup": round(ms_c / ms, 3)}
+    if "gdn_verify" in which:
+        # ---- Gated DeltaNet verify of 4 drafts + rollback, batch 256
+        w = wl["gdn_verify_b256_T4"]
+        sh, T = w.shape, w.T
+        dims = rs.gdn_dims(sh.batch, sh.nheads, sh.dk, sh.dv, sh.L)
+        S0 = torch.randn(sh.batch, sh.nheads, sh.dv, sh.dk, device=dev, generator=g).mul_(0.1)
+        cache = rs.gdn_cache(dims, ckpt=S0, device=dev)
+        drafts = []
+        for t in range(4):
+            st = gen.gdn_draft_inputs(sh, w.seed, t, T)
+            drafts.append(tuple(torch.from_numpy(a).to(torch.bfloat16).to(dev) for a in (st.q, st.k, st.v))
+                          + (torch.from_numpy(st.alpha).to(dev), torch.from_numpy(st.beta).to(dev)))
+        accs = [gen.accepted_counts(sh.batch, T, w.seed, t) for t in range(steps + warmup)]
+        accd = [torch.from_numpy(a).to(dev) for a in accs]
+        o = torch.empty(sh.batch, T, sh.nheads, sh.dv, device=dev)
+
+        def gvstep(t):
+            rs.gdn_verify(cache, *drafts[t % 4], o=o)
+            rs.gdn_rollback(cache, T, accd[t])
+
+        for t in range(warmup):
+            gvstep(t)
+        torch.cuda.synchronize(dev)
+        gu = bm.gdn_units(sh.nheads, sh.dk, sh.dv)
+        lens = cache.ring_len.cpu().numpy().astype(np.int64)
+        alg = 0
+        for t in range(warmup, warmup + steps):
+            alg += sum(bm.gdn_verify(gu, int(l), T, sh.L) for l in lens)
+            lens = np.where(lens + T > sh.L, 0, lens) + T - (T - accs[t])
+        ms = _timed(stream, lambda t: gvstep(warmup + t), steps)
+        assert int(cache.err.item()) == 0
+        # context: T in-place decodes of a state copy (what scoring the drafts costs a
+        # conventional step without the per-draft snapshots its rollback would need)
+        state = S0.clone()
+        o1 = torch.empty(sh.batch, sh.nheads, sh.dv, device=dev)
+        step_in = [tuple(a[:, i].contiguous() for a in drafts[0]) for i in range(T)]
+        ms_c = _timed(stream, lambda t: [rs.gdn_conventional_decode(dims, state, *step_in[i], o=o1)
+                                         for i in range(T)], steps)
+        out["gdn_verify_T4_b256"] = {"us_per_step": round(ms * 1e3 / steps, 1),
+                                     "seq_verify_s": round(sh.batch * steps / (ms / 1e3), 1),
+                                     "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1),
+                                     "T_inplace_decodes_us": round(ms_c * 1e3 / steps, 1)}
+        del cache, state
     return out
 
 

@@ -96,3 +96,10 @@ def gdn_replay_decode(u: GDNUnits, len_before: int, L: int) -> int:
 
 def gdn_replay_period(u: GDNUnits, L: int) -> float:
     return sum(gdn_replay_decode(u, k, L) for k in range(L)) / L
+
+
+def gdn_verify(u: GDNUnits, len_before: int, T: int, L: int) -> int:
+    """Replay verify of T drafts: the checkpoint once (written back on a pre-flush),
+    the T drafts' inputs and outputs, their records appended, the buffered records read."""
+    pre = len_before + T > L
+    return u.S + (u.S if pre else 0) + T * (u.I + u.Y + u.Rw) + len_before * u.Rr

@@ -29,3 +29,13 @@ def test_gdn_units():
     assert g.S == 2 * 1024 * 1024
     assert bm.gdn_conventional(g) == 4235520
     assert round(bm.gdn_replay_period(g, 16)) == 2409840
+
+
+def test_gdn_verify_bytes():
+    """Verify of T drafts at the batch-256 GDN shape: one 2 MiB checkpoint read,
+    a second (the write-back) only on a pre-flush, and T drafts' token bytes."""
+    u = bm.gdn_units(32, 128, 128)
+    assert u.S == 2 * 1024 * 1024
+    base = bm.gdn_verify(u, 0, 4, 16)
+    assert base == u.S + 4 * (u.I + u.Y + u.Rw)
+    assert bm.gdn_verify(u, 13, 4, 16) - bm.gdn_verify(u, 12, 4, 16) == u.S + u.Rr   # 13 + 4 > 16 pre-flushes

@@ -69,7 +69,7 @@ typedef enum {
 /* Bits that kernels OR into the caller's *err word. */
 #define RSSM_DEVERR_RING_META 0x1u /* ring_head/ring_len out of range: sequence skipped */
 #define RSSM_DEVERR_ROLLBACK  0x2u /* accepted outside [0,T] or ring_len < T - accepted */
-#define RSSM_DEVERR_SLOT      0x4u /* snapshot slot index outside [0, T] */
+#define RSSM_DEVERR_SLOT      0x4u /* snapshot slot outside [0, T], or cache slot outside [0, capacity) */
 #define RSSM_DEVERR_TIMEOUT   0x8u /* an asynchronous tile copy did not complete within ~2 s;
                                       the kernel abandoned the rest of its work and the
                                       cache (and its arrival counters) must be reset */
@@ -104,6 +104,14 @@ typedef struct {
     const float *A;       /* [nheads] */
     const float *D;       /* [nheads] */
     uint32_t *err;        /* one word; RSSM_DEVERR_* bits are ORed in */
+    /* Cache-slot indirection (engine-style state indices; continuous batching):
+     * the cache arrays above hold `capacity` sequences ([capacity] in place of
+     * [batch] in their layouts) and batch row b of a call's inputs and outputs
+     * belongs to the sequence in slot slots[b].  slots == NULL: row b uses slot b.
+     * capacity == 0: capacity = batch.  The slots of one call must be distinct.
+     * A slot outside [0, capacity) skips that row and sets RSSM_DEVERR_SLOT. */
+    const int32_t *slots; /* [batch] device, or NULL */
+    int32_t capacity;
 } rssm_mamba2_cache;
 
 /*
@@ -140,7 +148,8 @@ rssm_status replayssm_decode(const rssm_mamba2_dims *dims, const rssm_mamba2_cac
  * memory instead; every GPU that loads the library holds that array until
  * the process exits.  Everything else -- arguments, results, errors -- is as
  * replayssm_decode.
- *  - batch > 4096 returns RSSM_ERR_SHAPE before anything is enqueued.
+ *  - batch (or, with a slot map, the cache capacity) > 4096 returns RSSM_ERR_SHAPE
+ *    before anything is enqueued.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *  - The first call on a device looks up the array's device address with that
  *    device current; make that first call before any stream capture.

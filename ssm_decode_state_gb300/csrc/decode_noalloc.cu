@@ -50,14 +50,17 @@ extern "C" rssm_status replayssm_decode_noalloc(const rssm_mamba2_dims *dims, co
                                                 const float *dt, const void *x, const void *B, const void *C,
                                                 float *y, void *stream) {
     if (!dims || !cache) return RSSM_ERR_NULL;
-    if (dims->batch < 1 || dims->batch > kNoAllocMaxBatch) return RSSM_ERR_SHAPE;
+    // the counters are indexed by cache slot: the cache's capacity (batch without a
+    // slot map) must fit the fixed array
+    const int cap = cache->capacity > 0 ? cache->capacity : dims->batch;
+    if (dims->batch < 1 || cache->capacity < 0 || cap > kNoAllocMaxBatch) return RSSM_ERR_SHAPE;
     int32_t *scratch = nullptr;
     rssm_status s = scratch_for_current_device(&scratch);
     if (s != RSSM_OK) return s;
     // the counters must start at zero; a call that was abandoned could have
     // left some behind, so clear this call's share first (stream-ordered)
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, sizeof(int32_t) * (size_t)dims->batch, st) != cudaSuccess) {
+    if (cudaMemsetAsync(scratch, 0, sizeof(int32_t) * (size_t)cap, st) != cudaSuccess) {
         cudaGetLastError();
         return RSSM_ERR_CUDA;
     }

@@ -704,8 +704,8 @@ extern "C" rssm_status replayssm_gdn_rollback(const rssm_gdn_dims *d, const rssm
     if (s != RSSM_OK) return s;
     if (!c || !c->ring_head || !c->ring_len || !c->err || !accepted) return RSSM_ERR_NULL;
     if (T < 1 || T > kMaxT || T > d->L) return RSSM_ERR_RING;
-    return rssm::launch_ring_rollback(d->batch, d->L, T, accepted, c->ring_head, c->ring_len, c->err,
-                                      static_cast<cudaStream_t>(stream));
+    return rssm::launch_ring_rollback(d->batch, d->L, T, accepted, nullptr, d->batch, c->ring_head, c->ring_len,
+                                      c->err, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" rssm_status replayssm_gdn_conventional_decode(const rssm_gdn_dims *d, float *state, const uint16_t *q,

@@ -76,7 +76,7 @@ inline bool choose_geom(int batch, int heads, int rows, int cols, TileGeom &g, i
 }
 
 // Device-side ring rollback shared by the Mamba-2 and GDN caches (launch only).
-rssm_status launch_ring_rollback(int batch, int L, int T, const int32_t *accepted, int32_t *ring_head,
-                                 int32_t *ring_len, uint32_t *err, cudaStream_t st);
+rssm_status launch_ring_rollback(int batch, int L, int T, const int32_t *accepted, const int32_t *slots, int cap,
+                                 int32_t *ring_head, int32_t *ring_len, uint32_t *err, cudaStream_t st);
 
 }  // namespace rssm

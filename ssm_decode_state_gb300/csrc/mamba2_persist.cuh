@@ -78,7 +78,7 @@ struct PSmem {
         rdt_off = rC_off + up(N * 2, 16);
         rec_bytes = up(rdt_off + HPI * KM * 4, 128);
         rec_off = o;   o += RB * rec_bytes;
-        meta_off = o;  o += up(MY * 8, 16);                 // [items of this CTA][head, len]
+        meta_off = o;  o += up(MY * 12, 16);                // [items of this CTA][head, len, cache slot]
         cb_off = o;    o += up(3 * KM * 4, 16);             // [3 items][KM]
         w_off = o;     o += up(3 * HPI * KM * 4, 16);       // [3][HPI][KM]
         decay_off = o; o += up(3 * HPI * 4, 16);            // [3][HPI]
@@ -163,19 +163,28 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     // once: every item of the sequence, in every CTA, has read them already.
     for (int k = tid; k < n_my; k += blockDim.x) {
         const int it = item_of(k), b = item_b(it);
-        const int hd = __ldcg(a.ring_head + b), ln = __ldcg(a.ring_len + b);
-        s_meta[k * 2 + 0] = hd;
-        s_meta[k * 2 + 1] = ln;
+        const int sb = a.slots ? __ldg(a.slots + b) : b;     // the sequence's cache slot
+        if (sb < 0 || sb >= a.cap) {                         // skipped by every warp role
+            s_meta[k * 3 + 0] = -1;
+            s_meta[k * 3 + 1] = 0;
+            s_meta[k * 3 + 2] = 0;
+            if (item_h0(it) == 0) flag_error(a.err, RSSM_DEVERR_SLOT);
+            continue;
+        }
+        const int hd = __ldcg(a.ring_head + sb), ln = __ldcg(a.ring_len + sb);
+        s_meta[k * 3 + 0] = hd;
+        s_meta[k * 3 + 1] = ln;
+        s_meta[k * 3 + 2] = sb;
         if (meta_bad(hd, ln) && item_h0(it) == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
         __threadfence();
-        if (atomicAdd(a.arrive + b, 1) == pc.arrivals - 1) {
+        if (atomicAdd(a.arrive + sb, 1) == pc.arrivals - 1) {
             __threadfence();
             if (!meta_bad(hd, ln)) {
                 const bool fold = ln + 1 >= L;
-                a.ring_head[b] = fold ? (hd + ln + 1) % L : hd;
-                a.ring_len[b] = fold ? 0 : ln + 1;
+                a.ring_head[sb] = fold ? (hd + ln + 1) % L : hd;
+                a.ring_len[sb] = fold ? 0 : ln + 1;
             }
-            a.arrive[b] = 0;
+            a.arrive[sb] = 0;
         }
     }
     __syncthreads();                                     // the only CTA-wide barrier
@@ -188,9 +197,9 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         bool ok = true;
         int issued = 0;                                  // stage units issued so far
         for (int k = 0; k < n_my && ok; ++k) {
-            const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+            const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
             const bool f8 = fp8_item(hd, ln);
-            const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
+            const int it = item_of(k), sb = s_meta[k * 3 + 2], h0 = item_h0(it);
             const int nu = f8 ? HPI / Q8 : HPI;
             for (int uu = 0; uu < nu; ++uu) {
                 const int t = issued, s = t % S;
@@ -198,12 +207,12 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 if (!ok) break;
                 unsigned char *dst = stages + s * lay.stage_bytes;
                 if (!f8) {
-                    const size_t tile = ((size_t)b * H + h0 + uu) * P;
+                    const size_t tile = ((size_t)sb * H + h0 + uu) * P;
                     mbar_arrive_expect_tx(full + s, P * N * 4);
                     bulk_g2s(dst, a.ckpt + tile * N, P * N * 4, full + s, pol);
                 } else {
                     // Q8 consecutive heads: their codes, then their row scales
-                    const size_t tile = ((size_t)b * H + h0 + uu * Q8) * P;
+                    const size_t tile = ((size_t)sb * H + h0 + uu * Q8) * P;
                     mbar_arrive_expect_tx(full + s, Q8 * (P * N + P * 4));
                     bulk_g2s(dst, a.ckpt_q + tile * N, Q8 * P * N, full + s, pol);
                     bulk_g2s(dst + Q8 * P * N, a.ckpt_scale + tile, Q8 * P * 4, full + s, pol);
@@ -236,7 +245,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const int it = item_of(k), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
-            const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+            const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1], sb = s_meta[k * 3 + 2];
             const bool good = !meta_bad(hd, ln);
             if (good) {
                 // records: list position j < ln is ring slot (hd + j) mod L, j = ln the current
@@ -248,25 +257,25 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 if (lane == 0) mbar_arrive_expect_tx(rfull + r, (uint32_t)((HPI * nrec * P + nrec * N + N) * 2));
                 __syncwarp();
                 if (lane < HPI) {
-                    const size_t bh = (size_t)b * H + h0 + lane;
+                    const size_t bh = (size_t)sb * H + h0 + lane;      // cache
                     unsigned char *dx = rb + lay.rx_off + lane * KM * P * 2;
                     if (run1) bulk_g2s(dx, rx + (bh * L + hd) * P, run1 * P * 2, rfull + r);
                     if (run2) bulk_g2s(dx + run1 * P * 2, rx + bh * L * P, run2 * P * 2, rfull + r);
-                    bulk_g2s(dx + ln * P * 2, ix + bh * P, P * 2, rfull + r);
+                    bulk_g2s(dx + ln * P * 2, ix + ((size_t)b * H + h0 + lane) * P, P * 2, rfull + r);
                 } else if (lane == HPI) {
-                    const size_t bg = (size_t)b * G + g;
+                    const size_t bg = (size_t)sb * G + g;              // cache
                     unsigned char *dB = rb + lay.rB_off;
                     if (run1) bulk_g2s(dB, rB + (bg * L + hd) * N, run1 * N * 2, rfull + r);
                     if (run2) bulk_g2s(dB + run1 * N * 2, rB + bg * L * N, run2 * N * 2, rfull + r);
-                    bulk_g2s(dB + ln * N * 2, iB + bg * N, N * 2, rfull + r);
+                    bulk_g2s(dB + ln * N * 2, iB + ((size_t)b * G + g) * N, N * 2, rfull + r);
                 } else if (lane == HPI + 1) {
                     bulk_g2s(rb + lay.rC_off, iC + ((size_t)b * G + g) * N, N * 2, rfull + r);
                 }
                 for (int idx = lane; idx < HPI * nrec; idx += 32) {
                     const int hh = idx / nrec, j = idx - hh * nrec;
-                    const size_t bh = (size_t)b * H + h0 + hh;
                     const int slot = hd + j < L ? hd + j : hd + j - L;
-                    cp_async4(rb + lay.rdt_off + (hh * KM + j) * 4, j < ln ? a.rec_dt + bh * L + slot : a.dt + bh);
+                    cp_async4(rb + lay.rdt_off + (hh * KM + j) * 4,
+                              j < ln ? a.rec_dt + ((size_t)sb * H + h0 + hh) * L + slot : a.dt + (size_t)b * H + h0 + hh);
                 }
             }
             cp_async_arrive_noinc(rfull + r);
@@ -294,7 +303,8 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         bool live = true;
         for (int kk = 0; kk < n_my; ++kk) {
             const int r = kk % RB, ia = kk % 3;
-            const int it = item_of(kk), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
+            // the preparation only writes the cache (the ring appends): b is the item's slot
+            const int it = item_of(kk), b = s_meta[kk * 3 + 2], h0 = item_h0(it), g = h0 / hpg;
             if (live && kk >= 3 && !pwait(pempty + ia, (uint32_t)(((kk / 3) - 1) & 1), s_abort)) {
                 live = false;
                 *s_abort = 1;
@@ -303,7 +313,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 live = false;
                 *s_abort = 1;
             }
-            const int hd = s_meta[kk * 2 + 0], ln = s_meta[kk * 2 + 1];
+            const int hd = s_meta[kk * 3 + 0], ln = s_meta[kk * 3 + 1];
             const bool work = live && !meta_bad(hd, ln);
             const int nrec = ln + 1;
             const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
@@ -435,8 +445,8 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     int u = 0;                                           // stage units consumed so far
     for (int k = 0; k < n_my; ++k) {
         const int r = k % RB, ia = k % 3;
-        const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
-        const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+        const int it = item_of(k), b = item_b(it), h0 = item_h0(it), sb = s_meta[k * 3 + 2];
+        const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
         // the item's records and its prepared arrays
         if (live && !pwait(pfull + ia, (uint32_t)((k / 3) & 1), s_abort)) {
             live = false;
@@ -539,7 +549,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 __syncwarp();                            // the warp is done with the stage
                 if (lane == 0) mbar_arrive(empty + s);
                 if (!work) continue;
-                const size_t tile = ((size_t)b * H + h0 + hh) * P;
+                const size_t tile = ((size_t)sb * H + h0 + hh) * P;    // cache rows of this head
                 if (fold) {
                     const float *wh = w + hh * KM;
                     const uint16_t *xh = r_x + hh * KM * P;

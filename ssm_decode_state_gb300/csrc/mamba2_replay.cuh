@@ -44,6 +44,8 @@ struct M2Args {
     float *rec_dt;
     void *rec_x, *rec_B, *rec_C;
     int32_t *ring_head, *ring_len, *arrive;
+    const int32_t *slots;   // [B] cache slot of each batch row; nullptr: row b uses slot b
+    int cap;                // sequences the cache arrays hold
     const float *A, *D;
     uint32_t *err;
     const float *dt;
@@ -88,7 +90,12 @@ m2_replay_kernel(const M2Args a) {
 
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const int b = blockIdx.y;
+    const int b = blockIdx.y;                // batch row: inputs and outputs
+    const int sb = a.slots ? a.slots[b] : b;  // cache slot of the row's sequence
+    if (sb < 0 || sb >= a.cap) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.err, RSSM_DEVERR_SLOT);
+        return;
+    }
     const int h = blockIdx.x / a.split;
     const int sp = blockIdx.x - h * a.split;
     const int g = h / a.hpg;
@@ -98,8 +105,8 @@ m2_replay_kernel(const M2Args a) {
     const int E = bf ? 8 : 4;               // elements per 16-byte chunk
 
     // ---- 0. ring pointers and what this step does
-    const int head = a.ring_head[b];
-    const int len = a.ring_len[b];
+    const int head = a.ring_head[sb];
+    const int len = a.ring_len[sb];
     const bool bad = head < 0 || head >= L || len < 0 || len > L;
     if (bad) {
         if (blockIdx.x == 0 && tid == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
@@ -126,7 +133,7 @@ m2_replay_kernel(const M2Args a) {
     const int KM = L + (MODE == kVerify ? a.T : 1);
 
     // ---- checkpoint loads (in flight during staging)
-    const size_t tile = ((size_t)b * H + h) * P + p0;          // first row of the tile
+    const size_t tile = ((size_t)sb * H + h) * P + p0;         // first row of the tile
     const float4 *ck4 = reinterpret_cast<const float4 *>(a.ckpt + tile * N);
     float4 hv[VPT];
     uint32_t qv[VPT];
@@ -168,7 +175,7 @@ m2_replay_kernel(const M2Args a) {
                     const int j = idx / cx, c = idx - j * cx;
                     if (j < len) {
                         const int slot = (head + j) % L;
-                        src = rx + ((((size_t)b * H + h) * L + slot) * P + p0 + c * E) * esz;
+                        src = rx + ((((size_t)sb * H + h) * L + slot) * P + p0 + c * E) * esz;
                     } else {
                         const int i = j - len;   // 0 for decode
                         const size_t row = MODE == kVerify ? (((size_t)b * a.T + i) * H + h)
@@ -181,7 +188,7 @@ m2_replay_kernel(const M2Args a) {
                     const int j = k / cB, c = k - j * cB;
                     if (j < len) {
                         const int slot = (head + j) % L;
-                        src = rB + ((((size_t)b * a.G + g) * L + slot) * N + c * E) * esz;
+                        src = rB + ((((size_t)sb * a.G + g) * L + slot) * N + c * E) * esz;
                     } else {
                         const int i = j - len;
                         const size_t row = MODE == kVerify ? (((size_t)b * a.T + i) * a.G + g)
@@ -214,7 +221,7 @@ m2_replay_kernel(const M2Args a) {
     for (int j = tid; j < nrec; j += nthr) {
         float d;
         if (j < len) {
-            d = __ldcg(a.rec_dt + ((size_t)b * H + h) * L + (head + j) % L);
+            d = __ldcg(a.rec_dt + ((size_t)sb * H + h) * L + (head + j) % L);
         } else {
             const int i = j - len;
             d = MODE == kVerify ? __ldcg(a.dt + ((size_t)b * a.T + i) * H + h)
@@ -362,7 +369,7 @@ m2_replay_kernel(const M2Args a) {
             const int slot = (head2 + len2 + i) % L;
             const size_t irow = MODE == kVerify ? (((size_t)b * a.T + i) * H + h) : ((size_t)b * H + h);
             const uint4 val = __ldcg(reinterpret_cast<const uint4 *>(ix + (irow * P + p0 + c * E) * esz));
-            *reinterpret_cast<uint4 *>(wx_ + ((((size_t)b * H + h) * L + slot) * P + p0 + c * E) * esz) = val;
+            *reinterpret_cast<uint4 *>(wx_ + ((((size_t)sb * H + h) * L + slot) * P + p0 + c * E) * esz) = val;
         }
     }
 
@@ -371,7 +378,7 @@ m2_replay_kernel(const M2Args a) {
     __syncthreads();
     if (tid == 0) {
         __threadfence();
-        const int prev = atomicAdd(a.arrive + b, 1);
+        const int prev = atomicAdd(a.arrive + sb, 1);
         s_flag[0] = (prev == (int)gridDim.x - 1);
     }
     __syncthreads();
@@ -383,7 +390,7 @@ m2_replay_kernel(const M2Args a) {
             const int slot = (head2 + len2 + i) % L;
             const float d = MODE == kVerify ? __ldcg(a.dt + ((size_t)b * a.T + i) * H + hh)
                                             : __ldcg(a.dt + (size_t)b * H + hh);
-            a.rec_dt[((size_t)b * H + hh) * L + slot] = d;
+            a.rec_dt[((size_t)sb * H + hh) * L + slot] = d;
         }
         const int nBC = nnew * a.G * cB;
         char *wB = static_cast<char *>(a.rec_B);
@@ -398,7 +405,7 @@ m2_replay_kernel(const M2Args a) {
             const int slot = (head2 + len2 + i) % L;
             const size_t irow = MODE == kVerify ? (((size_t)b * a.T + i) * a.G + gg) : ((size_t)b * a.G + gg);
             const char *src = (isC ? iC : iB) + (irow * N + c * E) * esz;
-            char *dst = (isC ? wC : wB) + ((((size_t)b * a.G + gg) * L + slot) * N + c * E) * esz;
+            char *dst = (isC ? wC : wB) + ((((size_t)sb * a.G + gg) * L + slot) * N + c * E) * esz;
             *reinterpret_cast<uint4 *>(dst) = __ldcg(reinterpret_cast<const uint4 *>(src));
         }
     }
@@ -414,9 +421,9 @@ m2_replay_kernel(const M2Args a) {
             nh = (head + len) % L;
             nl = 0;
         }
-        a.ring_head[b] = nh;
-        a.ring_len[b] = nl;
-        a.arrive[b] = 0;
+        a.ring_head[sb] = nh;
+        a.ring_len[sb] = nl;
+        a.arrive[sb] = 0;
     }
 }
 

@@ -31,7 +31,12 @@ rssm_status check_cache(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c) {
     if (!aligned16(c->ckpt) || !aligned16(c->rec_x) || !aligned16(c->rec_B) ||
         (c->rec_C && !aligned16(c->rec_C)) || (d->read_copy && (!aligned16(c->ckpt_q) || !aligned16(c->ckpt_scale))))
         return RSSM_ERR_ALIGN;
+    if (c->capacity < 0 || (!c->slots && c->capacity > 0 && c->capacity < d->batch)) return RSSM_ERR_SHAPE;
     return RSSM_OK;
+}
+
+int cache_capacity(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c) {
+    return c->capacity > 0 ? c->capacity : d->batch;
 }
 
 template <int MODE, int TQ>
@@ -53,6 +58,7 @@ M2Args make_args(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c, const Ti
     a.rec_dt = c->rec_dt; a.rec_x = c->rec_x; a.rec_B = c->rec_B; a.rec_C = c->rec_C;
     a.ring_head = c->ring_head; a.ring_len = c->ring_len; a.arrive = c->arrive;
     a.A = c->A; a.D = c->D; a.err = c->err;
+    a.slots = c->slots; a.cap = cache_capacity(d, c);
     return a;
 }
 
@@ -71,11 +77,16 @@ rssm_status launch(const rssm_mamba2_dims *d, M2Args &a, const TileGeom &g, cuda
     return launch_status();
 }
 
-__global__ void rollback_kernel(int batch, int L, int T, const int32_t *accepted, int32_t *ring_head,
-                                int32_t *ring_len, uint32_t *err) {
+__global__ void rollback_kernel(int batch, int L, int T, const int32_t *accepted, const int32_t *slots, int cap,
+                                int32_t *ring_head, int32_t *ring_len, uint32_t *err) {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= batch) return;
-    const int head = ring_head[b], len = ring_len[b], acc = accepted[b];
+    const int sb = slots ? slots[b] : b;
+    if (sb < 0 || sb >= cap) {
+        flag_error(err, RSSM_DEVERR_SLOT);
+        return;
+    }
+    const int head = ring_head[sb], len = ring_len[sb], acc = accepted[b];
     if (head < 0 || head >= L || len < 0 || len > L) {
         flag_error(err, RSSM_DEVERR_RING_META);
         return;
@@ -84,7 +95,7 @@ __global__ void rollback_kernel(int batch, int L, int T, const int32_t *accepted
         flag_error(err, RSSM_DEVERR_ROLLBACK);
         return;
     }
-    ring_len[b] = len - (T - acc);
+    ring_len[sb] = len - (T - acc);
 }
 
 // One thread per float4 of the checkpoint; the N/4 lanes of a row agree on
@@ -109,10 +120,11 @@ __global__ void requant_kernel(const float *ckpt, uint8_t *q, float *scale, long
 
 // Rollback of ring_len by T - accepted[b] on the device (Mamba-2 and GDN caches
 // share the ring metadata).
-rssm_status launch_ring_rollback(int batch, int L, int T, const int32_t *accepted, int32_t *ring_head,
-                                 int32_t *ring_len, uint32_t *err, cudaStream_t st) {
+rssm_status launch_ring_rollback(int batch, int L, int T, const int32_t *accepted, const int32_t *slots, int cap,
+                                 int32_t *ring_head, int32_t *ring_len, uint32_t *err, cudaStream_t st) {
     const int thr = 128;
-    rollback_kernel<<<(batch + thr - 1) / thr, thr, 0, st>>>(batch, L, T, accepted, ring_head, ring_len, err);
+    rollback_kernel<<<(batch + thr - 1) / thr, thr, 0, st>>>(batch, L, T, accepted, slots, cap, ring_head,
+                                                             ring_len, err);
     return launch_status();
 }
 
@@ -178,8 +190,9 @@ extern "C" rssm_status replayssm_rollback(const rssm_mamba2_dims *d, const rssm_
     if (!c) return RSSM_ERR_NULL;
     if (!c->ring_head || !c->ring_len || !c->err || !accepted) return RSSM_ERR_NULL;
     if (T < 1 || T > d->L || T > kMaxT) return RSSM_ERR_RING;
-    return launch_ring_rollback(d->batch, d->L, T, accepted, c->ring_head, c->ring_len, c->err,
-                                static_cast<cudaStream_t>(stream));
+    if (c->capacity < 0 || (!c->slots && c->capacity > 0 && c->capacity < d->batch)) return RSSM_ERR_SHAPE;
+    return launch_ring_rollback(d->batch, d->L, T, accepted, c->slots, cache_capacity(d, c), c->ring_head,
+                                c->ring_len, c->err, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" rssm_status replayssm_requant(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c,
@@ -188,7 +201,8 @@ extern "C" rssm_status replayssm_requant(const rssm_mamba2_dims *d, const rssm_m
     if (s != RSSM_OK) return s;
     if (!c || !c->ckpt || !c->ckpt_q || !c->ckpt_scale) return RSSM_ERR_NULL;
     if (!aligned16(c->ckpt) || !aligned16(c->ckpt_q)) return RSSM_ERR_ALIGN;
-    const long long n4 = (long long)d->batch * d->nheads * d->headdim * d->dstate / 4;
+    if (c->capacity < 0) return RSSM_ERR_SHAPE;
+    const long long n4 = (long long)cache_capacity(d, c) * d->nheads * d->headdim * d->dstate / 4;
     const int thr = 256;
     const long long blocks = (n4 + thr - 1) / thr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

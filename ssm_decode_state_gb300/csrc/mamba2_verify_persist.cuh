@@ -56,7 +56,7 @@ struct VSmem {
         rdt_off = rC_off + up(T * N * 2, 16);
         rec_bytes = up(rdt_off + HPI * KM * 4, 128);
         rec_off = o;   o += RB * rec_bytes;
-        meta_off = o;  o += up(MY * 8, 16);                 // [items of this CTA][head, len]
+        meta_off = o;  o += up(MY * 12, 16);                // [items of this CTA][head, len, cache slot]
         // prepared items, triple-buffered
         decay_off = o; o += up(3 * HPI * T * 4, 16);        // [3][HPI][T]    exp(A S_i)
         wf_off = o;    o += up(3 * HPI * KM * 4, 16);       // [3][HPI][KM]   fold weights
@@ -143,19 +143,28 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
     // the verify's pointers (pre-flush when the drafts would overflow the ring)
     for (int k = tid; k < n_my; k += blockDim.x) {
         const int it = item_of(k), b = item_b(it);
-        const int hd = __ldcg(a.ring_head + b), ln = __ldcg(a.ring_len + b);
-        s_meta[k * 2 + 0] = hd;
-        s_meta[k * 2 + 1] = ln;
+        const int sb = a.slots ? __ldg(a.slots + b) : b;     // the sequence's cache slot
+        if (sb < 0 || sb >= a.cap) {                         // skipped by every warp role
+            s_meta[k * 3 + 0] = -1;
+            s_meta[k * 3 + 1] = 0;
+            s_meta[k * 3 + 2] = 0;
+            if (item_h0(it) == 0) flag_error(a.err, RSSM_DEVERR_SLOT);
+            continue;
+        }
+        const int hd = __ldcg(a.ring_head + sb), ln = __ldcg(a.ring_len + sb);
+        s_meta[k * 3 + 0] = hd;
+        s_meta[k * 3 + 1] = ln;
+        s_meta[k * 3 + 2] = sb;
         if (meta_bad(hd, ln) && item_h0(it) == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
         __threadfence();
-        if (atomicAdd(a.arrive + b, 1) == pc.arrivals - 1) {
+        if (atomicAdd(a.arrive + sb, 1) == pc.arrivals - 1) {
             __threadfence();
             if (!meta_bad(hd, ln)) {
                 const bool pre = ln + T > L;
-                a.ring_head[b] = pre ? (hd + ln) % L : hd;
-                a.ring_len[b] = (pre ? 0 : ln) + T;
+                a.ring_head[sb] = pre ? (hd + ln) % L : hd;
+                a.ring_len[sb] = (pre ? 0 : ln) + T;
             }
-            a.arrive[b] = 0;
+            a.arrive[sb] = 0;
         }
     }
     __syncthreads();                                     // the only CTA-wide barrier
@@ -168,12 +177,12 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
         bool ok = true;
         int issued = 0;
         for (int k = 0; k < n_my && ok; ++k) {
-            const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
+            const int it = item_of(k), sb = s_meta[k * 3 + 2], h0 = item_h0(it);
             for (int hh = 0; hh < HPI; ++hh) {
                 const int t = k * HPI + hh, s = t % S;
                 if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort);
                 if (!ok) break;
-                const size_t tile = ((size_t)b * H + h0 + hh) * P;
+                const size_t tile = ((size_t)sb * H + h0 + hh) * P;
                 mbar_arrive_expect_tx(full + s, P * N * 4);
                 bulk_g2s(stages + s * lay.stage_bytes, a.ckpt + tile * N, P * N * 4, full + s, pol);
                 issued = t + 1;
@@ -204,7 +213,7 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const int it = item_of(k), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
-            const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+            const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1], sb = s_meta[k * 3 + 2];
             const bool good = !meta_bad(hd, ln);
             if (good) {
                 // buffered records: at most two contiguous runs of ring slots; drafts: one
@@ -216,14 +225,14 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
                     mbar_arrive_expect_tx(rfull + r, (uint32_t)((HPI * nrec * P + nrec * N + T * N) * 2));
                 __syncwarp();
                 if (lane < HPI) {
-                    const size_t bh = (size_t)b * H + h0 + lane;
+                    const size_t bh = (size_t)sb * H + h0 + lane;      // cache
                     unsigned char *dx = rb + lay.rx_off + lane * KM * P * 2;
                     if (run1) bulk_g2s(dx, rx + (bh * L + hd) * P, run1 * P * 2, rfull + r);
                     if (run2) bulk_g2s(dx + run1 * P * 2, rx + bh * L * P, run2 * P * 2, rfull + r);
                     for (int i = 0; i < T; ++i)
                         bulk_g2s(dx + (ln + i) * P * 2, ix + (((size_t)b * T + i) * H + h0 + lane) * P, P * 2, rfull + r);
                 } else if (lane == HPI) {
-                    const size_t bg = (size_t)b * G + g;
+                    const size_t bg = (size_t)sb * G + g;              // cache
                     unsigned char *dB = rb + lay.rB_off;
                     if (run1) bulk_g2s(dB, rB + (bg * L + hd) * N, run1 * N * 2, rfull + r);
                     if (run2) bulk_g2s(dB + run1 * N * 2, rB + bg * L * N, run2 * N * 2, rfull + r);
@@ -235,7 +244,7 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
                 }
                 for (int idx = lane; idx < HPI * nrec; idx += 32) {
                     const int hh = idx / nrec, j = idx - hh * nrec;
-                    const size_t bh = (size_t)b * H + h0 + hh;
+                    const size_t bh = (size_t)sb * H + h0 + hh;        // cache
                     const int slot = hd + j < L ? hd + j : hd + j - L;
                     cp_async4(rb + lay.rdt_off + (hh * KM + j) * 4,
                               j < ln ? a.rec_dt + bh * L + slot : a.dt + ((size_t)b * T + (j - ln)) * H + h0 + hh);
@@ -261,7 +270,8 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
         bool live = true;
         for (int kk = 0; kk < n_my; ++kk) {
             const int r = kk % RB, ia = kk % 3;
-            const int it = item_of(kk), b = item_b(it), h0 = item_h0(it);
+            // the preparation only writes the cache (the draft appends): b is the item's slot
+            const int it = item_of(kk), b = s_meta[kk * 3 + 2], h0 = item_h0(it);
             if (live && kk >= 3 && !pwait(pempty + ia, (uint32_t)(((kk / 3) - 1) & 1), s_abort)) {
                 live = false;
                 *s_abort = 1;
@@ -270,7 +280,7 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
                 live = false;
                 *s_abort = 1;
             }
-            const int hd = s_meta[kk * 2 + 0], ln = s_meta[kk * 2 + 1];
+            const int hd = s_meta[kk * 3 + 0], ln = s_meta[kk * 3 + 1];
             const bool work = live && !meta_bad(hd, ln);
             const bool pre = ln + T > L;
             const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
@@ -422,7 +432,7 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
 
     for (int k = 0; k < n_my; ++k) {
         const int r = k % RB, ia = k % 3;
-        const int it = item_of(k), b = item_b(it), h0 = item_h0(it);
+        const int it = item_of(k), b = item_b(it), h0 = item_h0(it), sb = s_meta[k * 3 + 2];
         if (live && !pwait(pfull + ia, (uint32_t)((k / 3) & 1), s_abort)) {
             live = false;
             *s_abort = 1;
@@ -431,7 +441,7 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             live = false;
             *s_abort = 1;
         }
-        const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+        const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
         const bool work = live && !meta_bad(hd, ln);
         const bool pre = work && (ln + T > L);
         const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
@@ -460,7 +470,7 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             if (lane == 0) mbar_arrive(empty + s);
             if (!work) continue;
             const int h = h0 + hh;
-            const size_t tile = ((size_t)b * H + h) * P;
+            const size_t tile = ((size_t)sb * H + h) * P;              // cache rows of this head
             // T x 8 row dot products reduced across the warp: lane ends with (draft, row)
             float part[TQ * VPT];
 #pragma unroll
@@ -541,7 +551,9 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
 // verify kernel has already committed.
 __global__ void verify_bc_epilogue(const M2Args a) {
     const int b = blockIdx.x;
-    const int hd = a.ring_head[b], ln = a.ring_len[b], L = a.L, T = a.T, G = a.G, N = a.N;
+    const int sb = a.slots ? a.slots[b] : b;
+    if (sb < 0 || sb >= a.cap) return;
+    const int hd = a.ring_head[sb], ln = a.ring_len[sb], L = a.L, T = a.T, G = a.G, N = a.N;
     if (hd < 0 || hd >= L || ln < T || ln > L) return;
     const int CB = N / 8;
     const int total = 2 * T * G * CB;
@@ -553,7 +565,7 @@ __global__ void verify_bc_epilogue(const M2Args a) {
         if (dst == nullptr) continue;
         const uint16_t *src = static_cast<const uint16_t *>(isC ? a.Cin : a.Bin);
         const int slot = (hd + ln - T + i) % L;
-        *reinterpret_cast<uint4 *>(dst + ((((size_t)b * G + g) * L + slot) * N + c * 8)) =
+        *reinterpret_cast<uint4 *>(dst + ((((size_t)sb * G + g) * L + slot) * N + c * 8)) =
             __ldcg(reinterpret_cast<const uint4 *>(src + ((((size_t)b * T + i) * G + g) * N + c * 8)));
     }
 }

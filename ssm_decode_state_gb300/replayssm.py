@@ -46,7 +46,7 @@ class Mamba2Dims(ctypes.Structure):
 class Mamba2CacheC(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("ckpt", "ckpt_q", "ckpt_scale", "rec_dt", "rec_x", "rec_B", "rec_C",
-                 "ring_head", "ring_len", "arrive", "A", "D", "err")]
+                 "ring_head", "ring_len", "arrive", "A", "D", "err", "slots")] + [("capacity", ctypes.c_int32)]
 
 
 class GDNDims(ctypes.Structure):
@@ -133,9 +133,14 @@ class Mamba2Cache:
     A: torch.Tensor
     D: torch.Tensor
     err: torch.Tensor
+    slots: torch.Tensor | None = None      # [batch] int32 cache slot of each batch row (None: row b -> slot b)
+    capacity: int = 0                      # sequences the cache holds (0: batch)
 
-    def c_struct(self) -> Mamba2CacheC:
-        return Mamba2CacheC(*(_ptr(getattr(self, f)) for f, _ in Mamba2CacheC._fields_))
+    def c_struct(self, slots=None) -> Mamba2CacheC:
+        """The C struct; ``slots`` (int32 [batch] on the device) overrides the cache's map."""
+        sl = self.slots if slots is None else slots
+        vals = [_ptr(getattr(self, f)) for f, _ in Mamba2CacheC._fields_[:-2]]
+        return Mamba2CacheC(*vals, _ptr(sl), int(self.capacity))
 
 
 def mamba2_dims(batch, nheads, headdim, dstate, ngroups, L=16, read_copy=0, io_bf16=True) -> Mamba2Dims:
@@ -143,9 +148,11 @@ def mamba2_dims(batch, nheads, headdim, dstate, ngroups, L=16, read_copy=0, io_b
 
 
 def mamba2_cache(dims: Mamba2Dims, A: torch.Tensor, D: torch.Tensor, ckpt: torch.Tensor | None = None,
-                 keep_C: bool = True, device="cuda") -> Mamba2Cache:
-    """Allocate an empty-ring cache.  ``ckpt`` (if given) is used as the checkpoint."""
-    b, H, P, N, G, L = dims.batch, dims.nheads, dims.headdim, dims.dstate, dims.ngroups, dims.L
+                 keep_C: bool = True, device="cuda", capacity: int = 0) -> Mamba2Cache:
+    """Allocate an empty-ring cache for ``capacity`` sequences (0: dims.batch).
+    ``ckpt`` (if given) is used as the checkpoint."""
+    H, P, N, G, L = dims.nheads, dims.headdim, dims.dstate, dims.ngroups, dims.L
+    b = capacity if capacity > 0 else dims.batch
     io = torch.bfloat16 if dims.io_bf16 else torch.float32
     z = lambda *s, dtype=torch.float32: torch.zeros(*s, dtype=dtype, device=device)  # noqa: E731
     if ckpt is None:
@@ -160,50 +167,50 @@ def mamba2_cache(dims: Mamba2Dims, A: torch.Tensor, D: torch.Tensor, ckpt: torch
         arrive=z(b, dtype=torch.int32),
         A=A.to(device=device, dtype=torch.float32).contiguous(),
         D=D.to(device=device, dtype=torch.float32).contiguous(),
-        err=z(1, dtype=torch.int32))
+        err=z(1, dtype=torch.int32), capacity=int(capacity))
 
 
-def decode(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None) -> torch.Tensor:
+def decode(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None, slots=None) -> torch.Tensor:
     d = cache.dims
     if y is None:
         y = torch.empty(d.batch, d.nheads, d.headdim, dtype=torch.float32, device=dt.device)
-    cs = cache.c_struct()
+    cs = cache.c_struct(slots)
     _check(_lib.replayssm_decode(ctypes.byref(d), ctypes.byref(cs), _ptr(dt), _ptr(x), _ptr(B), _ptr(C),
                                  _ptr(y), _stream(stream)))
     return y
 
 
-def decode_noalloc(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None) -> torch.Tensor:
+def decode_noalloc(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None, slots=None) -> torch.Tensor:
     """decode() for callers that cannot allocate: the arrival counters live in
     the library's own device memory (cache.arrive is not used; batch <= 4096)."""
     d = cache.dims
     if y is None:
         y = torch.empty(d.batch, d.nheads, d.headdim, dtype=torch.float32, device=dt.device)
-    cs = cache.c_struct()
+    cs = cache.c_struct(slots)
     cs.arrive = None
     _check(_lib.replayssm_decode_noalloc(ctypes.byref(d), ctypes.byref(cs), _ptr(dt), _ptr(x), _ptr(B),
                                          _ptr(C), _ptr(y), _stream(stream)))
     return y
 
 
-def flush(cache: Mamba2Cache, mask=None, stream=None) -> None:
-    cs = cache.c_struct()
+def flush(cache: Mamba2Cache, mask=None, stream=None, slots=None) -> None:
+    cs = cache.c_struct(slots)
     _check(_lib.replayssm_flush(ctypes.byref(cache.dims), ctypes.byref(cs), _ptr(mask), _stream(stream)))
 
 
-def verify(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None) -> torch.Tensor:
+def verify(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None, slots=None) -> torch.Tensor:
     d = cache.dims
     T = dt.shape[1]
     if y is None:
         y = torch.empty(d.batch, T, d.nheads, d.headdim, dtype=torch.float32, device=dt.device)
-    cs = cache.c_struct()
+    cs = cache.c_struct(slots)
     _check(_lib.replayssm_verify(ctypes.byref(d), ctypes.byref(cs), T, _ptr(dt), _ptr(x), _ptr(B), _ptr(C),
                                  _ptr(y), _stream(stream)))
     return y
 
 
-def rollback(cache: Mamba2Cache, T: int, accepted, stream=None) -> None:
-    cs = cache.c_struct()
+def rollback(cache: Mamba2Cache, T: int, accepted, stream=None, slots=None) -> None:
+    cs = cache.c_struct(slots)
     _check(_lib.replayssm_rollback(ctypes.byref(cache.dims), ctypes.byref(cs), T, _ptr(accepted),
                                    _stream(stream)))
 

@@ -125,3 +125,67 @@ def test_gdn_verify_pins_catch(monkeypatch, mutant):
     attr, fn = mutant
     monkeypatch.setattr(gdn_mod.GDNStepwise, attr, fn)
     assert _run_pins(gdn_pins) > 0
+
+
+def _nvfp4_mutants():
+    import oracle.nvfp4 as nv
+
+    def swapped_nibbles(codes):
+        c = np.asarray(codes, np.uint8)
+        return (c[..., 1::2] | (c[..., 0::2] << 4)).astype(np.uint8)
+
+    def ties_away_from_zero(v):
+        v = np.asarray(v, np.float32)
+        a = np.abs(v.astype(np.float64))
+        _, ex = np.frexp(a)
+        q = np.ldexp(0.5, np.maximum(ex - 1, 0))
+        val = np.minimum(np.floor(a / q + 0.5) * q, 6.0)
+        mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+        code = np.abs(val[..., None] - mags).argmin(axis=-1)
+        return (code | (np.signbit(v).astype(np.int64) << 3)).astype(np.uint8)
+
+    def dropped_sign(v):
+        return nv._orig_encode(np.abs(np.asarray(v, np.float32)))
+
+    def row_target_448(h):
+        old = nv.ROW_TARGET
+        nv.ROW_TARGET = 448.0
+        try:
+            return nv._orig_quantize(h)
+        finally:
+            nv.ROW_TARGET = old
+
+    def block_of_8(h):
+        old = nv.BLOCK
+        nv.BLOCK = 8
+        try:
+            return nv._orig_quantize(h)
+        finally:
+            nv.BLOCK = old
+
+    def block_scale_from_row_max(h):
+        h = np.asarray(h, np.float32)
+        codes, sb, s_r = nv._orig_quantize(h)
+        top = sb.max(axis=-1, keepdims=True)
+        return codes, np.broadcast_to(top, sb.shape).copy(), s_r
+
+    return [("pack_codes", swapped_nibbles), ("e2m1_encode", ties_away_from_zero),
+            ("e2m1_encode", dropped_sign), ("quantize_rows", row_target_448),
+            ("quantize_rows", block_of_8), ("quantize_rows", block_scale_from_row_max)]
+
+
+@pytest.mark.parametrize("target,mutant", _nvfp4_mutants(), ids=lambda m: getattr(m, "__name__", str(m)))
+def test_nvfp4_pins_catch(monkeypatch, target, mutant):
+    import oracle.nvfp4 as nv
+    from tests import test_oracle_nvfp4 as nv_pins
+    nv._orig_encode = nv.e2m1_encode
+    nv._orig_quantize = nv.quantize_rows
+    monkeypatch.setattr(nv, target, mutant)
+    failed = 0
+    for name in dir(nv_pins):
+        if name.startswith("test_"):
+            try:
+                getattr(nv_pins, name)()
+            except (AssertionError, ValueError):      # a wrong value, or a wrong block count
+                failed += 1
+    assert failed > 0

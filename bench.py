@@ -430,7 +430,7 @@ def run_sweep(args):
     print(json.dumps({"sweep": out}), flush=True)
 
 
-ROWS = ("fp8", "verify", "gdn", "gdn_verify")
+ROWS = ("fp8", "nvfp4", "verify", "gdn", "gdn_verify")
 
 
 def measure_rows(rs, dev, steps, warmup, which=ROWS):
@@ -450,12 +450,14 @@ def measure_rows(rs, dev, steps, warmup, which=ROWS):
         return (torch.from_numpy(st.dt).to(dev), torch.from_numpy(st.x).to(torch.bfloat16).to(dev),
                 torch.from_numpy(st.B).to(torch.bfloat16).to(dev), torch.from_numpy(st.C).to(torch.bfloat16).to(dev))
 
-    if "fp8" in which:
-        # ---- FP8 read copy, batch 256
-        w = wl["mamba2_fp8read_b256"]
+    for rc, name, wname in ((1, "fp8", "mamba2_fp8read_b256"), (2, "nvfp4", "mamba2_nvfp4read_b256")):
+        if name not in which:
+            continue
+        # ---- FP8 or NVFP4 read copy, batch 256
+        w = wl[wname]
         sh = w.shape
         prm = gen.mamba2_params(sh, w.seed)
-        dims = rs.mamba2_dims(sh.batch, sh.nheads, sh.headdim, sh.dstate, sh.ngroups, sh.L, read_copy=1)
+        dims = rs.mamba2_dims(sh.batch, sh.nheads, sh.headdim, sh.dstate, sh.ngroups, sh.L, read_copy=rc)
         ck = torch.randn(sh.batch, sh.nheads, sh.headdim, sh.dstate, device=dev, generator=g).mul_(0.1)
         cache = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D), ckpt=ck, device=dev)
         rs.requant(cache)
@@ -469,13 +471,25 @@ def measure_rows(rs, dev, steps, warmup, which=ROWS):
         K = (steps // sh.L) * sh.L
         alg = 0
         for _ in range(K):
-            alg += bm.mamba2_replay_decode(u, ln, sh.L, read_copy=True) * sh.batch
+            alg += bm.mamba2_replay_decode(u, ln, sh.L, read_copy=rc) * sh.batch
             ln = 0 if ln + 1 >= sh.L else ln + 1
         ms = _timed(stream, lambda t: rs.decode(cache, *pool[t % 8], y=y), K)
         assert int(cache.err.item()) == 0
-        out["fp8_read_decode_b256"] = {"us_per_step": round(ms * 1e3 / K, 1),
-                                       "seq_tok_s": round(sh.batch * K / (ms / 1e3), 1),
-                                       "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1)}
+        # per-step split over two flush periods, each launch between its own events
+        ln0 = int(cache.ring_len[0].item())
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * sh.L)]
+        for i, (s0, s1) in enumerate(evs):
+            s0.record(stream)
+            rs.decode(cache, *pool[i % 8], y=y)
+            s1.record(stream)
+        torch.cuda.synchronize(dev)
+        split = {"nonflush": [], "flush": []}
+        for i, (s0, s1) in enumerate(evs):
+            split["flush" if (ln0 + i) % sh.L == sh.L - 1 else "nonflush"].append(s0.elapsed_time(s1) * 1e3)
+        out[f"{name}_read_decode_b256"] = {"us_per_step": round(ms * 1e3 / K, 1),
+                                           "seq_tok_s": round(sh.batch * K / (ms / 1e3), 1),
+                                           "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1),
+                                           "step_us": {k: round(statistics.median(v), 1) for k, v in split.items()}}
         del cache, ck
 
     if "verify" in which:

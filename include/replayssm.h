@@ -85,14 +85,19 @@ typedef struct {
     int32_t dstate;     /* N, one of 16, 32, 64, 128 */
     int32_t ngroups;    /* G */
     int32_t L;          /* ring capacity = flush threshold, 1..32 */
-    int32_t read_copy;  /* 0: reads use the FP32 checkpoint; 1: FP8 E4M3 read copy */
+    int32_t read_copy;  /* 0: reads use the FP32 checkpoint; 1: FP8 E4M3 read copy;
+                           2: NVFP4 read copy (E2M1 codes, E4M3 scale per 16 columns) */
     int32_t io_bf16;    /* 1: x, B, C and their records are bf16; 0: float32 */
 } rssm_mamba2_dims;
 
 typedef struct {
     float    *ckpt;       /* [batch][nheads][headdim][dstate] FP32 checkpoint h_c */
-    uint8_t  *ckpt_q;     /* [batch][nheads][headdim][dstate] E4M3 codes (read_copy = 1) */
-    float    *ckpt_scale; /* [batch][nheads][headdim] one scale per row (read_copy = 1) */
+    uint8_t  *ckpt_q;     /* read_copy = 1: [batch][nheads][headdim][dstate] E4M3 codes;
+                             read_copy = 2: per (sequence, head) headdim*dstate*9/16 bytes,
+                             the E2M1 codes [headdim][dstate/2] (column 2i in the low
+                             nibble of byte i) then the E4M3 block scales
+                             [headdim][dstate/16] */
+    float    *ckpt_scale; /* [batch][nheads][headdim] one float32 scale per row (read_copy 1, 2) */
     float    *rec_dt;     /* [batch][nheads][L] */
     void     *rec_x;      /* [batch][nheads][L][headdim], bf16 or float32 per io_bf16 */
     void     *rec_B;      /* [batch][ngroups][L][dstate] */
@@ -130,7 +135,7 @@ typedef struct {
  *                 copy is re-quantised, ring_head <- (ring_head + len + 1) mod L,
  *                 ring_len <- 0; the current token is not stored.
  * y is the replay output above in every case.  Non-flush steps read the FP8
- * copy when dims->read_copy = 1.
+ * copy when dims->read_copy = 1 and the NVFP4 copy when it is 2.
  */
 rssm_status replayssm_decode(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
                              const float *dt, const void *x, const void *B, const void *C,
@@ -198,11 +203,20 @@ rssm_status replayssm_rollback(const rssm_mamba2_dims *dims, const rssm_mamba2_c
                                int32_t T, const int32_t *accepted, void *stream);
 
 /*
- * (Re)build the FP8 read copy from the FP32 checkpoint for every sequence:
- * per (head, row) amax = max|h|, scale = amax/448, code = E4M3 round-to-
- * nearest-even, saturating, of h * (448/amax); a zero row gets scale 1 and
- * zero codes (AT Pulse §Technical analysis "quantization").  Used once after
- * the checkpoint is initialised; flushes keep the copy current afterwards.
+ * (Re)build the read copy from the FP32 checkpoint for every sequence (AT
+ * Pulse §Technical analysis "quantization": a high-precision checkpoint drives
+ * the recurrence, a low-precision copy serves the reads).
+ * FP8 (read_copy 0 or 1): per (head, row) amax = max|h|, scale = amax/448,
+ * code = E4M3 round-to-nearest-even, saturating, of h * (448/amax); a zero row
+ * gets scale 1 and zero codes.
+ * NVFP4 (read_copy 2; AT Pulse §What happened: 4-bit NVFP4 reads; the block
+ * layout is the format's public definition): per row s_r = amax/2688 and
+ * k_r = 448/amax; per 16-column block with maximum m, block scale code
+ * E4M3(m * k_r), d = e4m3(code) * s_r, element code E2M1 round-to-nearest-
+ * even, saturating, of h * (1/d); every step one correctly rounded float32
+ * operation; a zero row stores zero codes, zero block scales and s_r = 0.
+ * Used once after the checkpoint is initialised; flushes keep the copy
+ * current afterwards.
  */
 rssm_status replayssm_requant(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
                               void *stream);

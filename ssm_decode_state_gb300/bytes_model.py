@@ -20,6 +20,7 @@ from dataclasses import dataclass
 class Mamba2Units:
     S: int    # FP32 checkpoint
     Sq: int   # FP8 read copy: codes + one float32 scale per row
+    Sq4: int  # NVFP4 read copy: 4-bit codes + an E4M3 scale per 16 columns + a float32 scale per row
     I: int    # one token's inputs: dt, x, B, C
     Y: int    # one token's output y (float32)
     Rw: int   # one record written: dt, x, B, C
@@ -30,29 +31,37 @@ def mamba2_units(nheads, headdim, dstate, ngroups, io_bytes=2, keep_C=True) -> M
     H, P, N, G = nheads, headdim, dstate, ngroups
     S = H * P * N * 4
     Sq = H * P * N + H * P * 4
+    Sq4 = H * P * N // 2 + H * P * N // 16 + H * P * 4
     I = H * 4 + H * P * io_bytes + 2 * G * N * io_bytes
     Y = H * P * 4
     Rw = H * 4 + H * P * io_bytes + (2 if keep_C else 1) * G * N * io_bytes
     Rr = H * 4 + H * P * io_bytes + G * N * io_bytes
-    return Mamba2Units(S, Sq, I, Y, Rw, Rr)
+    return Mamba2Units(S, Sq, Sq4, I, Y, Rw, Rr)
 
 
 def mamba2_conventional(u: Mamba2Units) -> int:
     return 2 * u.S + u.I + u.Y
 
 
-def mamba2_replay_decode(u: Mamba2Units, len_before: int, L: int, read_copy: bool = False) -> int:
-    """One replay decode step of a sequence holding ``len_before`` records."""
+def _copy_bytes(u: Mamba2Units, read_copy) -> int:
+    """Size of the read copy: none (0 / False), FP8 (1 / True), NVFP4 (2)."""
+    return {0: 0, 1: u.Sq, 2: u.Sq4}[int(read_copy)]
+
+
+def mamba2_replay_decode(u: Mamba2Units, len_before: int, L: int, read_copy: int = 0) -> int:
+    """One replay decode step of a sequence holding ``len_before`` records; a
+    read copy (1 FP8, 2 NVFP4) replaces the checkpoint read on non-flush steps
+    and is rewritten at the flush."""
     fold = len_before + 1 >= L
     b = u.I + u.Y + len_before * u.Rr
     if fold:
-        b += 2 * u.S + (u.Sq if read_copy else 0)
+        b += 2 * u.S + _copy_bytes(u, read_copy)
     else:
-        b += (u.Sq if read_copy else u.S) + u.Rw
+        b += (_copy_bytes(u, read_copy) or u.S) + u.Rw
     return b
 
 
-def mamba2_replay_period(u: Mamba2Units, L: int, read_copy: bool = False) -> float:
+def mamba2_replay_period(u: Mamba2Units, L: int, read_copy: int = 0) -> float:
     """Mean over one flush period of L steps from an empty ring."""
     return sum(mamba2_replay_decode(u, k, L, read_copy) for k in range(L)) / L
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -190,6 +191,128 @@ __device__ __forceinline__ void e4m3_quantize_rows(const float4 (&o)[V], uint32_
     for (int v = 0; v < V; ++v) {
         const float iv = __shfl_sync(0xffffffffu, inv, v * (32 / V));
         q[v] = e4m3_pack4(__fmul_rn(o[v].x, iv), __fmul_rn(o[v].y, iv), __fmul_rn(o[v].z, iv), __fmul_rn(o[v].w, iv));
+    }
+}
+
+// --------------------------------------------------------------------- NVFP4
+//
+// NVFP4 read copy: E2M1 element codes (OCP Microscaling Formats: 1 sign bit,
+// 2 exponent bits with bias 1, 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2,
+// 3, 4, 6), one E4M3 scale per 16 consecutive columns of a row and one float32
+// scale per row.  One head's copy is its codes [P][N/2] (column 2i in the low
+// nibble of byte i) followed by its block scales [P][N/16].
+
+constexpr float kNv4RowTarget = 2688.0f;    // 6 (largest E2M1) x 448 (largest E4M3)
+
+__host__ __device__ constexpr int nv4_head_bytes(int P, int N) { return P * N / 2 + P * N / 16; }
+
+// Row scale s_r = amax / 2688 and the block-scale factor k_r = 448 / amax,
+// each one correctly rounded float32 division; a zero row, or one whose
+// scales leave the float32 range, gets s_r = k_r = 0 (every block scale 0).
+__device__ __forceinline__ void nv4_row_scale(float amax, float &s_r, float &k_r) {
+    s_r = __fdiv_rn(amax, kNv4RowTarget);
+    k_r = __fdiv_rn(448.0f, amax);
+    if (!(amax > 0.0f) || !(s_r > 0.0f) || isinf(k_r)) {
+        s_r = 0.0f;
+        k_r = 0.0f;
+    }
+}
+
+// Value of an E4M3 code as float32, exactly: its exponent and mantissa bits
+// placed as the low exponent bits and top mantissa bits of a float32 read
+// 2^-120 times the value (subnormal codes as float32 subnormals), then scaled
+// back.  Never given NaN codes.
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+    return __uint_as_float(((code & 0x7fu) << 20) | ((code & 0x80u) << 24)) * 0x1p120f;
+}
+
+// Block scale code of a block with largest magnitude amax_c, and the inverse
+// of its effective scale e4m3(code) * s_r (0 when that is 0 or its inverse
+// overflows).
+__device__ __forceinline__ uint32_t nv4_block_scale(float amax_c, float s_r, float k_r, float &inv) {
+    const uint32_t code = __nv_cvt_float_to_fp8(__fmul_rn(amax_c, k_r), __NV_SATFINITE, __NV_E4M3);
+    const float d = __fmul_rn(e4m3_value(code), s_r);
+    inv = d > 0.0f ? __frcp_rn(d) : 0.0f;
+    if (isinf(inv)) inv = 0.0f;
+    return code;
+}
+
+// Four float32 values -> four E2M1 codes (round to nearest even, saturating),
+// nibble i of the 16-bit result = element i.
+__device__ __forceinline__ uint32_t e2m1_pack4(float a, float b, float c, float d) {
+    const uint32_t lo = __nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest);
+    const uint32_t hi = __nv_cvt_float2_to_fp4x2(make_float2(c, d), __NV_E2M1, cudaRoundNearest);
+    return (lo & 0xffu) | ((hi & 0xffu) << 8);
+}
+
+// Four E2M1 codes (nibble i = element i) -> float4 of their values.  The
+// code's exponent and mantissa bits become the low exponent bits and top
+// mantissa bit of a float32 that reads 2^-126 times the value (the 0.5 code
+// as a float32 subnormal), scaled back exactly.
+__device__ __forceinline__ float4 e2m1_unpack4(uint32_t w) {
+    float r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t n = (w >> (4 * i)) & 0xfu;
+        r[i] = __uint_as_float(((n & 7u) << 22) | ((n & 8u) << 28)) * 0x1p126f;
+    }
+    return make_float4(r[0], r[1], r[2], r[3]);
+}
+
+// Eight E2M1 codes (nibble k = column k) as four pairs of bfloat16 values, each
+// 2^-126 times the code's value (same bit placement as e2m1_unpack4, in the
+// bfloat16 layout), integer operations only.  Pair i holds columns (i, i + 4):
+// those nibbles sit 16 bits apart, so one shift and one mask place both.
+__device__ __forceinline__ void e2m1_to_bf16_pairs(uint32_t w, uint32_t (&p)[4]) {
+    p[0] = ((w << 6) & 0x01c001c0u) | ((w << 12) & 0x80008000u);
+    p[1] = ((w << 2) & 0x01c001c0u) | ((w << 8) & 0x80008000u);
+    p[2] = ((w >> 2) & 0x01c001c0u) | ((w << 4) & 0x80008000u);
+    p[3] = ((w >> 6) & 0x01c001c0u) | (w & 0x80008000u);
+}
+
+// NVFP4 copy of 8 rows held by one warp, 32 lanes per row (lane i holds
+// columns 4i..4i+3, so the 16-column block c spans lanes 4c..4c+3), written
+// to the head's copy hq (codes, then block scales) and row scales rs.  The
+// per-(row, block) scalar work is split over the block's 4 lanes: a transposed
+// max exchange leaves lane 4c + j with the block maxima of rows 2j and 2j + 1,
+// three butterflies across the blocks give those rows' maxima, the lane
+// derives both rows' scales and stores their block-scale codes, and the
+// inverses go back to the block's lanes by shuffles.  Same float32 operations
+// per row and block as nv4_row_scale + nv4_block_scale + e2m1_pack4.
+// row_of(v) is the head row of this warp's v-th row.
+template <class RowFn>
+__device__ __forceinline__ void nv4_quantize_store(const float4 (&o)[8], uint8_t *hq, float *rs, int P, int N,
+                                                   RowFn row_of) {
+    const int lane = threadIdx.x & 31, c = lane >> 2, j = lane & 3;
+    float m[8];
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+        m[v] = fmaxf(fmaxf(fabsf(o[v].x), fabsf(o[v].y)), fmaxf(fabsf(o[v].z), fabsf(o[v].w)));
+    group_reduce_max<4, 8>(m);                           // m[i]: block maximum of row 2j + i
+    float r0 = m[0], r1 = m[1];
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+        r0 = fmaxf(r0, __shfl_xor_sync(0xffffffffu, r0, x));
+        r1 = fmaxf(r1, __shfl_xor_sync(0xffffffffu, r1, x));
+    }
+    float s0, k0, s1, k1, inv0, inv1;
+    nv4_row_scale(r0, s0, k0);
+    nv4_row_scale(r1, s1, k1);
+    const uint32_t sb0 = nv4_block_scale(m[0], s0, k0, inv0);
+    const uint32_t sb1 = nv4_block_scale(m[1], s1, k1, inv1);
+    const int ra = row_of(2 * j), rb = row_of(2 * j + 1);
+    hq[P * N / 2 + ra * (N / 16) + c] = (uint8_t)sb0;
+    hq[P * N / 2 + rb * (N / 16) + c] = (uint8_t)sb1;
+    if (c == 0) {
+        rs[ra] = s0;
+        rs[rb] = s1;
+    }
+    const int base = lane & ~3;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        const float inv = __shfl_sync(0xffffffffu, (v & 1) ? inv1 : inv0, base + (v >> 1));
+        reinterpret_cast<uint16_t *>(hq + row_of(v) * (N / 2))[lane] = (uint16_t)e2m1_pack4(
+            __fmul_rn(o[v].x, inv), __fmul_rn(o[v].y, inv), __fmul_rn(o[v].z, inv), __fmul_rn(o[v].w, inv));
     }
 }
 

@@ -10,7 +10,8 @@
 //    of shared-memory buffers with one-dimensional bulk copies (the TMA
 //    engine), completing on the stage's "full" mbarrier as transaction bytes:
 //    one FP32 head tile (P x N) per stage, or on non-flush steps of a cache
-//    with a read copy the FP8 codes and row scales of Q8 heads per stage.
+//    with a read copy the FP8 codes and row scales of Q8 heads per stage (the
+//    NVFP4 codes, block scales and row scales of Q4 heads).
 //  * record warp (warp 1): copies each item's records (the used ring slots of
 //    x and B are at most two contiguous runs each, plus the current token's x,
 //    B and C, by bulk copy; dt words by cp.async) into a ring of RB record
@@ -48,8 +49,10 @@ constexpr int persist_threads(int nc) { return nc + 64; }
 constexpr int persist_decode_threads(int nc) { return nc + 64 + kPrepThreads; }
 
 // Byte layout of the persistent kernel's shared memory.
-// Heads whose FP8 codes share one stage (one wait, one release).
+// Heads whose FP8 codes share one stage (one wait, one release); the same
+// count for NVFP4 copies (Q4).
 __host__ __device__ constexpr int persist_q8(int hpi) { return hpi >= 4 ? 4 : hpi; }
+__host__ __device__ constexpr int persist_q4(int hpi) { return hpi >= 4 ? 4 : hpi; }
 
 struct PSmem {
     int stage_bytes, stages_off;
@@ -60,8 +63,11 @@ struct PSmem {
     __host__ __device__ PSmem(int P, int N, int L, int HPI, int S, int RB, int H, int MY) {
         const int KM = L + 1;
         auto up = [](int v, int a) { return (v + a - 1) / a * a; };
-        // one FP32 tile, or the codes and row scales of persist_q8(HPI) heads
+        // one FP32 tile, or the codes and row scales of persist_q8(HPI) heads (FP8), or
+        // the codes, block scales and row scales of persist_q4(HPI) heads (NVFP4)
         stage_bytes = P * N * 4 > persist_q8(HPI) * (P * N + P * 4) ? P * N * 4 : persist_q8(HPI) * (P * N + P * 4);
+        if (persist_q4(HPI) * (nv4_head_bytes(P, N) + P * 4) > stage_bytes)
+            stage_bytes = persist_q4(HPI) * (nv4_head_bytes(P, N) + P * 4);
         int o = 0;
         stages_off = o; o += S * stage_bytes;
         full_off = o;   o += 8 * S;
@@ -99,6 +105,8 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     constexpr int G4 = N / 4;                            // lanes per row
     constexpr int CX = P / 8, CB = N / 8;                // 16-byte chunks per x / B row
     constexpr int Q8 = persist_q8(HPI);                  // heads per stage of FP8 codes
+    constexpr int Q4 = persist_q4(HPI);                  // heads per stage of NVFP4 codes
+    constexpr int HB4 = nv4_head_bytes(P, N);            // one head's NVFP4 codes + block scales
     static_assert(G4 == 32 && VPT == 8 && kPConsumers / 32 * VPT == P, "a warp owns 8 whole consecutive rows");
     extern __shared__ __align__(128) unsigned char smraw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -125,7 +133,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
 
     const int grid = gridDim.x;
     const int n_my = (pc.items - (int)blockIdx.x + grid - 1) / grid;
-    const bool q8 = a.read_copy != 0;
+    const bool q8 = a.read_copy == 1, q4 = a.read_copy == 2;
     auto item_of = [&](int k) { return (int)blockIdx.x + k * grid; };
     auto item_b = [&](int it) { return it / (G * pc.nchunk); };      // item = (b * G + g) * nchunk + c
     auto item_h0 = [&](int it) {
@@ -136,6 +144,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     // a non-flush item of a cache with a read copy streams the FP8 codes, Q8 heads
     // per stage; every other item streams FP32 tiles, one head per stage
     auto fp8_item = [&](int hd, int ln) { return q8 && !meta_bad(hd, ln) && ln + 1 < L; };
+    auto nv4_item = [&](int hd, int ln) { return q4 && !meta_bad(hd, ln) && ln + 1 < L; };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -198,15 +207,21 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         int issued = 0;                                  // stage units issued so far
         for (int k = 0; k < n_my && ok; ++k) {
             const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
-            const bool f8 = fp8_item(hd, ln);
+            const bool f8 = fp8_item(hd, ln), f4 = nv4_item(hd, ln);
             const int it = item_of(k), sb = s_meta[k * 3 + 2], h0 = item_h0(it);
-            const int nu = f8 ? HPI / Q8 : HPI;
+            const int nu = f8 ? HPI / Q8 : f4 ? HPI / Q4 : HPI;
             for (int uu = 0; uu < nu; ++uu) {
                 const int t = issued, s = t % S;
                 if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort);
                 if (!ok) break;
                 unsigned char *dst = stages + s * lay.stage_bytes;
-                if (!f8) {
+                if (f4) {
+                    // Q4 consecutive heads: their codes and block scales, then their row scales
+                    const size_t hd0 = (size_t)sb * H + h0 + uu * Q4;
+                    mbar_arrive_expect_tx(full + s, Q4 * (HB4 + P * 4));
+                    bulk_g2s(dst, a.ckpt_q + hd0 * HB4, Q4 * HB4, full + s, pol);
+                    bulk_g2s(dst + Q4 * HB4, a.ckpt_scale + hd0 * P, Q4 * P * 4, full + s, pol);
+                } else if (!f8) {
                     const size_t tile = ((size_t)sb * H + h0 + uu) * P;
                     mbar_arrive_expect_tx(full + s, P * N * 4);
                     bulk_g2s(dst, a.ckpt + tile * N, P * N * 4, full + s, pol);
@@ -484,7 +499,77 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 a.y[((size_t)b * H + h0 + hh) * P + row] = fmaf(dec[hh], part[0], rt[hh * P + row]);
             }
         };
-        if (fp8_item(hd, ln)) {
+        if (nv4_item(hd, ln)) {
+            // NVFP4 codes, Q4 heads per stage.  Lane (blk, rsub) takes the 16-column
+            // block blk = lane & 7 of rows rsub and rsub + 4 (rsub = lane >> 3) of the
+            // warp's 8 rows: its block sums need one block scale each, then the 8
+            // lanes of a row reduce them.  C_t of the block enters times 2^64 (exact),
+            // so that the products with the codes' 2^-126 offset stay normal floats.
+            const int blk = lane & 7, rsub = lane >> 3;
+            uint32_t cp[8];                              // pairs (k, k + 4) of each 8-column half
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c0 = blk * 16 + hf * 8 + i;
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(bf16_at(r_C, c0) * 0x1p64f,
+                                                                    bf16_at(r_C, c0 + 4) * 0x1p64f);
+                    cp[hf * 4 + i] = *reinterpret_cast<const uint32_t *>(&pr);
+                }
+            }
+            for (int uu = 0; uu < HPI / Q4; ++uu, ++u) {
+                const int s = u % S;
+                if (live && !pwait(full + s, (uint32_t)((u / S) & 1), s_abort)) {
+                    live = false;
+                    *s_abort = 1;
+                }
+                const unsigned char *stg = stages + s * lay.stage_bytes;
+                const float *sc = reinterpret_cast<const float *>(stg + Q4 * HB4);
+                uint2 qc[Q4][2];
+                uint32_t sbc[Q4][2];
+#pragma unroll
+                for (int hq = 0; hq < Q4; ++hq) {
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const int row = cw * VPT + rsub + 4 * m;
+                        qc[hq][m] = *reinterpret_cast<const uint2 *>(stg + hq * HB4 + row * (N / 2) + blk * 8);
+                        sbc[hq][m] = stg[hq * HB4 + P * N / 2 + row * (N / 16) + blk];
+                    }
+                }
+                // the row scale of the (head, row) this lane ends up with after the reduction
+                float rsv;
+                {
+                    const int vi = reduced_index<8, Q4 * 2>(0);
+                    rsv = sc[(vi >> 1) * P + cw * VPT + rsub + 4 * (vi & 1)];
+                }
+                __syncwarp();                            // the warp is done with the stage
+                if (lane == 0) mbar_arrive(empty + s);
+                if (!work) continue;
+                float part[Q4 * 2];
+#pragma unroll
+                for (int hq = 0; hq < Q4; ++hq) {
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        uint32_t pa[4], pb[4];
+                        e2m1_to_bf16_pairs(qc[hq][m].x, pa);
+                        e2m1_to_bf16_pairs(qc[hq][m].y, pb);
+                        float acc = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc = fma_bf16_pair(pa[i], cp[i], acc);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc = fma_bf16_pair(pb[i], cp[4 + i], acc);
+                        part[hq * 2 + m] = acc * e4m3_value(sbc[hq][m]);
+                    }
+                }
+                group_reduce<8, Q4 * 2>(part);
+                if (reduced_writer<8, Q4 * 2>()) {
+                    const int vi = reduced_index<8, Q4 * 2>(0);
+                    const int hh = uu * Q4 + (vi >> 1), row = cw * VPT + rsub + 4 * (vi & 1);
+                    a.y[((size_t)b * H + h0 + hh) * P + row] =
+                        fmaf(dec[hh], (part[0] * 0x1p62f) * rsv, rt[hh * P + row]);
+                }
+            }
+        } else if (fp8_item(hd, ln)) {
             // C_t of this lane's columns as bfloat16 pairs (0, 2) and (1, 3)
             const uint2 craw = *reinterpret_cast<const uint2 *>(r_C + col4 * 4);
             const uint32_t ce = __byte_perm(craw.x, craw.y, 0x5410), co = __byte_perm(craw.x, craw.y, 0x7632);
@@ -591,7 +676,10 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                         f2unpack(fma2(dd, f2pack(hv[v].z, hv[v].w), acc23[v]), o[v].z, o[v].w);
                         st_stream(ckp + (cw * VPT + v) * G4 + lane, o[v]);
                     }
-                    if (q8) {
+                    if (q4) {
+                        nv4_quantize_store(o, a.ckpt_q + ((size_t)sb * H + h0 + hh) * HB4, a.ckpt_scale + tile, P, N,
+                                           [&](int v) { return cw * VPT + v; });
+                    } else if (q8) {
                         uint32_t q[VPT];
                         float rs;
                         e4m3_quantize_rows<VPT>(o, q, rs);

@@ -142,12 +142,24 @@ m2_replay_kernel(const M2Args a) {
     if (!use_q) {
 #pragma unroll
         for (int v = 0; v < VPT; ++v) hv[v] = ld_stream(ck4 + tid + v * nthr);
-    } else {
+    } else if (a.read_copy == 1) {
         const uint32_t *q4 = reinterpret_cast<const uint32_t *>(a.ckpt_q + tile * N);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             qv[v] = ld_stream_u32(q4 + tid + v * nthr);
             qs[v] = __ldcs(a.ckpt_scale + tile + (tid + v * nthr) / G4);
+        }
+    } else {
+        // NVFP4: this thread's 4 codes of each row (16 bits) and the effective
+        // scale of their block, e4m3(block scale) * row scale
+        const uint8_t *hq = a.ckpt_q + ((size_t)sb * H + h) * nv4_head_bytes(P, N);
+        const uint16_t *q16 = reinterpret_cast<const uint16_t *>(hq + (size_t)p0 * (N / 2));
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int idx = tid + v * nthr, row = p0 + idx / G4;
+            qv[v] = __ldcs(q16 + idx);
+            qs[v] = __fmul_rn(e4m3_value(__ldcs(hq + P * N / 2 + row * (N / 16) + col4 / 4)),
+                              __ldcs(a.ckpt_scale + tile + idx / G4));
         }
     }
 
@@ -304,7 +316,19 @@ m2_replay_kernel(const M2Args a) {
             acc.z = fmaf(fdec, hv[v].z, acc.z);
             acc.w = fmaf(fdec, hv[v].w, acc.w);
             st_stream(reinterpret_cast<float4 *>(a.ckpt + tile * N) + tid + v * nthr, acc);
-            if (a.read_copy) {
+            if (a.read_copy == 2) {
+                const float m4 = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
+                const float m = group_max<G4>(m4), mb = group_max<4>(m4);
+                float s_r, k_r, inv;
+                nv4_row_scale(m, s_r, k_r);
+                const uint32_t sbc = nv4_block_scale(mb, s_r, k_r, inv);
+                uint8_t *hq = a.ckpt_q + ((size_t)sb * H + h) * nv4_head_bytes(P, N);
+                const int prow = p0 + row;
+                reinterpret_cast<uint16_t *>(hq + (size_t)prow * (N / 2))[col4] = (uint16_t)e2m1_pack4(
+                    __fmul_rn(acc.x, inv), __fmul_rn(acc.y, inv), __fmul_rn(acc.z, inv), __fmul_rn(acc.w, inv));
+                if ((col4 & 3) == 0) hq[P * N / 2 + prow * (N / 16) + col4 / 4] = (uint8_t)sbc;
+                if (col4 == 0) a.ckpt_scale[tile + row] = s_r;
+            } else if (a.read_copy) {
                 float m = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
                 m = group_max<G4>(m);
                 float scale, inv;
@@ -326,7 +350,7 @@ m2_replay_kernel(const M2Args a) {
             for (int v = 0; v < VPT; ++v) {
                 float4 hh;
                 float sc = 1.0f;
-                if (use_q) { hh = e4m3_unpack4(qv[v]); sc = qs[v]; }
+                if (use_q) { hh = a.read_copy == 2 ? e2m1_unpack4(qv[v]) : e4m3_unpack4(qv[v]); sc = qs[v]; }
                 else hh = hv[v];
                 float d = hh.x * c.x;
                 d = fmaf(hh.y, c.y, d);

@@ -16,7 +16,7 @@ rssm_status check_dims(const rssm_mamba2_dims *d) {
     if (!(d->dstate == 16 || d->dstate == 32 || d->dstate == 64 || d->dstate == 128)) return RSSM_ERR_SHAPE;
     if (d->headdim < 8 || d->headdim > 256 || d->headdim % 8) return RSSM_ERR_SHAPE;
     if (d->L < 1 || d->L > kMaxL) return RSSM_ERR_SHAPE;
-    if (d->read_copy != 0 && d->read_copy != 1) return RSSM_ERR_SHAPE;
+    if (d->read_copy < 0 || d->read_copy > 2) return RSSM_ERR_SHAPE;   // none, FP8 E4M3, NVFP4
     if (d->io_bf16 != 0 && d->io_bf16 != 1) return RSSM_ERR_SHAPE;
     if (d->batch > 65535) return RSSM_ERR_SHAPE;
     return RSSM_OK;
@@ -116,6 +116,28 @@ __global__ void requant_kernel(const float *ckpt, uint8_t *q, float *scale, long
     if ((threadIdx.x & (G4 - 1)) == 0) scale[i / G4] = sc;
 }
 
+// NVFP4 copy: the same thread mapping; a 16-column block spans 4 lanes.
+template <int N>
+__global__ void requant_nv4_kernel(const float *ckpt, uint8_t *q, float *scale, long long n4, int P) {
+    constexpr int G4 = N / 4;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool in = i < n4;
+    const float4 h = in ? __ldcs(reinterpret_cast<const float4 *>(ckpt) + i) : make_float4(0, 0, 0, 0);
+    const float m4 = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
+    const float m = group_max<G4>(m4), mb = group_max<4>(m4);
+    float s_r, k_r, inv;
+    nv4_row_scale(m, s_r, k_r);
+    const uint32_t sb = nv4_block_scale(mb, s_r, k_r, inv);
+    if (!in) return;
+    const long long row = i / G4, head = row / P;
+    const int p = (int)(row - head * P), col4 = (int)(i - row * G4);
+    uint8_t *hq = q + head * nv4_head_bytes(P, N);
+    reinterpret_cast<uint16_t *>(hq + p * (N / 2))[col4] =
+        (uint16_t)e2m1_pack4(__fmul_rn(h.x, inv), __fmul_rn(h.y, inv), __fmul_rn(h.z, inv), __fmul_rn(h.w, inv));
+    if ((col4 & 3) == 0) hq[P * N / 2 + p * (N / 16) + col4 / 4] = (uint8_t)sb;
+    if (col4 == 0) scale[row] = s_r;
+}
+
 }  // namespace
 
 // Rollback of ring_len by T - accepted[b] on the device (Mamba-2 and GDN caches
@@ -206,8 +228,14 @@ extern "C" rssm_status replayssm_requant(const rssm_mamba2_dims *d, const rssm_m
     const int thr = 256;
     const long long blocks = (n4 + thr - 1) / thr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-#define RSSM_RQ(NN) \
-    if (d->dstate == NN) requant_kernel<NN><<<(unsigned)blocks, thr, 0, st>>>(c->ckpt, c->ckpt_q, c->ckpt_scale, n4);
+#define RSSM_RQ(NN)                                                                                      \
+    if (d->dstate == NN) {                                                                               \
+        if (d->read_copy == 2)                                                                           \
+            requant_nv4_kernel<NN><<<(unsigned)blocks, thr, 0, st>>>(c->ckpt, c->ckpt_q, c->ckpt_scale, n4, \
+                                                                     d->headdim);                        \
+        else                                                                                             \
+            requant_kernel<NN><<<(unsigned)blocks, thr, 0, st>>>(c->ckpt, c->ckpt_q, c->ckpt_scale, n4);  \
+    }
     RSSM_RQ(16) RSSM_RQ(32) RSSM_RQ(64) RSSM_RQ(128)
 #undef RSSM_RQ
     return launch_status();

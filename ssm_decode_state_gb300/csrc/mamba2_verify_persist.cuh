@@ -525,7 +525,10 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
                     f2unpack(fma2(dd, f2pack(hv[v].z, hv[v].w), acc23[v]), o[v].z, o[v].w);
                     st_stream(ckp + ctid + v * NC, o[v]);
                 }
-                if (a.read_copy) {
+                if (a.read_copy == 2) {
+                    nv4_quantize_store(o, a.ckpt_q + (tile / P) * nv4_head_bytes(P, N), a.ckpt_scale + tile, P, N,
+                                       [&](int v) { return cw + RSTEP * v; });
+                } else if (a.read_copy) {
                     uint32_t q[VPT];
                     float rs;
                     e4m3_quantize_rows<VPT>(o, q, rs);

@@ -159,7 +159,8 @@ def mamba2_cache(dims: Mamba2Dims, A: torch.Tensor, D: torch.Tensor, ckpt: torch
         ckpt = z(b, H, P, N)
     return Mamba2Cache(
         dims=dims, ckpt=ckpt,
-        ckpt_q=z(b, H, P, N, dtype=torch.uint8) if dims.read_copy else None,
+        ckpt_q=(z(b, H, P, N, dtype=torch.uint8) if dims.read_copy == 1 else
+                z(b, H, P * N // 2 + P * N // 16, dtype=torch.uint8) if dims.read_copy == 2 else None),
         ckpt_scale=z(b, H, P) if dims.read_copy else None,
         rec_dt=z(b, H, L), rec_x=z(b, H, L, P, dtype=io), rec_B=z(b, G, L, N, dtype=io),
         rec_C=z(b, G, L, N, dtype=io) if keep_C else None,

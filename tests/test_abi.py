@@ -96,7 +96,9 @@ def test_null_and_shape_errors(rs):
     assert _decode(rs, _m2(rs, nheads=6, ngroups=4), _cache(rs)) == 3
     assert _decode(rs, _m2(rs, L=0), _cache(rs)) == 3
     assert _decode(rs, _m2(rs, L=33), _cache(rs)) == 3
-    assert _decode(rs, _m2(rs, read_copy=2), _cache(rs)) == 3
+    assert _decode(rs, _m2(rs, read_copy=3), _cache(rs)) == 3
+    assert _decode(rs, _m2(rs, read_copy=-1), _cache(rs)) == 3
+    assert _decode(rs, _m2(rs, read_copy=2), _cache(rs, ckpt_q=None)) == 1   # NVFP4 copy missing
     assert _decode(rs, _m2(rs), _cache(rs, ring_len=None)) == 1
     assert _decode(rs, _m2(rs), _cache(rs, arrive=None)) == 1
     assert _decode(rs, _m2(rs, read_copy=1), _cache(rs, ckpt_q=None)) == 1

@@ -21,6 +21,17 @@ def test_replay_roughly_halves_traffic():
     assert round(period) == 4671968
     assert 0.5 < period / conv < 0.6
     assert round(bm.mamba2_replay_period(u, 16, read_copy=True)) == 1821152
+
+
+def test_nvfp4_copy_bytes():
+    """NVFP4 copy of one sequence: 4-bit codes (512 KiB), an E4M3 scale per 16
+    columns (64 KiB) and a float32 scale per row (32 KiB); every step of a
+    period moves the copy once (15 reads, 1 rewrite at the flush), so the
+    period mean is the FP8 one less the size difference."""
+    u = bm.mamba2_units(128, 64, 128, 8)
+    assert u.Sq4 == 524288 + 65536 + 32768 == 622592
+    assert round(bm.mamba2_replay_period(u, 16, read_copy=2)) == 1821152 - (1081344 - 622592) == 1362400
+    assert bm.mamba2_replay_decode(u, 3, 16, 2) == bm.mamba2_replay_decode(u, 3, 16) - u.S + u.Sq4
     assert bm.mamba2_conventional_verify(u, 4) == 21186560
 
 

@@ -259,16 +259,35 @@ __device__ __forceinline__ float4 e2m1_unpack4(uint32_t w) {
     return make_float4(r[0], r[1], r[2], r[3]);
 }
 
-// Eight E2M1 codes (nibble k = column k) as four pairs of bfloat16 values, each
-// 2^-126 times the code's value (same bit placement as e2m1_unpack4, in the
-// bfloat16 layout), integer operations only.  Pair i holds columns (i, i + 4):
-// those nibbles sit 16 bits apart, so one shift and one mask place both.
-__device__ __forceinline__ void e2m1_to_bf16_pairs(uint32_t w, uint32_t (&p)[4]) {
-    p[0] = ((w << 6) & 0x01c001c0u) | ((w << 12) & 0x80008000u);
-    p[1] = ((w << 2) & 0x01c001c0u) | ((w << 8) & 0x80008000u);
-    p[2] = ((w >> 2) & 0x01c001c0u) | ((w << 4) & 0x80008000u);
-    p[3] = ((w >> 6) & 0x01c001c0u) | (w & 0x80008000u);
+// Eight E2M1 codes (nibble k = column k) -> their values as four f16 pairs,
+// pair i = columns (2i, 2i + 1), by the hardware conversion (E2M1 values are
+// exact in f16).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+    asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
 }
+
+// acc + a.lo * c.lo + a.hi * c.hi: f16 pairs, products exact, FP32
+// accumulation (mixed-precision fma of sm_100 and later).
+__device__ __forceinline__ float fma_f16_pair(uint32_t a, uint32_t c, float acc) {
+    asm("{ .reg .b16 al, ah, cl, ch;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {cl, ch}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, cl, %0;\n\t"
+        "fma.rn.f32.f16 %0, ah, ch, %0; }"
+        : "+f"(acc)
+        : "r"(a), "r"(c));
+    return acc;
+}
+
+// 2^e as a float32 for -126 <= e <= 127.
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
 // NVFP4 copy of 8 rows held by one warp, 32 lanes per row (lane i holds
 // columns 4i..4i+3, so the 16-column block c spans lanes 4c..4c+3), written

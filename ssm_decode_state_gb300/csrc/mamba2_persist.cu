@@ -50,12 +50,17 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
     pc.arrivals = d->nheads / hpi;
     constexpr int VPT = kPersistVPT;
     void *k = nullptr;
-    switch (hpi) {
-        case 8: k = (void *)m2_decode_persistent<128, 64, VPT, 8>; break;
-        case 4: k = (void *)m2_decode_persistent<128, 64, VPT, 4>; break;
-        case 2: k = (void *)m2_decode_persistent<128, 64, VPT, 2>; break;
-        default: k = (void *)m2_decode_persistent<128, 64, VPT, 1>; break;
+#define RSSM_PD(RC)                                                                         \
+    switch (hpi) {                                                                          \
+        case 8: k = (void *)m2_decode_persistent<128, 64, VPT, 8, RC>; break;              \
+        case 4: k = (void *)m2_decode_persistent<128, 64, VPT, 4, RC>; break;              \
+        case 2: k = (void *)m2_decode_persistent<128, 64, VPT, 2, RC>; break;              \
+        default: k = (void *)m2_decode_persistent<128, 64, VPT, 1, RC>; break;             \
     }
+    if (d->read_copy == 2) { RSSM_PD(2) }
+    else if (d->read_copy == 1) { RSSM_PD(1) }
+    else { RSSM_PD(0) }
+#undef RSSM_PD
     rssm_status s = ensure_smem((const void *)k, smem);
     if (s != RSSM_OK) return s;
     M2Args a = args;

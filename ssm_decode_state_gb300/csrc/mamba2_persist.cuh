@@ -98,7 +98,9 @@ struct PSmem {
     }
 };
 
-template <int N, int P, int VPT, int HPI>
+// RC: the cache's read copy (0 none, 1 FP8, 2 NVFP4), fixed per instantiation so
+// that each holds only the consumer paths it runs.
+template <int N, int P, int VPT, int HPI, int RC>
 __global__ void __launch_bounds__(persist_decode_threads(P * N / 4 / VPT), 1)
 m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     constexpr int kPConsumers = P * N / 4 / VPT;         // consumer threads
@@ -133,7 +135,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
 
     const int grid = gridDim.x;
     const int n_my = (pc.items - (int)blockIdx.x + grid - 1) / grid;
-    const bool q8 = a.read_copy == 1, q4 = a.read_copy == 2;
+    constexpr bool q8 = RC == 1, q4 = RC == 2;
     auto item_of = [&](int k) { return (int)blockIdx.x + k * grid; };
     auto item_b = [&](int it) { return it / (G * pc.nchunk); };      // item = (b * G + g) * nchunk + c
     auto item_h0 = [&](int it) {
@@ -503,19 +505,24 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             // NVFP4 codes, Q4 heads per stage.  Lane (blk, rsub) takes the 16-column
             // block blk = lane & 7 of rows rsub and rsub + 4 (rsub = lane >> 3) of the
             // warp's 8 rows: its block sums need one block scale each, then the 8
-            // lanes of a row reduce them.  C_t of the block enters times 2^64 (exact),
-            // so that the products with the codes' 2^-126 offset stay normal floats.
+            // lanes of a row reduce them.  Codes become f16 pairs in hardware; C_t
+            // enters as f16 pairs times 2^e, e set from the item's largest |C_t| so
+            // that it lands just below 2^15: the scaling is exact and cannot
+            // overflow, and only values below max|C_t| 2^-29 lose bits (f16
+            // subnormals).  Products are exact, sums FP32; 2^-e comes off at the end.
             const int blk = lane & 7, rsub = lane >> 3;
-            uint32_t cp[8];                              // pairs (k, k + 4) of each 8-column half
+            float cmax = 0.0f;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+            for (int i = 0; i < 16; ++i) cmax = fmaxf(cmax, fabsf(bf16_at(r_C, blk * 16 + i)));
+            cmax = group_max<32>(cmax);
+            const int ce = cmax > 0.0f ? min(max(14 - ilogbf(cmax), -120), 120) : 0;
+            const float cs = pow2f(ce), cinv = pow2f(-ce);
+            uint32_t cp[8];                              // pairs (2i, 2i + 1) of the block
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c0 = blk * 16 + hf * 8 + i;
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(bf16_at(r_C, c0) * 0x1p64f,
-                                                                    bf16_at(r_C, c0 + 4) * 0x1p64f);
-                    cp[hf * 4 + i] = *reinterpret_cast<const uint32_t *>(&pr);
-                }
+            for (int i = 0; i < 8; ++i) {
+                const __half2 pr = __floats2half2_rn(bf16_at(r_C, blk * 16 + 2 * i) * cs,
+                                                     bf16_at(r_C, blk * 16 + 2 * i + 1) * cs);
+                cp[i] = *reinterpret_cast<const uint32_t *>(&pr);
             }
             for (int uu = 0; uu < HPI / Q4; ++uu, ++u) {
                 const int s = u % S;
@@ -551,13 +558,13 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {
                         uint32_t pa[4], pb[4];
-                        e2m1_to_bf16_pairs(qc[hq][m].x, pa);
-                        e2m1_to_bf16_pairs(qc[hq][m].y, pb);
+                        e2m1x8_to_f16x2(qc[hq][m].x, pa);
+                        e2m1x8_to_f16x2(qc[hq][m].y, pb);
                         float acc = 0.0f;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) acc = fma_bf16_pair(pa[i], cp[i], acc);
+                        for (int i = 0; i < 4; ++i) acc = fma_f16_pair(pa[i], cp[i], acc);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) acc = fma_bf16_pair(pb[i], cp[4 + i], acc);
+                        for (int i = 0; i < 4; ++i) acc = fma_f16_pair(pb[i], cp[4 + i], acc);
                         part[hq * 2 + m] = acc * e4m3_value(sbc[hq][m]);
                     }
                 }
@@ -566,7 +573,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                     const int vi = reduced_index<8, Q4 * 2>(0);
                     const int hh = uu * Q4 + (vi >> 1), row = cw * VPT + rsub + 4 * (vi & 1);
                     a.y[((size_t)b * H + h0 + hh) * P + row] =
-                        fmaf(dec[hh], (part[0] * 0x1p62f) * rsv, rt[hh * P + row]);
+                        fmaf(dec[hh], (part[0] * cinv) * rsv, rt[hh * P + row]);
                 }
             }
         } else if (fp8_item(hd, ln)) {

@@ -189,3 +189,48 @@ def test_nvfp4_pins_catch(monkeypatch, target, mutant):
             except (AssertionError, ValueError):      # a wrong value, or a wrong block count
                 failed += 1
     assert failed > 0
+
+
+def _f16sr_mutants():
+    import oracle.f16sr as sr
+
+    def philox_nine_rounds(ctr, key):
+        c = np.asarray(ctr, np.uint64) & 0xFFFFFFFF
+        k = np.asarray(key, np.uint64) & 0xFFFFFFFF
+        c0, c1, c2, c3 = c[..., 0], c[..., 1], c[..., 2], c[..., 3]
+        k0, k1 = k[..., 0], k[..., 1]
+        for rnd in range(9):
+            if rnd > 0:
+                k0 = (k0 + sr._W0) & 0xFFFFFFFF
+                k1 = (k1 + sr._W1) & 0xFFFFFFFF
+            p0, p1 = c0 * np.uint64(sr._M0), c2 * np.uint64(sr._M1)
+            c0, c1, c2, c3 = (p1 >> np.uint64(32)) ^ c1 ^ k0, p1 & np.uint64(0xFFFFFFFF), \
+                (p0 >> np.uint64(32)) ^ c3 ^ k1, p0 & np.uint64(0xFFFFFFFF)
+        return np.stack([c0, c1, c2, c3], axis=-1).astype(np.uint32)
+
+    def halves_swapped(seed, slot, head, P, N):
+        r = sr._orig_random16(seed, slot, head, P, N)
+        return ((r >> 8) | (r << 8)) & 0xFFFF
+
+    def round_to_nearest(v, r):
+        return np.asarray(v, np.float32).astype(np.float16)
+
+    def round_up_on_equal(v, r):
+        v = np.asarray(v, np.float32)
+        return sr._orig_sr(v, np.asarray(r) - 1)           # r <= p * 65536
+
+    def truncate(v, r):
+        return sr._orig_sr(v, np.full(np.shape(v), 65535))
+
+    return [("philox4x32_10", philox_nine_rounds), ("random16", halves_swapped),
+            ("sr_f16", round_to_nearest), ("sr_f16", round_up_on_equal), ("sr_f16", truncate)]
+
+
+@pytest.mark.parametrize("target,mutant", _f16sr_mutants(), ids=lambda m: getattr(m, "__name__", str(m)))
+def test_f16sr_pins_catch(monkeypatch, target, mutant):
+    import oracle.f16sr as sr
+    from tests import test_oracle_f16sr as pins
+    sr._orig_random16 = sr.random16
+    sr._orig_sr = sr.sr_f16
+    monkeypatch.setattr(sr, target, mutant)
+    assert _run_pins(pins) > 0

@@ -42,6 +42,7 @@ METRIC = "replay SSM decode tokens/s/layer at B=256; achieved HBM GB/s vs GB300 
 UNIT = "seq*tok/s/layer"
 POOL = 32                       # distinct per-step input sets kept on the device
 KERNEL_SOURCES = ["ssm_decode_state_gb300/csrc/mamba2_persist.cuh",
+                  "ssm_decode_state_gb300/csrc/mamba2_persist_launch.cuh",
                   "ssm_decode_state_gb300/csrc/persist_common.cuh",
                   "ssm_decode_state_gb300/csrc/common.cuh"]
 
@@ -430,7 +431,7 @@ def run_sweep(args):
     print(json.dumps({"sweep": out}), flush=True)
 
 
-ROWS = ("fp8", "nvfp4", "verify", "gdn", "gdn_verify")
+ROWS = ("fp8", "nvfp4", "f16ckpt", "f16ckpt_nvfp4", "verify", "gdn", "gdn_verify")
 
 
 def measure_rows(rs, dev, steps, warmup, which=ROWS):
@@ -450,17 +451,23 @@ def measure_rows(rs, dev, steps, warmup, which=ROWS):
         return (torch.from_numpy(st.dt).to(dev), torch.from_numpy(st.x).to(torch.bfloat16).to(dev),
                 torch.from_numpy(st.B).to(torch.bfloat16).to(dev), torch.from_numpy(st.C).to(torch.bfloat16).to(dev))
 
-    for rc, name, wname in ((1, "fp8", "mamba2_fp8read_b256"), (2, "nvfp4", "mamba2_nvfp4read_b256")):
+    for rc, ckf, name, wname in ((1, False, "fp8", "mamba2_fp8read_b256"), (2, False, "nvfp4", "mamba2_nvfp4read_b256"),
+                                 (0, True, "f16ckpt", "mamba2_f16ckpt_b256"),
+                                 (2, True, "f16ckpt_nvfp4", "mamba2_f16ckpt_b256")):
         if name not in which:
             continue
-        # ---- FP8 or NVFP4 read copy, batch 256
+        # ---- FP8 or NVFP4 read copy, and / or an FP16 checkpoint (stochastic rounding), batch 256
         w = wl[wname]
         sh = w.shape
         prm = gen.mamba2_params(sh, w.seed)
-        dims = rs.mamba2_dims(sh.batch, sh.nheads, sh.headdim, sh.dstate, sh.ngroups, sh.L, read_copy=rc)
+        dims = rs.mamba2_dims(sh.batch, sh.nheads, sh.headdim, sh.dstate, sh.ngroups, sh.L, read_copy=rc,
+                              ckpt_f16=ckf)
         ck = torch.randn(sh.batch, sh.nheads, sh.headdim, sh.dstate, device=dev, generator=g).mul_(0.1)
+        if ckf:
+            ck = ck.half()
         cache = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D), ckpt=ck, device=dev)
-        rs.requant(cache)
+        if rc:
+            rs.requant(cache)
         pool = [dev_step(gen.mamba2_step_inputs(sh, prm, w.seed, t)) for t in range(8)]
         y = torch.empty(sh.batch, sh.nheads, sh.headdim, device=dev)
         for t in range(warmup):
@@ -471,7 +478,7 @@ def measure_rows(rs, dev, steps, warmup, which=ROWS):
         K = (steps // sh.L) * sh.L
         alg = 0
         for _ in range(K):
-            alg += bm.mamba2_replay_decode(u, ln, sh.L, read_copy=rc) * sh.batch
+            alg += bm.mamba2_replay_decode(u, ln, sh.L, read_copy=rc, ckpt_f16=ckf) * sh.batch
             ln = 0 if ln + 1 >= sh.L else ln + 1
         ms = _timed(stream, lambda t: rs.decode(cache, *pool[t % 8], y=y), K)
         assert int(cache.err.item()) == 0

@@ -88,10 +88,14 @@ typedef struct {
     int32_t read_copy;  /* 0: reads use the FP32 checkpoint; 1: FP8 E4M3 read copy;
                            2: NVFP4 read copy (E2M1 codes, E4M3 scale per 16 columns) */
     int32_t io_bf16;    /* 1: x, B, C and their records are bf16; 0: float32 */
+    int32_t ckpt_f16;   /* 0: FP32 checkpoint; 1: FP16 checkpoint, rounded stochastically
+                           at every flush (the random integers come from Philox4x32-10
+                           keyed by cache->sr_seed) */
 } rssm_mamba2_dims;
 
 typedef struct {
-    float    *ckpt;       /* [batch][nheads][headdim][dstate] FP32 checkpoint h_c */
+    void     *ckpt;       /* [batch][nheads][headdim][dstate] checkpoint h_c: float32, or
+                             FP16 (IEEE binary16) when dims->ckpt_f16 = 1 */
     uint8_t  *ckpt_q;     /* read_copy = 1: [batch][nheads][headdim][dstate] E4M3 codes;
                              read_copy = 2: per (sequence, head) headdim*dstate*9/16 bytes,
                              the E2M1 codes [headdim][dstate/2] (column 2i in the low
@@ -117,6 +121,13 @@ typedef struct {
      * A slot outside [0, capacity) skips that row and sets RSSM_DEVERR_SLOT. */
     const int32_t *slots; /* [batch] device, or NULL */
     int32_t capacity;
+    /* Seed of this call's stochastic rounding (dims->ckpt_f16 = 1): the element
+     * in column n, row p of head h of cache slot s takes 16 random bits from
+     * Philox4x32-10 with counter (n/8, p, h, s) and key (seed mod 2^32,
+     * seed / 2^32), half n mod 2 of output word (n mod 8)/2.  Pass a new seed
+     * to every call that may flush (decode, verify, flush), e.g. a step count:
+     * a repeated seed repeats the rounding decisions. */
+    uint64_t sr_seed;
 } rssm_mamba2_cache;
 
 /*

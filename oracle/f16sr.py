@@ -25,10 +25,11 @@ Random integers: Philox4x32-10, the counter-based generator of Salmon, Moraes,
 Dror and Shaw ("Parallel random numbers: as easy as 1, 2, 3", SC'11): a 128-bit
 counter and a 64-bit key, ten rounds of two 32x32 -> 64-bit multiplications by
 0xD2511F53 and 0xCD9E8D57 with the key advanced by the Weyl increments
-0x9E3779B9 and 0xBB67AE85 between rounds.  The element in column n, row p of
-head h of cache slot s at a call with seed S takes
-    out = Philox4x32-10(counter = (n / 4, p, h, s), key = (S mod 2^32, S / 2^32))
-    r   = 16-bit half (n mod 2) of word ((n mod 4) / 2) of out  (low half first).
+0x9E3779B9 and 0xBB67AE85 between rounds.  One generator call serves 8
+consecutive columns: the element in column n, row p of head h of cache slot s
+at a call with seed S takes
+    out = Philox4x32-10(counter = (n / 8, p, h, s), key = (S mod 2^32, S / 2^32))
+    r   = 16-bit half (n mod 2) of word ((n mod 8) / 2) of out  (low half first).
 
 The recurrence: the Mamba-2 stepwise update of oracle.mamba2, in float64, from
 an FP16 checkpoint; a flush (the step at which a sequence's ring of L records
@@ -65,15 +66,15 @@ def philox4x32_10(ctr, key) -> np.ndarray:
 
 def random16(seed: int, slot: int, head: int, P: int, N: int) -> np.ndarray:
     """The 16-bit random integers of one head's P x N elements (uint32 [P, N])."""
-    ctr = np.zeros((P, N // 4, 4), np.uint64)
-    ctr[..., 0] = np.arange(N // 4)[None, :]
+    ctr = np.zeros((P, N // 8, 4), np.uint64)
+    ctr[..., 0] = np.arange(N // 8)[None, :]
     ctr[..., 1] = np.arange(P)[:, None]
     ctr[..., 2] = head
     ctr[..., 3] = slot
     key = np.array([seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF], np.uint64)
-    out = philox4x32_10(ctr, key).astype(np.uint64)          # [P, N/4, 4]
+    out = philox4x32_10(ctr, key).astype(np.uint64)          # [P, N/8, 4]
     n = np.arange(N)
-    word = out[:, n // 4, (n % 4) // 2]                      # [P, N]
+    word = out[:, n // 8, (n % 8) // 2]                      # [P, N]
     return ((word >> (16 * (n % 2)).astype(np.uint64)) & 0xFFFF).astype(np.uint32)
 
 

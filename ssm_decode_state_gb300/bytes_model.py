@@ -48,22 +48,24 @@ def _copy_bytes(u: Mamba2Units, read_copy) -> int:
     return {0: 0, 1: u.Sq, 2: u.Sq4}[int(read_copy)]
 
 
-def mamba2_replay_decode(u: Mamba2Units, len_before: int, L: int, read_copy: int = 0) -> int:
+def mamba2_replay_decode(u: Mamba2Units, len_before: int, L: int, read_copy: int = 0,
+                         ckpt_f16: bool = False) -> int:
     """One replay decode step of a sequence holding ``len_before`` records; a
     read copy (1 FP8, 2 NVFP4) replaces the checkpoint read on non-flush steps
-    and is rewritten at the flush."""
+    and is rewritten at the flush; an FP16 checkpoint is half the bytes."""
     fold = len_before + 1 >= L
+    S = u.S // 2 if ckpt_f16 else u.S
     b = u.I + u.Y + len_before * u.Rr
     if fold:
-        b += 2 * u.S + _copy_bytes(u, read_copy)
+        b += 2 * S + _copy_bytes(u, read_copy)
     else:
-        b += (_copy_bytes(u, read_copy) or u.S) + u.Rw
+        b += (_copy_bytes(u, read_copy) or S) + u.Rw
     return b
 
 
-def mamba2_replay_period(u: Mamba2Units, L: int, read_copy: int = 0) -> float:
+def mamba2_replay_period(u: Mamba2Units, L: int, read_copy: int = 0, ckpt_f16: bool = False) -> float:
     """Mean over one flush period of L steps from an empty ring."""
-    return sum(mamba2_replay_decode(u, k, L, read_copy) for k in range(L)) / L
+    return sum(mamba2_replay_decode(u, k, L, read_copy, ckpt_f16) for k in range(L)) / L
 
 
 def mamba2_verify(u: Mamba2Units, len_before: int, T: int, L: int) -> int:

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -333,6 +334,74 @@ __device__ __forceinline__ void nv4_quantize_store(const float4 (&o)[8], uint8_t
         reinterpret_cast<uint16_t *>(hq + row_of(v) * (N / 2))[lane] = (uint16_t)e2m1_pack4(
             __fmul_rn(o[v].x, inv), __fmul_rn(o[v].y, inv), __fmul_rn(o[v].z, inv), __fmul_rn(o[v].w, inv));
     }
+}
+
+// ------------------------------------------------------ FP16 checkpoint (SR)
+//
+// An FP16 checkpoint is rounded stochastically at every flush.  Random
+// integers come from Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel
+// random numbers: as easy as 1, 2, 3", SC'11): counter (column / 8, row,
+// head, cache slot), key = the call's 64-bit seed; the element in column
+// 8q + k takes the 16-bit half k mod 2 of output word k / 2.
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+// Stochastic rounding of v to FP16 with a 16-bit random integer r: lo = the
+// FP16 value at or below |v|, u = the FP16 step above lo, round up when
+// r < 65536 (|v| - lo) / u; |v| >= 65504 saturates.  In the normal FP16 range
+// (a) (|v| - lo) / u is the 13 float32 mantissa bits below the FP16 mantissa
+// over 2^13, so the test is (r >> 3) < those bits and rounding up adds one
+// FP16 step to the truncated bit pattern; below it (b) the step is 2^-24 and
+// every operation is exact in float32.
+__device__ __forceinline__ uint32_t sr_f16(float v, uint32_t r) {
+    const uint32_t ub = __float_as_uint(v), sgn = (ub >> 16) & 0x8000u, ab = ub & 0x7fffffffu;
+    if (ab >= 0x477fe000u) return sgn | 0x7bffu;                  // |v| >= 65504
+    if (ab >= 0x38800000u) {                                      // (a) |v| >= 2^-14
+        const uint32_t t = (ab & ~0x1fffu) + ((r >> 3) < (ab & 0x1fffu) ? 0x2000u : 0u);
+        return sgn | __half_as_ushort(__float2half_rn(__uint_as_float(t)));
+    }
+    const float a = __uint_as_float(ab);                          // (b) FP16 subnormals: step 2^-24
+    const float lo = __half2float(__float2half_rz(a));
+    const float res = __uint2float_rn(r) < (a - lo) * 0x1p40f ? lo + 0x1p-24f : lo;
+    return sgn | __half_as_ushort(__float2half_rn(res));
+}
+
+// Four consecutive columns rounded stochastically to FP16 with the random
+// words w0 (columns 0, 1) and w1 (columns 2, 3), packed low column first; `o`
+// becomes the rounded values.
+__device__ __forceinline__ uint2 sr_f16x4_words(float4 &o, uint32_t w0, uint32_t w1) {
+    const uint32_t e0 = sr_f16(o.x, w0 & 0xffffu), e1 = sr_f16(o.y, w0 >> 16);
+    const uint32_t e2 = sr_f16(o.z, w1 & 0xffffu), e3 = sr_f16(o.w, w1 >> 16);
+    o = make_float4(__half2float(__ushort_as_half((unsigned short)e0)), __half2float(__ushort_as_half((unsigned short)e1)),
+                    __half2float(__ushort_as_half((unsigned short)e2)), __half2float(__ushort_as_half((unsigned short)e3)));
+    return make_uint2(e0 | (e1 << 16), e2 | (e3 << 16));
+}
+
+// Columns 4c..4c+3 of row `row` of head `head` of cache slot `slot`: one
+// generator call for the column group c / 2, words 2 (c mod 2) and 2 (c mod 2) + 1.
+__device__ __forceinline__ uint2 sr_f16x4(float4 &o, uint32_t c, uint32_t row, uint32_t head, uint32_t slot,
+                                          uint32_t seed_lo, uint32_t seed_hi) {
+    const uint4 r = philox4x32_10(make_uint4(c >> 1, row, head, slot), seed_lo, seed_hi);
+    return (c & 1) ? sr_f16x4_words(o, r.z, r.w) : sr_f16x4_words(o, r.x, r.y);
+}
+
+// Four FP16 values (packed low first) -> float4.
+__device__ __forceinline__ float4 f16x4_to_float4(uint2 w) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+    return make_float4(a.x, a.y, b.x, b.y);
 }
 
 // ------------------------------------------------------------------ the ring

@@ -53,6 +53,8 @@ constexpr int persist_decode_threads(int nc) { return nc + 64 + kPrepThreads; }
 // count for NVFP4 copies (Q4).
 __host__ __device__ constexpr int persist_q8(int hpi) { return hpi >= 4 ? 4 : hpi; }
 __host__ __device__ constexpr int persist_q4(int hpi) { return hpi >= 4 ? 4 : hpi; }
+// Heads per stage of an FP16 checkpoint read on non-flush steps.
+__host__ __device__ constexpr int persist_q16(int hpi) { return hpi >= 2 ? 2 : 1; }
 
 struct PSmem {
     int stage_bytes, stages_off;
@@ -60,13 +62,16 @@ struct PSmem {
     int rec_off, rx_off, rB_off, rC_off, rdt_off, rec_bytes;
     int meta_off, cb_off, w_off, decay_off, rt_off, wx_off, ad_off, flag_off, total;
     int pfull_off, pempty_off, wcb_off, sfx_off;
-    __host__ __device__ PSmem(int P, int N, int L, int HPI, int S, int RB, int H, int MY) {
+    // RC: read copy (0 none, 1 FP8, 2 NVFP4); CK: checkpoint precision (0 float32, 1 FP16)
+    __host__ __device__ PSmem(int P, int N, int L, int HPI, int S, int RB, int H, int MY, int RC, int CK) {
         const int KM = L + 1;
         auto up = [](int v, int a) { return (v + a - 1) / a * a; };
-        // one FP32 tile, or the codes and row scales of persist_q8(HPI) heads (FP8), or
-        // the codes, block scales and row scales of persist_q4(HPI) heads (NVFP4)
-        stage_bytes = P * N * 4 > persist_q8(HPI) * (P * N + P * 4) ? P * N * 4 : persist_q8(HPI) * (P * N + P * 4);
-        if (persist_q4(HPI) * (nv4_head_bytes(P, N) + P * 4) > stage_bytes)
+        // one checkpoint tile (float32 or FP16), or the codes and row scales of
+        // persist_q8(HPI) heads (FP8), or the codes, block scales and row scales of
+        // persist_q4(HPI) heads (NVFP4)
+        stage_bytes = CK ? persist_q16(HPI) * P * N * 2 : P * N * 4;
+        if (RC == 1 && persist_q8(HPI) * (P * N + P * 4) > stage_bytes) stage_bytes = persist_q8(HPI) * (P * N + P * 4);
+        if (RC == 2 && persist_q4(HPI) * (nv4_head_bytes(P, N) + P * 4) > stage_bytes)
             stage_bytes = persist_q4(HPI) * (nv4_head_bytes(P, N) + P * 4);
         int o = 0;
         stages_off = o; o += S * stage_bytes;
@@ -98,9 +103,10 @@ struct PSmem {
     }
 };
 
-// RC: the cache's read copy (0 none, 1 FP8, 2 NVFP4), fixed per instantiation so
-// that each holds only the consumer paths it runs.
-template <int N, int P, int VPT, int HPI, int RC>
+// RC: the cache's read copy (0 none, 1 FP8, 2 NVFP4), and CK: the checkpoint's
+// precision (0 float32, 1 FP16 rounded stochastically at flushes), fixed per
+// instantiation so that each holds only the paths it runs.
+template <int N, int P, int VPT, int HPI, int RC, int CK>
 __global__ void __launch_bounds__(persist_decode_threads(P * N / 4 / VPT), 1)
 m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     constexpr int kPConsumers = P * N / 4 / VPT;         // consumer threads
@@ -108,13 +114,15 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     constexpr int CX = P / 8, CB = N / 8;                // 16-byte chunks per x / B row
     constexpr int Q8 = persist_q8(HPI);                  // heads per stage of FP8 codes
     constexpr int Q4 = persist_q4(HPI);                  // heads per stage of NVFP4 codes
+    constexpr int Q16 = persist_q16(HPI);                // heads per stage of FP16 tiles, non-flush steps
     constexpr int HB4 = nv4_head_bytes(P, N);            // one head's NVFP4 codes + block scales
     static_assert(G4 == 32 && VPT == 8 && kPConsumers / 32 * VPT == P, "a warp owns 8 whole consecutive rows");
     extern __shared__ __align__(128) unsigned char smraw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = a.L, H = a.H, G = a.G, hpg = a.hpg, KM = L + 1;
     const int S = pc.stages, RB = pc.recbufs;
-    const PSmem lay(P, N, L, HPI, S, RB, H, pc.max_my);
+    const PSmem lay(P, N, L, HPI, S, RB, H, pc.max_my, RC, CK);
+    constexpr int TB = P * N * (CK ? 2 : 4);             // bytes of one checkpoint tile
     unsigned char *stages = smraw + lay.stages_off;
     uint64_t *full = reinterpret_cast<uint64_t *>(smraw + lay.full_off);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + lay.empty_off);
@@ -147,6 +155,8 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     // per stage; every other item streams FP32 tiles, one head per stage
     auto fp8_item = [&](int hd, int ln) { return q8 && !meta_bad(hd, ln) && ln + 1 < L; };
     auto nv4_item = [&](int hd, int ln) { return q4 && !meta_bad(hd, ln) && ln + 1 < L; };
+    // a non-flush item of an FP16 checkpoint without read copy: Q16 heads per stage
+    auto h16_item = [&](int hd, int ln) { return CK && RC == 0 && !meta_bad(hd, ln) && ln + 1 < L; };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -209,9 +219,9 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         int issued = 0;                                  // stage units issued so far
         for (int k = 0; k < n_my && ok; ++k) {
             const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
-            const bool f8 = fp8_item(hd, ln), f4 = nv4_item(hd, ln);
+            const bool f8 = fp8_item(hd, ln), f4 = nv4_item(hd, ln), f16 = h16_item(hd, ln);
             const int it = item_of(k), sb = s_meta[k * 3 + 2], h0 = item_h0(it);
-            const int nu = f8 ? HPI / Q8 : f4 ? HPI / Q4 : HPI;
+            const int nu = f8 ? HPI / Q8 : f4 ? HPI / Q4 : f16 ? HPI / Q16 : HPI;
             for (int uu = 0; uu < nu; ++uu) {
                 const int t = issued, s = t % S;
                 if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort);
@@ -223,10 +233,16 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                     mbar_arrive_expect_tx(full + s, Q4 * (HB4 + P * 4));
                     bulk_g2s(dst, a.ckpt_q + hd0 * HB4, Q4 * HB4, full + s, pol);
                     bulk_g2s(dst + Q4 * HB4, a.ckpt_scale + hd0 * P, Q4 * P * 4, full + s, pol);
+                } else if (f16) {
+                    // Q16 consecutive heads' FP16 tiles, contiguous in the cache
+                    const size_t tile = ((size_t)sb * H + h0 + uu * Q16) * P;
+                    mbar_arrive_expect_tx(full + s, Q16 * TB);
+                    bulk_g2s(dst, reinterpret_cast<const unsigned char *>(a.ckpt) + tile * N * 2, Q16 * TB, full + s, pol);
                 } else if (!f8) {
                     const size_t tile = ((size_t)sb * H + h0 + uu) * P;
-                    mbar_arrive_expect_tx(full + s, P * N * 4);
-                    bulk_g2s(dst, a.ckpt + tile * N, P * N * 4, full + s, pol);
+                    mbar_arrive_expect_tx(full + s, TB);
+                    bulk_g2s(dst, reinterpret_cast<const unsigned char *>(a.ckpt) + tile * N * (CK ? 2 : 4), TB, full + s,
+                             pol);
                 } else {
                     // Q8 consecutive heads: their codes, then their row scales
                     const size_t tile = ((size_t)sb * H + h0 + uu * Q8) * P;
@@ -501,7 +517,34 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 a.y[((size_t)b * H + h0 + hh) * P + row] = fmaf(dec[hh], part[0], rt[hh * P + row]);
             }
         };
-        if (nv4_item(hd, ln)) {
+        if (h16_item(hd, ln)) {
+            // FP16 checkpoint tiles of Q16 heads per stage: read this warp's rows of
+            // every head, free the stage, then the heads' outputs
+            for (int uu = 0; uu < HPI / Q16; ++uu, ++u) {
+                const int s = u % S;
+                if (live && !pwait(full + s, (uint32_t)((u / S) & 1), s_abort)) {
+                    live = false;
+                    *s_abort = 1;
+                }
+                const uint2 *stg = reinterpret_cast<const uint2 *>(stages + s * lay.stage_bytes);
+                uint2 hw[Q16][VPT];
+#pragma unroll
+                for (int hq = 0; hq < Q16; ++hq) {
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) hw[hq][v] = stg[hq * (P * N / 4) + (cw * VPT + v) * G4 + lane];
+                }
+                __syncwarp();                            // the warp is done with the stage
+                if (lane == 0) mbar_arrive(empty + s);
+                if (!work) continue;
+#pragma unroll
+                for (int hq = 0; hq < Q16; ++hq) {
+                    float4 hv[VPT];
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) hv[v] = f16x4_to_float4(hw[hq][v]);
+                    head_y(uu * Q16 + hq, hv);
+                }
+            }
+        } else if (nv4_item(hd, ln)) {
             // NVFP4 codes, Q4 heads per stage.  Lane (blk, rsub) takes the 16-column
             // block blk = lane & 7 of rows rsub and rsub + 4 (rsub = lane >> 3) of the
             // warp's 8 rows: its block sums need one block scale each, then the 8
@@ -634,10 +677,16 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                     live = false;
                     *s_abort = 1;
                 }
-                const float4 *stg = reinterpret_cast<const float4 *>(stages + s * lay.stage_bytes);
                 float4 hv[VPT];
+                if constexpr (CK) {
+                    const uint2 *stg = reinterpret_cast<const uint2 *>(stages + s * lay.stage_bytes);
 #pragma unroll
-                for (int v = 0; v < VPT; ++v) hv[v] = stg[(cw * VPT + v) * G4 + lane];
+                    for (int v = 0; v < VPT; ++v) hv[v] = f16x4_to_float4(stg[(cw * VPT + v) * G4 + lane]);
+                } else {
+                    const float4 *stg = reinterpret_cast<const float4 *>(stages + s * lay.stage_bytes);
+#pragma unroll
+                    for (int v = 0; v < VPT; ++v) hv[v] = stg[(cw * VPT + v) * G4 + lane];
+                }
                 __syncwarp();                            // the warp is done with the stage
                 if (lane == 0) mbar_arrive(empty + s);
                 if (!work) continue;
@@ -675,13 +724,37 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                     }
                     const float dk = dec[hh];
                     const unsigned long long dd = f2pack(dk, dk);
-                    float4 *ckp = reinterpret_cast<float4 *>(a.ckpt + tile * N);
                     float4 o[VPT];
 #pragma unroll
                     for (int v = 0; v < VPT; ++v) {
                         f2unpack(fma2(dd, f2pack(hv[v].x, hv[v].y), acc01[v]), o[v].x, o[v].y);
                         f2unpack(fma2(dd, f2pack(hv[v].z, hv[v].w), acc23[v]), o[v].z, o[v].w);
-                        st_stream(ckp + (cw * VPT + v) * G4 + lane, o[v]);
+                    }
+                    if constexpr (CK) {
+                        // stochastic rounding to FP16; o[v] becomes the stored values.  One
+                        // generator call serves the 8 columns of a lane pair: the even lane
+                        // draws rows 2m, the odd lane rows 2m + 1, and each passes its
+                        // partner the partner's two words of the row
+                        const bool odd = lane & 1;
+                        uint2 *ck2 = reinterpret_cast<uint2 *>(a.ckpt) + tile * N / 4;
+#pragma unroll
+                        for (int m = 0; m < VPT / 2; ++m) {
+                            const uint4 r = philox4x32_10(
+                                make_uint4((uint32_t)(lane >> 1), (uint32_t)(cw * VPT + 2 * m + odd),
+                                           (uint32_t)(h0 + hh), (uint32_t)sb), a.seed_lo, a.seed_hi);
+                            const uint32_t g0 = __shfl_xor_sync(0xffffffffu, odd ? r.x : r.z, 1);
+                            const uint32_t g1 = __shfl_xor_sync(0xffffffffu, odd ? r.y : r.w, 1);
+                            // select the words first: one rounding call per row for every lane
+                            const int v0 = 2 * m, v1 = 2 * m + 1;
+                            const uint32_t a0 = odd ? g0 : r.x, a1 = odd ? g1 : r.y;
+                            const uint32_t b0 = odd ? r.z : g0, b1 = odd ? r.w : g1;
+                            __stcs(ck2 + (cw * VPT + v0) * G4 + lane, sr_f16x4_words(o[v0], a0, a1));
+                            __stcs(ck2 + (cw * VPT + v1) * G4 + lane, sr_f16x4_words(o[v1], b0, b1));
+                        }
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < VPT; ++v)
+                            st_stream(reinterpret_cast<float4 *>(a.ckpt + tile * N) + (cw * VPT + v) * G4 + lane, o[v]);
                     }
                     if (q4) {
                         nv4_quantize_store(o, a.ckpt_q + ((size_t)sb * H + h0 + hh) * HB4, a.ckpt_scale + tile, P, N,

@@ -38,7 +38,9 @@ enum { kDecode = 0, kVerify = 1, kFlush = 2 };
 struct M2Args {
     int B, H, P, N, G, L, R, split, T, hpg;
     int read_copy, io_bf16;
-    float *ckpt;
+    int ckpt_f16;                     // checkpoint in FP16 (stochastic rounding at flushes)
+    uint32_t seed_lo, seed_hi;        // the call's rounding seed
+    float *ckpt;                      // float32, or FP16 values when ckpt_f16
     uint8_t *ckpt_q;
     float *ckpt_scale;
     float *rec_dt;
@@ -139,7 +141,11 @@ m2_replay_kernel(const M2Args a) {
     uint32_t qv[VPT];
     float qs[VPT];
     const int col4 = tid % G4;
-    if (!use_q) {
+    if (!use_q && a.ckpt_f16) {
+        const uint2 *ck2 = reinterpret_cast<const uint2 *>(a.ckpt) + tile * N / 4;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) hv[v] = f16x4_to_float4(__ldcs(ck2 + tid + v * nthr));
+    } else if (!use_q) {
 #pragma unroll
         for (int v = 0; v < VPT; ++v) hv[v] = ld_stream(ck4 + tid + v * nthr);
     } else if (a.read_copy == 1) {
@@ -315,7 +321,15 @@ m2_replay_kernel(const M2Args a) {
             acc.y = fmaf(fdec, hv[v].y, acc.y);
             acc.z = fmaf(fdec, hv[v].z, acc.z);
             acc.w = fmaf(fdec, hv[v].w, acc.w);
-            st_stream(reinterpret_cast<float4 *>(a.ckpt + tile * N) + tid + v * nthr, acc);
+            if (a.ckpt_f16) {
+                // stochastic rounding to FP16; acc becomes the rounded values (the read copy
+                // below is built from the stored checkpoint)
+                const uint2 w = sr_f16x4(acc, (uint32_t)col4, (uint32_t)(p0 + row), (uint32_t)h, (uint32_t)sb,
+                                         a.seed_lo, a.seed_hi);
+                __stcs(reinterpret_cast<uint2 *>(a.ckpt) + tile * N / 4 + tid + v * nthr, w);
+            } else {
+                st_stream(reinterpret_cast<float4 *>(a.ckpt + tile * N) + tid + v * nthr, acc);
+            }
             if (a.read_copy == 2) {
                 const float m4 = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
                 const float m = group_max<G4>(m4), mb = group_max<4>(m4);

@@ -18,6 +18,7 @@ rssm_status check_dims(const rssm_mamba2_dims *d) {
     if (d->L < 1 || d->L > kMaxL) return RSSM_ERR_SHAPE;
     if (d->read_copy < 0 || d->read_copy > 2) return RSSM_ERR_SHAPE;   // none, FP8 E4M3, NVFP4
     if (d->io_bf16 != 0 && d->io_bf16 != 1) return RSSM_ERR_SHAPE;
+    if (d->ckpt_f16 != 0 && d->ckpt_f16 != 1) return RSSM_ERR_SHAPE;
     if (d->batch > 65535) return RSSM_ERR_SHAPE;
     return RSSM_OK;
 }
@@ -54,7 +55,9 @@ M2Args make_args(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c, const Ti
     a.B = d->batch; a.H = d->nheads; a.P = d->headdim; a.N = d->dstate; a.G = d->ngroups;
     a.L = d->L; a.R = g.R; a.split = g.split; a.T = 0; a.hpg = d->nheads / d->ngroups;
     a.read_copy = d->read_copy; a.io_bf16 = d->io_bf16;
-    a.ckpt = c->ckpt; a.ckpt_q = c->ckpt_q; a.ckpt_scale = c->ckpt_scale;
+    a.ckpt = static_cast<float *>(c->ckpt); a.ckpt_q = c->ckpt_q; a.ckpt_scale = c->ckpt_scale;
+    a.ckpt_f16 = d->ckpt_f16;
+    a.seed_lo = (uint32_t)(c->sr_seed & 0xffffffffu); a.seed_hi = (uint32_t)(c->sr_seed >> 32);
     a.rec_dt = c->rec_dt; a.rec_x = c->rec_x; a.rec_B = c->rec_B; a.rec_C = c->rec_C;
     a.ring_head = c->ring_head; a.ring_len = c->ring_len; a.arrive = c->arrive;
     a.A = c->A; a.D = c->D; a.err = c->err;
@@ -100,12 +103,18 @@ __global__ void rollback_kernel(int batch, int L, int T, const int32_t *accepted
 
 // One thread per float4 of the checkpoint; the N/4 lanes of a row agree on
 // its maximum with shuffles.
+// Four consecutive checkpoint values (float32, or FP16 when f16).
+__device__ __forceinline__ float4 ckpt_load4(const void *ckpt, long long i, int f16) {
+    return f16 ? f16x4_to_float4(__ldcs(reinterpret_cast<const uint2 *>(ckpt) + i))
+               : __ldcs(reinterpret_cast<const float4 *>(ckpt) + i);
+}
+
 template <int N>
-__global__ void requant_kernel(const float *ckpt, uint8_t *q, float *scale, long long n4) {
+__global__ void requant_kernel(const void *ckpt, int f16, uint8_t *q, float *scale, long long n4) {
     constexpr int G4 = N / 4;
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const bool in = i < n4;
-    const float4 h = in ? __ldcs(reinterpret_cast<const float4 *>(ckpt) + i) : make_float4(0, 0, 0, 0);
+    const float4 h = in ? ckpt_load4(ckpt, i, f16) : make_float4(0, 0, 0, 0);
     float m = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
     m = group_max<G4>(m);
     float sc, inv;
@@ -118,11 +127,11 @@ __global__ void requant_kernel(const float *ckpt, uint8_t *q, float *scale, long
 
 // NVFP4 copy: the same thread mapping; a 16-column block spans 4 lanes.
 template <int N>
-__global__ void requant_nv4_kernel(const float *ckpt, uint8_t *q, float *scale, long long n4, int P) {
+__global__ void requant_nv4_kernel(const void *ckpt, int f16, uint8_t *q, float *scale, long long n4, int P) {
     constexpr int G4 = N / 4;
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const bool in = i < n4;
-    const float4 h = in ? __ldcs(reinterpret_cast<const float4 *>(ckpt) + i) : make_float4(0, 0, 0, 0);
+    const float4 h = in ? ckpt_load4(ckpt, i, f16) : make_float4(0, 0, 0, 0);
     const float m4 = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
     const float m = group_max<G4>(m4), mb = group_max<4>(m4);
     float s_r, k_r, inv;
@@ -231,10 +240,11 @@ extern "C" rssm_status replayssm_requant(const rssm_mamba2_dims *d, const rssm_m
 #define RSSM_RQ(NN)                                                                                      \
     if (d->dstate == NN) {                                                                               \
         if (d->read_copy == 2)                                                                           \
-            requant_nv4_kernel<NN><<<(unsigned)blocks, thr, 0, st>>>(c->ckpt, c->ckpt_q, c->ckpt_scale, n4, \
-                                                                     d->headdim);                        \
+            requant_nv4_kernel<NN><<<(unsigned)blocks, thr, 0, st>>>(c->ckpt, d->ckpt_f16, c->ckpt_q,       \
+                                                                     c->ckpt_scale, n4, d->headdim);     \
         else                                                                                             \
-            requant_kernel<NN><<<(unsigned)blocks, thr, 0, st>>>(c->ckpt, c->ckpt_q, c->ckpt_scale, n4);  \
+            requant_kernel<NN><<<(unsigned)blocks, thr, 0, st>>>(c->ckpt, d->ckpt_f16, c->ckpt_q,           \
+                                                                 c->ckpt_scale, n4);                     \
     }
     RSSM_RQ(16) RSSM_RQ(32) RSSM_RQ(64) RSSM_RQ(128)
 #undef RSSM_RQ

@@ -245,6 +245,10 @@ def workloads() -> dict[str, Workload]:
             "mamba2_nvfp4read_b256", "mamba2_nvfp4",
             Mamba2Shape(batch=256, nheads=128, headdim=64, dstate=128, ngroups=8, L=16),
             steps=1024, seed=1006),
+        "mamba2_f16ckpt_b256": Workload(
+            "mamba2_f16ckpt_b256", "mamba2_f16ckpt",
+            Mamba2Shape(batch=256, nheads=128, headdim=64, dstate=128, ngroups=8, L=16),
+            steps=1024, seed=1007),
         "mamba2_verify_b512_T4": Workload(
             "mamba2_verify_b512_T4", "mamba2_verify",
             Mamba2Shape(batch=512, nheads=128, headdim=64, dstate=128, ngroups=8, L=16),

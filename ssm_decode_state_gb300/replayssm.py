@@ -40,13 +40,14 @@ class ReplaySSMError(RuntimeError):
 
 class Mamba2Dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("batch", "nheads", "headdim", "dstate", "ngroups", "L", "read_copy", "io_bf16")]
+                ("batch", "nheads", "headdim", "dstate", "ngroups", "L", "read_copy", "io_bf16", "ckpt_f16")]
 
 
 class Mamba2CacheC(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("ckpt", "ckpt_q", "ckpt_scale", "rec_dt", "rec_x", "rec_B", "rec_C",
-                 "ring_head", "ring_len", "arrive", "A", "D", "err", "slots")] + [("capacity", ctypes.c_int32)]
+                 "ring_head", "ring_len", "arrive", "A", "D", "err", "slots")] + \
+        [("capacity", ctypes.c_int32), ("sr_seed", ctypes.c_uint64)]
 
 
 class GDNDims(ctypes.Structure):
@@ -135,16 +136,26 @@ class Mamba2Cache:
     err: torch.Tensor
     slots: torch.Tensor | None = None      # [batch] int32 cache slot of each batch row (None: row b -> slot b)
     capacity: int = 0                      # sequences the cache holds (0: batch)
+    sr_seed: int = 0                       # seed of the next call's stochastic rounding (FP16 checkpoint)
 
     def c_struct(self, slots=None) -> Mamba2CacheC:
         """The C struct; ``slots`` (int32 [batch] on the device) overrides the cache's map."""
         sl = self.slots if slots is None else slots
-        vals = [_ptr(getattr(self, f)) for f, _ in Mamba2CacheC._fields_[:-2]]
-        return Mamba2CacheC(*vals, _ptr(sl), int(self.capacity))
+        vals = [_ptr(getattr(self, f)) for f, _ in Mamba2CacheC._fields_[:-3]]
+        return Mamba2CacheC(*vals, _ptr(sl), int(self.capacity), int(self.sr_seed) & (2 ** 64 - 1))
+
+    def _seeded(self, slots=None) -> Mamba2CacheC:
+        """The C struct of a call that may flush: it takes the current seed and
+        the next such call the following one."""
+        cs = self.c_struct(slots)
+        self.sr_seed = (int(self.sr_seed) + 1) & (2 ** 64 - 1)
+        return cs
 
 
-def mamba2_dims(batch, nheads, headdim, dstate, ngroups, L=16, read_copy=0, io_bf16=True) -> Mamba2Dims:
-    return Mamba2Dims(batch, nheads, headdim, dstate, ngroups, L, int(read_copy), int(bool(io_bf16)))
+def mamba2_dims(batch, nheads, headdim, dstate, ngroups, L=16, read_copy=0, io_bf16=True,
+                ckpt_f16=False) -> Mamba2Dims:
+    return Mamba2Dims(batch, nheads, headdim, dstate, ngroups, L, int(read_copy), int(bool(io_bf16)),
+                      int(bool(ckpt_f16)))
 
 
 def mamba2_cache(dims: Mamba2Dims, A: torch.Tensor, D: torch.Tensor, ckpt: torch.Tensor | None = None,
@@ -156,7 +167,7 @@ def mamba2_cache(dims: Mamba2Dims, A: torch.Tensor, D: torch.Tensor, ckpt: torch
     io = torch.bfloat16 if dims.io_bf16 else torch.float32
     z = lambda *s, dtype=torch.float32: torch.zeros(*s, dtype=dtype, device=device)  # noqa: E731
     if ckpt is None:
-        ckpt = z(b, H, P, N)
+        ckpt = z(b, H, P, N, dtype=torch.float16 if dims.ckpt_f16 else torch.float32)
     return Mamba2Cache(
         dims=dims, ckpt=ckpt,
         ckpt_q=(z(b, H, P, N, dtype=torch.uint8) if dims.read_copy == 1 else
@@ -175,7 +186,7 @@ def decode(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None, slots=None) -> 
     d = cache.dims
     if y is None:
         y = torch.empty(d.batch, d.nheads, d.headdim, dtype=torch.float32, device=dt.device)
-    cs = cache.c_struct(slots)
+    cs = cache._seeded(slots)
     _check(_lib.replayssm_decode(ctypes.byref(d), ctypes.byref(cs), _ptr(dt), _ptr(x), _ptr(B), _ptr(C),
                                  _ptr(y), _stream(stream)))
     return y
@@ -187,7 +198,7 @@ def decode_noalloc(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None, slots=N
     d = cache.dims
     if y is None:
         y = torch.empty(d.batch, d.nheads, d.headdim, dtype=torch.float32, device=dt.device)
-    cs = cache.c_struct(slots)
+    cs = cache._seeded(slots)
     cs.arrive = None
     _check(_lib.replayssm_decode_noalloc(ctypes.byref(d), ctypes.byref(cs), _ptr(dt), _ptr(x), _ptr(B),
                                          _ptr(C), _ptr(y), _stream(stream)))
@@ -195,7 +206,7 @@ def decode_noalloc(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None, slots=N
 
 
 def flush(cache: Mamba2Cache, mask=None, stream=None, slots=None) -> None:
-    cs = cache.c_struct(slots)
+    cs = cache._seeded(slots)
     _check(_lib.replayssm_flush(ctypes.byref(cache.dims), ctypes.byref(cs), _ptr(mask), _stream(stream)))
 
 
@@ -204,7 +215,7 @@ def verify(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None, slots=None) -> 
     T = dt.shape[1]
     if y is None:
         y = torch.empty(d.batch, T, d.nheads, d.headdim, dtype=torch.float32, device=dt.device)
-    cs = cache.c_struct(slots)
+    cs = cache._seeded(slots)
     _check(_lib.replayssm_verify(ctypes.byref(d), ctypes.byref(cs), T, _ptr(dt), _ptr(x), _ptr(B), _ptr(C),
                                  _ptr(y), _stream(stream)))
     return y

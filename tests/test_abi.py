@@ -43,9 +43,11 @@ def test_struct_layout_matches_binding(rs, tmp_path):
 #include <stddef.h>
 #include "replayssm.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(rssm_mamba2_dims), sizeof(rssm_mamba2_cache),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(rssm_mamba2_dims), sizeof(rssm_mamba2_cache),
          sizeof(rssm_gdn_dims), sizeof(rssm_gdn_cache), offsetof(rssm_mamba2_cache, err),
-         offsetof(rssm_mamba2_cache, arrive), offsetof(rssm_gdn_cache, err));
+         offsetof(rssm_mamba2_cache, arrive), offsetof(rssm_gdn_cache, err),
+         offsetof(rssm_mamba2_cache, capacity), offsetof(rssm_mamba2_cache, sr_seed),
+         offsetof(rssm_mamba2_dims, ckpt_f16));
   return 0;
 }''')
     exe = tmp_path / "probe"
@@ -55,7 +57,8 @@ int main(void) {
                                           check=True).stdout.split()]
     assert out == [ctypes.sizeof(rs.Mamba2Dims), ctypes.sizeof(rs.Mamba2CacheC),
                    ctypes.sizeof(rs.GDNDims), ctypes.sizeof(rs.GDNCacheC),
-                   rs.Mamba2CacheC.err.offset, rs.Mamba2CacheC.arrive.offset, rs.GDNCacheC.err.offset]
+                   rs.Mamba2CacheC.err.offset, rs.Mamba2CacheC.arrive.offset, rs.GDNCacheC.err.offset,
+                   rs.Mamba2CacheC.capacity.offset, rs.Mamba2CacheC.sr_seed.offset, rs.Mamba2Dims.ckpt_f16.offset]
 
 
 def test_status_strings(rs):
@@ -71,7 +74,7 @@ MIS = 0x10008
 
 
 def _m2(rs, **kw):
-    d = dict(batch=2, nheads=4, headdim=16, dstate=16, ngroups=1, L=16, read_copy=0, io_bf16=1)
+    d = dict(batch=2, nheads=4, headdim=16, dstate=16, ngroups=1, L=16, read_copy=0, io_bf16=1, ckpt_f16=0)
     d.update(kw)
     return rs.Mamba2Dims(**d)
 
@@ -97,6 +100,7 @@ def test_null_and_shape_errors(rs):
     assert _decode(rs, _m2(rs, L=0), _cache(rs)) == 3
     assert _decode(rs, _m2(rs, L=33), _cache(rs)) == 3
     assert _decode(rs, _m2(rs, read_copy=3), _cache(rs)) == 3
+    assert _decode(rs, _m2(rs, ckpt_f16=2), _cache(rs)) == 3
     assert _decode(rs, _m2(rs, read_copy=-1), _cache(rs)) == 3
     assert _decode(rs, _m2(rs, read_copy=2), _cache(rs, ckpt_q=None)) == 1   # NVFP4 copy missing
     assert _decode(rs, _m2(rs), _cache(rs, ring_len=None)) == 1

@@ -32,6 +32,15 @@ def test_nvfp4_copy_bytes():
     assert u.Sq4 == 524288 + 65536 + 32768 == 622592
     assert round(bm.mamba2_replay_period(u, 16, read_copy=2)) == 1821152 - (1081344 - 622592) == 1362400
     assert bm.mamba2_replay_decode(u, 3, 16, 2) == bm.mamba2_replay_decode(u, 3, 16) - u.S + u.Sq4
+
+
+def test_fp16_checkpoint_bytes():
+    """An FP16 checkpoint (2 MiB per sequence) halves the checkpoint term of
+    every step: read on non-flush steps, read and written at the flush."""
+    u = bm.mamba2_units(128, 64, 128, 8)
+    assert bm.mamba2_replay_decode(u, 3, 16, ckpt_f16=True) == bm.mamba2_replay_decode(u, 3, 16) - 2 * 1024 * 1024
+    assert bm.mamba2_replay_decode(u, 15, 16, ckpt_f16=True) == bm.mamba2_replay_decode(u, 15, 16) - 4 * 1024 * 1024
+    assert round(bm.mamba2_replay_period(u, 16, ckpt_f16=True)) == 4671968 - (15 * 2 + 4) * 1024 * 1024 // 16
     assert bm.mamba2_conventional_verify(u, 4) == 21186560
 
 

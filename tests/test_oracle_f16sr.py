@@ -27,15 +27,15 @@ def test_philox_known_answers():
 
 
 def test_random16_element_mapping():
-    """Element (p, n) of a head takes half n mod 2 of word (n mod 4) / 2 of the
-    Philox output for counter (n / 4, p, head, slot), checked one call at a time."""
+    """Element (p, n) of a head takes half n mod 2 of word (n mod 8) / 2 of the
+    Philox output for counter (n / 8, p, head, slot), checked one call at a time."""
     seed, slot, head, P, N = 0x1234_5678_9ABC_DEF0, 7, 3, 4, 16
     r = sr.random16(seed, slot, head, P, N)
     key = np.array([seed & 0xFFFFFFFF, seed >> 32], np.uint64)
     for p in range(P):
         for n in range(N):
-            out = sr.philox4x32_10(np.array([n // 4, p, head, slot], np.uint64), key)
-            w = int(out[(n % 4) // 2])
+            out = sr.philox4x32_10(np.array([n // 8, p, head, slot], np.uint64), key)
+            w = int(out[(n % 8) // 2])
             assert int(r[p, n]) == (w >> (16 * (n % 2))) & 0xFFFF
 
 

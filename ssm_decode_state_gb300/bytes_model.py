@@ -114,3 +114,27 @@ def gdn_verify(u: GDNUnits, len_before: int, T: int, L: int) -> int:
     the T drafts' inputs and outputs, their records appended, the buffered records read."""
     pre = len_before + T > L
     return u.S + (u.S if pre else 0) + T * (u.I + u.Y + u.Rw) + len_before * u.Rr
+
+
+def mamba2_cache_bytes(nheads, headdim, dstate, ngroups, L, io_bytes=2, keep_C=True,
+                       read_copy: int = 0, ckpt_f16: bool = False) -> dict:
+    """Device memory one sequence's replay cache holds per layer, by part: the
+    checkpoint, the read copy, the ring of L records and its pointers.  Engines
+    that cap concurrent requests by state memory now hold the record buffer
+    beside each checkpoint, so their accounting changes with it (AT Pulse,
+    cost item); the conventional state is the checkpoint alone."""
+    H, P, N, G = nheads, headdim, dstate, ngroups
+    u = mamba2_units(H, P, N, G, io_bytes, keep_C)
+    ckpt = u.S // 2 if ckpt_f16 else u.S
+    ring = L * (H * 4 + H * P * io_bytes + (2 if keep_C else 1) * G * N * io_bytes)
+    parts = {"checkpoint": ckpt, "read_copy": _copy_bytes(u, read_copy), "ring": ring, "pointers": 12}
+    parts["total"] = sum(parts.values())
+    parts["conventional"] = u.S
+    return parts
+
+
+def sequences_that_fit(budget_bytes: int, layers: int, **cache_kw) -> dict:
+    """Concurrent sequences a device-memory budget holds for `layers` SSM layers,
+    replay cache against conventional state."""
+    c = mamba2_cache_bytes(**cache_kw)
+    return {"replay": budget_bytes // (layers * c["total"]), "conventional": budget_bytes // (layers * c["conventional"])}

@@ -59,3 +59,22 @@ def test_gdn_verify_bytes():
     base = bm.gdn_verify(u, 0, 4, 16)
     assert base == u.S + 4 * (u.I + u.Y + u.Rw)
     assert bm.gdn_verify(u, 13, 4, 16) - bm.gdn_verify(u, 12, 4, 16) == u.S + u.Rr   # 13 + 4 > 16 pre-flushes
+
+
+def test_cache_memory_accounting():
+    """Per sequence and layer at the serving shape: the 4 MiB checkpoint plus a ring of
+    16 records of 20,992 bytes (dt, x, B, C) and 12 bytes of pointers; the read copies
+    add their size, an FP16 checkpoint halves the first term.  In 100 GiB of cache for
+    24 SSM layers that is 987 replay sequences against 1,066 conventional ones (FP32), and
+    1,464 with an FP16 checkpoint and NVFP4 reads."""
+    kw = dict(nheads=128, headdim=64, dstate=128, ngroups=8, L=16)
+    c = bm.mamba2_cache_bytes(**kw)
+    assert c["checkpoint"] == 4 * 1024 * 1024 and c["ring"] == 16 * 20992 and c["pointers"] == 12
+    assert c["total"] == 4194304 + 335872 + 12
+    assert bm.mamba2_cache_bytes(**kw, read_copy=1)["read_copy"] == 1081344
+    assert bm.mamba2_cache_bytes(**kw, read_copy=2, ckpt_f16=True)["total"] == 2097152 + 622592 + 335872 + 12
+    fit = bm.sequences_that_fit(100 * 2 ** 30, 24, **kw)
+    assert fit == {"replay": 100 * 2 ** 30 // (24 * 4530188), "conventional": 100 * 2 ** 30 // (24 * 4194304)}
+    assert fit["replay"] == 987 and fit["conventional"] == 1066
+    assert bm.sequences_that_fit(100 * 2 ** 30, 24, **kw, read_copy=2, ckpt_f16=True)["replay"] == \
+        100 * 2 ** 30 // (24 * 3055628) == 1464

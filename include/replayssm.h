@@ -297,6 +297,12 @@ typedef struct {
     int32_t  *ring_len;   /* [batch] */
     int32_t  *arrive;     /* [batch] scratch counters, zero before the first call */
     uint32_t *err;
+    /* Cache-slot indirection, as for the Mamba-2 cache: the arrays above hold
+     * `capacity` sequences and batch row b uses slot slots[b] (NULL: slot b;
+     * capacity 0: batch; distinct slots per call; an out-of-range slot skips
+     * its row and sets RSSM_DEVERR_SLOT). */
+    const int32_t *slots; /* [batch] device, or NULL */
+    int32_t capacity;
 } rssm_gdn_cache;
 
 /*

@@ -32,6 +32,8 @@ struct GArgs {
     const float *alpha, *beta;
     float *o;
     const uint8_t *mask;
+    const int32_t *slots;   // [batch] cache slot of each batch row; nullptr: row b uses slot b
+    int cap;                // sequences the cache arrays hold
 };
 
 struct GSmem {
@@ -64,8 +66,13 @@ __global__ void __launch_bounds__(256) gdn_replay_kernel(const GArgs a) {
     const int h = blockIdx.x / a.split, sp = blockIdx.x - h * a.split;
     const int R = a.R, L = a.L, H = a.H, DV = a.DV;
     const int p0 = sp * R;
+    const int sb = a.slots ? __ldg(a.slots + b) : b;           // the sequence's cache slot
+    if (sb < 0 || sb >= a.cap) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.err, RSSM_DEVERR_SLOT);
+        return;
+    }
 
-    const int head = a.ring_head[b], len = a.ring_len[b];
+    const int head = a.ring_head[sb], len = a.ring_len[sb];
     if (head < 0 || head >= L || len < 0 || len > L) {
         if (blockIdx.x == 0 && tid == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
         return;
@@ -74,7 +81,7 @@ __global__ void __launch_bounds__(256) gdn_replay_kernel(const GArgs a) {
     const int nrec = MODE == gDecode ? len + 1 : len;
     const bool fold = MODE == gDecode ? (len + 1 >= L) : true;
 
-    const size_t tile = ((size_t)b * H + h) * DV + p0;
+    const size_t tile = ((size_t)sb * H + h) * DV + p0;        // cache rows
     float4 *ck4 = reinterpret_cast<float4 *>(a.ckpt + tile * DK);
     float4 hv[VPT];
 #pragma unroll
@@ -85,7 +92,7 @@ __global__ void __launch_bounds__(256) gdn_replay_kernel(const GArgs a) {
     float *s_k = sm + lay.k, *s_v = sm + lay.v, *s_q = sm + lay.q, *s_u = sm + lay.u, *s_o = sm + lay.o;
 
     // ---- stage records (ring slots for j < len, the current token at j = len)
-    const size_t bh = (size_t)b * H + h;
+    const size_t bh = (size_t)b * H + h, cbh = (size_t)sb * H + h;   // inputs / outputs, cache
     const int ck = DK / 8, cv = R / 8;
     const int nk = nrec * ck, nv = nrec * cv, nq = (MODE == gDecode) ? ck : 0;
     const int total = nk + nv + nq;
@@ -100,12 +107,12 @@ __global__ void __launch_bounds__(256) gdn_replay_kernel(const GArgs a) {
                 const uint16_t *src;
                 if (idx < nk) {
                     const int j = idx / ck, c = idx - j * ck;
-                    src = j < len ? a.rec_k + ((bh * L + (head + j) % L) * DK + c * 8) : a.k + (bh * DK + c * 8);
+                    src = j < len ? a.rec_k + ((cbh * L + (head + j) % L) * DK + c * 8) : a.k + (bh * DK + c * 8);
                     dst[u] = s_k + j * DK + c * 8;
                 } else if (idx < nk + nv) {
                     const int m = idx - nk;
                     const int j = m / cv, c = m - j * cv;
-                    src = j < len ? a.rec_v + ((bh * L + (head + j) % L) * DV + p0 + c * 8)
+                    src = j < len ? a.rec_v + ((cbh * L + (head + j) % L) * DV + p0 + c * 8)
                                   : a.v + (bh * DV + p0 + c * 8);
                     dst[u] = s_v + j * R + c * 8;
                 } else {
@@ -122,7 +129,7 @@ __global__ void __launch_bounds__(256) gdn_replay_kernel(const GArgs a) {
     }
     for (int j = tid; j < nrec; j += nthr) {
         if (j < len) {
-            const size_t r = bh * L + (head + j) % L;
+            const size_t r = cbh * L + (head + j) % L;
             s_al[j] = __ldcg(a.rec_alpha + r);
             s_be[j] = __ldcg(a.rec_beta + r);
         } else {
@@ -225,15 +232,15 @@ __global__ void __launch_bounds__(256) gdn_replay_kernel(const GArgs a) {
         if (!fold) {
             const int slot = (head + len) % L;
             for (int c = tid; c < cv; c += nthr)
-                *reinterpret_cast<uint4 *>(a.rec_v + (bh * L + slot) * DV + p0 + c * 8) =
+                *reinterpret_cast<uint4 *>(a.rec_v + (cbh * L + slot) * DV + p0 + c * 8) =
                     __ldcg(reinterpret_cast<const uint4 *>(a.v + bh * DV + p0 + c * 8));
             if (sp == 0) {
                 for (int c = tid; c < ck; c += nthr)
-                    *reinterpret_cast<uint4 *>(a.rec_k + (bh * L + slot) * DK + c * 8) =
+                    *reinterpret_cast<uint4 *>(a.rec_k + (cbh * L + slot) * DK + c * 8) =
                         __ldcg(reinterpret_cast<const uint4 *>(a.k + bh * DK + c * 8));
                 if (tid == 0) {
-                    a.rec_alpha[bh * L + slot] = s_al[len];
-                    a.rec_beta[bh * L + slot] = s_be[len];
+                    a.rec_alpha[cbh * L + slot] = s_al[len];
+                    a.rec_beta[cbh * L + slot] = s_be[len];
                 }
             }
         }
@@ -243,17 +250,17 @@ __global__ void __launch_bounds__(256) gdn_replay_kernel(const GArgs a) {
     __syncthreads();
     if (tid == 0) {
         __threadfence();
-        const int prev = atomicAdd(a.arrive + b, 1);
+        const int prev = atomicAdd(a.arrive + sb, 1);
         if (prev == (int)gridDim.x - 1) {
             __threadfence();
             if (MODE == gDecode) {
-                a.ring_head[b] = fold ? (head + len + 1) % L : head;
-                a.ring_len[b] = fold ? 0 : len + 1;
+                a.ring_head[sb] = fold ? (head + len + 1) % L : head;
+                a.ring_len[sb] = fold ? 0 : len + 1;
             } else {
-                a.ring_head[b] = (head + len) % L;
-                a.ring_len[b] = 0;
+                a.ring_head[sb] = (head + len) % L;
+                a.ring_len[sb] = 0;
             }
-            a.arrive[b] = 0;
+            a.arrive[sb] = 0;
         }
     }
 }
@@ -287,8 +294,13 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const GArgs a) {
     const int h = blockIdx.x / a.split, sp = blockIdx.x - h * a.split;
     const int R = a.R, L = a.L, H = a.H, DV = a.DV, T = a.T;
     const int p0 = sp * R;
+    const int sb = a.slots ? __ldg(a.slots + b) : b;           // the sequence's cache slot
+    if (sb < 0 || sb >= a.cap) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.err, RSSM_DEVERR_SLOT);
+        return;
+    }
 
-    const int head = a.ring_head[b], len = a.ring_len[b];
+    const int head = a.ring_head[sb], len = a.ring_len[sb];
     if (head < 0 || head >= L || len < 0 || len > L) {
         if (blockIdx.x == 0 && tid == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
         return;
@@ -296,7 +308,7 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const GArgs a) {
     const bool pre = len + T > L;
     const int nrec = len + T, KM = L + T;
 
-    const size_t tile = ((size_t)b * H + h) * DV + p0;
+    const size_t tile = ((size_t)sb * H + h) * DV + p0;        // cache rows
     float4 *ck4 = reinterpret_cast<float4 *>(a.ckpt + tile * DK);
     float4 hv[VPT];
 #pragma unroll
@@ -307,7 +319,7 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const GArgs a) {
     float *s_k = sm + lay.k, *s_v = sm + lay.v, *s_q = sm + lay.q, *s_u = sm + lay.u, *s_o = sm + lay.o;
 
     // ---- stage the records (ring slots, then the drafts) and the drafts' q
-    const size_t bh = (size_t)b * H + h;
+    const size_t cbh = (size_t)sb * H + h;                       // cache
     const int ck = DK / 8, cv = R / 8;
     const int nk = nrec * ck, nv = nrec * cv, nq = T * ck, total = nk + nv + nq;
     for (int idx = tid; idx < total; idx += nthr) {
@@ -315,12 +327,12 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const GArgs a) {
         float *dst;
         if (idx < nk) {
             const int j = idx / ck, c = idx - j * ck;
-            src = j < len ? a.rec_k + ((bh * L + (head + j) % L) * DK + c * 8)
+            src = j < len ? a.rec_k + ((cbh * L + (head + j) % L) * DK + c * 8)
                           : a.k + ((((size_t)b * T + (j - len)) * H + h) * DK + c * 8);
             dst = s_k + j * DK + c * 8;
         } else if (idx < nk + nv) {
             const int m = idx - nk, j = m / cv, c = m - j * cv;
-            src = j < len ? a.rec_v + ((bh * L + (head + j) % L) * DV + p0 + c * 8)
+            src = j < len ? a.rec_v + ((cbh * L + (head + j) % L) * DV + p0 + c * 8)
                           : a.v + ((((size_t)b * T + (j - len)) * H + h) * DV + p0 + c * 8);
             dst = s_v + j * R + c * 8;
         } else {
@@ -332,7 +344,7 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const GArgs a) {
     }
     for (int j = tid; j < nrec; j += nthr) {
         if (j < len) {
-            const size_t r = bh * L + (head + j) % L;
+            const size_t r = cbh * L + (head + j) % L;
             s_al[j] = __ldcg(a.rec_alpha + r);
             s_be[j] = __ldcg(a.rec_beta + r);
         } else {
@@ -439,11 +451,11 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const GArgs a) {
     __syncthreads();
     if (tid == 0) {
         __threadfence();
-        if (atomicAdd(a.arrive + b, 1) == (int)gridDim.x - 1) {
+        if (atomicAdd(a.arrive + sb, 1) == (int)gridDim.x - 1) {
             __threadfence();
-            a.ring_head[b] = pre ? (head + len) % L : head;
-            a.ring_len[b] = (pre ? 0 : len) + T;
-            a.arrive[b] = 0;
+            a.ring_head[sb] = pre ? (head + len) % L : head;
+            a.ring_len[sb] = (pre ? 0 : len) + T;
+            a.arrive[sb] = 0;
         }
     }
 }
@@ -452,13 +464,15 @@ __global__ void __launch_bounds__(256) gdn_verify_kernel(const GArgs a) {
 // the last T slots of the ring, whose pointers the verify has committed.
 __global__ void gdn_verify_append(const GArgs a) {
     const int bh = blockIdx.x, b = bh / a.H, h = bh - b * a.H;
-    const int hd = a.ring_head[b], ln = a.ring_len[b], L = a.L, T = a.T, DK = a.DK, DV = a.DV;
+    const int sb = a.slots ? __ldg(a.slots + b) : b;           // (the verify flagged a bad slot)
+    if (sb < 0 || sb >= a.cap) return;
+    const int hd = a.ring_head[sb], ln = a.ring_len[sb], L = a.L, T = a.T, DK = a.DK, DV = a.DV;
     if (hd < 0 || hd >= L || ln < T || ln > L) return;
     const int ck = DK / 8, cv = DV / 8;
     for (int idx = threadIdx.x; idx < T * (ck + cv + 1); idx += blockDim.x) {
         const int i = idx / (ck + cv + 1), c = idx - i * (ck + cv + 1);
         const int slot = (hd + ln - T + i) % L;
-        const size_t src = ((size_t)b * T + i) * a.H + h, dst = (size_t)bh * L + slot;
+        const size_t src = ((size_t)b * T + i) * a.H + h, dst = ((size_t)sb * a.H + h) * L + slot;
         if (c < ck) {
             *reinterpret_cast<uint4 *>(a.rec_k + dst * DK + c * 8) =
                 __ldcg(reinterpret_cast<const uint4 *>(a.k + src * DK + c * 8));
@@ -547,13 +561,18 @@ rssm_status check(const rssm_gdn_dims *d) {
     return RSSM_OK;
 }
 
-rssm_status check_cache(const rssm_gdn_cache *c) {
+rssm_status check_cache(const rssm_gdn_dims *d, const rssm_gdn_cache *c) {
     if (!c) return RSSM_ERR_NULL;
     if (!c->ckpt || !c->rec_k || !c->rec_v || !c->rec_alpha || !c->rec_beta || !c->ring_head ||
         !c->ring_len || !c->arrive || !c->err)
         return RSSM_ERR_NULL;
     if (!aligned16(c->ckpt) || !aligned16(c->rec_k) || !aligned16(c->rec_v)) return RSSM_ERR_ALIGN;
+    if (c->capacity < 0 || (!c->slots && c->capacity > 0 && c->capacity < d->batch)) return RSSM_ERR_SHAPE;
     return RSSM_OK;
+}
+
+int cache_capacity(const rssm_gdn_dims *d, const rssm_gdn_cache *c) {
+    return c->capacity > 0 ? c->capacity : d->batch;
 }
 
 template <int MODE>
@@ -587,10 +606,11 @@ GArgs make_args(const rssm_gdn_dims *d, const TileGeom &g) {
     return a;
 }
 
-void set_cache(GArgs &a, const rssm_gdn_cache *c) {
+void set_cache(GArgs &a, const rssm_gdn_dims *d, const rssm_gdn_cache *c) {
     a.ckpt = c->ckpt; a.rec_k = c->rec_k; a.rec_v = c->rec_v; a.rec_alpha = c->rec_alpha;
     a.rec_beta = c->rec_beta; a.ring_head = c->ring_head; a.ring_len = c->ring_len;
     a.arrive = c->arrive; a.err = c->err;
+    a.slots = c->slots; a.cap = cache_capacity(d, c);
 }
 
 rssm_status launch(void *k, const rssm_gdn_dims *d, GArgs &a, const TileGeom &g, size_t smem,
@@ -630,6 +650,7 @@ rssm_status launch_persistent(const rssm_gdn_dims *d, const rssm_gdn_cache *c, c
     a.ckpt = c->ckpt; a.rec_k = c->rec_k; a.rec_v = c->rec_v; a.rec_alpha = c->rec_alpha; a.rec_beta = c->rec_beta;
     a.ring_head = c->ring_head; a.ring_len = c->ring_len; a.arrive = c->arrive; a.err = c->err;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.o = o;
+    a.slots = c->slots; a.cap = cache_capacity(d, c);
     void *kern = (void *)gdn_decode_persistent<128, 128>;
     rssm_status s = ensure_smem((const void *)kern, smem);
     if (s != RSSM_OK) return s;
@@ -649,7 +670,7 @@ extern "C" rssm_status replayssm_gdn_decode(const rssm_gdn_dims *d, const rssm_g
                                             const float *beta, float *o, void *stream) {
     rssm_status s = check(d);
     if (s != RSSM_OK) return s;
-    if ((s = check_cache(c)) != RSSM_OK) return s;
+    if ((s = check_cache(d, c)) != RSSM_OK) return s;
     if (!q || !k || !v || !alpha || !beta || !o) return RSSM_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return RSSM_ERR_ALIGN;
     s = launch_persistent(d, c, q, k, v, alpha, beta, o, static_cast<cudaStream_t>(stream));
@@ -657,7 +678,7 @@ extern "C" rssm_status replayssm_gdn_decode(const rssm_gdn_dims *d, const rssm_g
     TileGeom g;
     if (!choose_geom(d->batch, d->nheads, d->dv, d->dk, g)) return RSSM_ERR_UNSUPPORTED;
     GArgs a = make_args(d, g);
-    set_cache(a, c);
+    set_cache(a, d, c);
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.o = o;
     const size_t smem = (size_t)GSmem(d->L, g.R, d->dk).total * sizeof(float);
     return launch(pick_replay<gDecode>(d->dk, g.vpt), d, a, g, smem, static_cast<cudaStream_t>(stream));
@@ -667,11 +688,11 @@ extern "C" rssm_status replayssm_gdn_flush(const rssm_gdn_dims *d, const rssm_gd
                                            void *stream) {
     rssm_status s = check(d);
     if (s != RSSM_OK) return s;
-    if ((s = check_cache(c)) != RSSM_OK) return s;
+    if ((s = check_cache(d, c)) != RSSM_OK) return s;
     TileGeom g;
     if (!choose_geom(d->batch, d->nheads, d->dv, d->dk, g)) return RSSM_ERR_UNSUPPORTED;
     GArgs a = make_args(d, g);
-    set_cache(a, c);
+    set_cache(a, d, c);
     a.mask = mask;
     const size_t smem = (size_t)GSmem(d->L, g.R, d->dk).total * sizeof(float);
     return launch(pick_replay<gFlush>(d->dk, g.vpt), d, a, g, smem, static_cast<cudaStream_t>(stream));
@@ -682,14 +703,14 @@ extern "C" rssm_status replayssm_gdn_verify(const rssm_gdn_dims *d, const rssm_g
                                             const float *alpha, const float *beta, float *o, void *stream) {
     rssm_status s = check(d);
     if (s != RSSM_OK) return s;
-    if ((s = check_cache(c)) != RSSM_OK) return s;
+    if ((s = check_cache(d, c)) != RSSM_OK) return s;
     if (T < 1 || T > kMaxT || T > d->L) return RSSM_ERR_RING;
     if (!q || !k || !v || !alpha || !beta || !o) return RSSM_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return RSSM_ERR_ALIGN;
     TileGeom g;
     if (!choose_geom(d->batch, d->nheads, d->dv, d->dk, g)) return RSSM_ERR_UNSUPPORTED;
     GArgs a = make_args(d, g);
-    set_cache(a, c);
+    set_cache(a, d, c);
     a.T = T; a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.o = o;
     const size_t smem = (size_t)GVSmem(d->L, T, g.R, d->dk).total * sizeof(float);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -704,7 +725,9 @@ extern "C" rssm_status replayssm_gdn_rollback(const rssm_gdn_dims *d, const rssm
     if (s != RSSM_OK) return s;
     if (!c || !c->ring_head || !c->ring_len || !c->err || !accepted) return RSSM_ERR_NULL;
     if (T < 1 || T > kMaxT || T > d->L) return RSSM_ERR_RING;
-    return rssm::launch_ring_rollback(d->batch, d->L, T, accepted, nullptr, d->batch, c->ring_head, c->ring_len,
+    if (c->capacity < 0 || (!c->slots && c->capacity > 0 && c->capacity < d->batch)) return RSSM_ERR_SHAPE;
+    return rssm::launch_ring_rollback(d->batch, d->L, T, accepted, c->slots, cache_capacity(d, c), c->ring_head,
+                                      c->ring_len,
                                       c->err, static_cast<cudaStream_t>(stream));
 }
 

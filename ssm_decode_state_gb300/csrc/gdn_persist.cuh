@@ -40,6 +40,8 @@ struct GPArgs {
     const uint16_t *q, *k, *v;
     const float *alpha, *beta;
     float *o;
+    const int32_t *slots;   // [batch] cache slot of each batch row; nullptr: row b uses slot b
+    int cap;                // sequences the cache arrays hold
 };
 
 constexpr int kGdnRows = 64;     // state rows per stage
@@ -75,7 +77,7 @@ struct GPSmem {
         rbe_off = ral_off + up(KM * 4, 16);
         rec_bytes = up(rbe_off + KM * 4, 128);
         rec_off = o;  o += RB * rec_bytes;
-        meta_off = o; o += up(MY * 8, 16);                  // [items of this CTA][head, len]
+        meta_off = o; o += up(MY * 12, 16);                 // [items of this CTA][head, len, cache slot]
         u_off = o;    o += up(kGdnBufs * DK * 4, 16);       // u_0 per prepared item
         rt_off = o;   o += up(kGdnBufs * DV * 4, 16);       // record term per prepared item
         fc_off = o;   o += up(kGdnBufs * kFcStride * 4, 16); // fold constants per prepared item
@@ -113,6 +115,8 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
     auto item_of = [&](int k) { return (int)blockIdx.x + k * grid; };   // item = b * H + h
     auto meta_bad = [&](int hd, int ln) { return hd < 0 || hd >= L || ln < 0 || ln > L; };
     auto rec = [&](int r) { return smraw + lay.rec_off + r * lay.rec_bytes; };
+    // (cache slot, head) of item k: where its checkpoint and records live
+    auto cb_of = [&](int k) { return (size_t)s_meta[k * 3 + 2] * H + (size_t)(item_of(k) % H); };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -135,19 +139,28 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
     // sequence, in every CTA, has read them by then).
     for (int k = tid; k < n_my; k += blockDim.x) {
         const int it = item_of(k), b = it / H;
-        const int hd = __ldcg(a.ring_head + b), ln = __ldcg(a.ring_len + b);
-        s_meta[k * 2 + 0] = hd;
-        s_meta[k * 2 + 1] = ln;
+        const int sb = a.slots ? __ldg(a.slots + b) : b;     // the sequence's cache slot
+        if (sb < 0 || sb >= a.cap) {                         // skipped by every warp role
+            s_meta[k * 3 + 0] = -1;
+            s_meta[k * 3 + 1] = 0;
+            s_meta[k * 3 + 2] = 0;
+            if (it % H == 0) flag_error(a.err, RSSM_DEVERR_SLOT);
+            continue;
+        }
+        const int hd = __ldcg(a.ring_head + sb), ln = __ldcg(a.ring_len + sb);
+        s_meta[k * 3 + 0] = hd;
+        s_meta[k * 3 + 1] = ln;
+        s_meta[k * 3 + 2] = sb;
         if (meta_bad(hd, ln) && it % H == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
         __threadfence();
-        if (atomicAdd(a.arrive + b, 1) == H - 1) {
+        if (atomicAdd(a.arrive + sb, 1) == H - 1) {
             __threadfence();
             if (!meta_bad(hd, ln)) {
                 const bool fold = ln + 1 >= L;
-                a.ring_head[b] = fold ? (hd + ln + 1) % L : hd;
-                a.ring_len[b] = fold ? 0 : ln + 1;
+                a.ring_head[sb] = fold ? (hd + ln + 1) % L : hd;
+                a.ring_len[sb] = fold ? 0 : ln + 1;
             }
-            a.arrive[b] = 0;
+            a.arrive[sb] = 0;
         }
     }
     __syncthreads();                                     // the only CTA-wide barrier
@@ -160,13 +173,13 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
         bool ok = true;
         int issued = 0;
         for (int k = 0; k < n_my && ok; ++k) {
-            const size_t bh = (size_t)item_of(k);
+            const size_t cbh = cb_of(k);                     // cache
             for (int uu = 0; uu < NU; ++uu) {
                 const int t = issued, s = t % S;
                 if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort);
                 if (!ok) break;
                 mbar_arrive_expect_tx(full + s, lay.stage_bytes);
-                bulk_g2s(stages + s * lay.stage_bytes, a.ckpt + (bh * DV + uu * kGdnRows) * DK, lay.stage_bytes,
+                bulk_g2s(stages + s * lay.stage_bytes, a.ckpt + (cbh * DV + uu * kGdnRows) * DK, lay.stage_bytes,
                          full + s, pol);
                 issued = t + 1;
             }
@@ -189,8 +202,8 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
             if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            const size_t bh = (size_t)item_of(k);
-            const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+            const size_t bh = (size_t)item_of(k), cbh = cb_of(k);    // inputs, cache
+            const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
             const bool good = !meta_bad(hd, ln);
             if (good) {
                 // list position j < ln is ring slot (hd + j) mod L, j = ln the token
@@ -201,21 +214,21 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
                 __syncwarp();
                 if (lane == 0) {
                     unsigned char *d = rb + lay.rk_off;
-                    if (run1) bulk_g2s(d, a.rec_k + (bh * L + hd) * DK, run1 * DK * 2, rfull + r);
-                    if (run2) bulk_g2s(d + run1 * DK * 2, a.rec_k + bh * L * DK, run2 * DK * 2, rfull + r);
+                    if (run1) bulk_g2s(d, a.rec_k + (cbh * L + hd) * DK, run1 * DK * 2, rfull + r);
+                    if (run2) bulk_g2s(d + run1 * DK * 2, a.rec_k + cbh * L * DK, run2 * DK * 2, rfull + r);
                     bulk_g2s(d + ln * DK * 2, a.k + bh * DK, DK * 2, rfull + r);
                 } else if (lane == 1) {
                     unsigned char *d = rb + lay.rv_off;
-                    if (run1) bulk_g2s(d, a.rec_v + (bh * L + hd) * DV, run1 * DV * 2, rfull + r);
-                    if (run2) bulk_g2s(d + run1 * DV * 2, a.rec_v + bh * L * DV, run2 * DV * 2, rfull + r);
+                    if (run1) bulk_g2s(d, a.rec_v + (cbh * L + hd) * DV, run1 * DV * 2, rfull + r);
+                    if (run2) bulk_g2s(d + run1 * DV * 2, a.rec_v + cbh * L * DV, run2 * DV * 2, rfull + r);
                     bulk_g2s(d + ln * DV * 2, a.v + bh * DV, DV * 2, rfull + r);
                 } else if (lane == 2) {
                     bulk_g2s(rb + lay.rq_off, a.q + bh * DK, DK * 2, rfull + r);
                 }
                 for (int j = lane; j <= ln; j += 32) {
                     const int slot = hd + j < L ? hd + j : hd + j - L;
-                    cp_async4(rb + lay.ral_off + j * 4, j < ln ? a.rec_alpha + bh * L + slot : a.alpha + bh);
-                    cp_async4(rb + lay.rbe_off + j * 4, j < ln ? a.rec_beta + bh * L + slot : a.beta + bh);
+                    cp_async4(rb + lay.ral_off + j * 4, j < ln ? a.rec_alpha + cbh * L + slot : a.alpha + bh);
+                    cp_async4(rb + lay.rbe_off + j * 4, j < ln ? a.rec_beta + cbh * L + slot : a.beta + bh);
                 }
             }
             cp_async_arrive_noinc(rfull + r);
@@ -246,8 +259,8 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
                 live = false;
                 *s_abort = 1;
             }
-            const size_t bh = (size_t)item_of(kk);
-            const int hd = s_meta[kk * 2 + 0], ln = s_meta[kk * 2 + 1];
+            const size_t cbh = cb_of(kk);                    // the preparation writes the cache only
+            const int hd = s_meta[kk * 3 + 0], ln = s_meta[kk * 3 + 1];
             const bool work = live && !meta_bad(hd, ln);
             const unsigned char *rb = rec(r);
             const uint16_t *r_k = reinterpret_cast<const uint16_t *>(rb + lay.rk_off);
@@ -259,16 +272,16 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
                 // a non-flush step appends the token to the ring, slot (hd + ln) mod L
                 const int slot = hd + ln < L ? hd + ln : hd + ln - L;
                 if (lane < CK) {
-                    *reinterpret_cast<uint4 *>(a.rec_k + (bh * L + slot) * DK + lane * 8) =
+                    *reinterpret_cast<uint4 *>(a.rec_k + (cbh * L + slot) * DK + lane * 8) =
                         *reinterpret_cast<const uint4 *>(r_k + ln * DK + lane * 8);
                 } else if (lane < CK + CV) {
                     const int c = lane - CK;
-                    *reinterpret_cast<uint4 *>(a.rec_v + (bh * L + slot) * DV + c * 8) =
+                    *reinterpret_cast<uint4 *>(a.rec_v + (cbh * L + slot) * DV + c * 8) =
                         *reinterpret_cast<const uint4 *>(r_v + ln * DV + c * 8);
                 }
                 if (lane == 0) {
-                    a.rec_alpha[bh * L + slot] = r_al[ln];
-                    a.rec_beta[bh * L + slot] = r_be[ln];
+                    a.rec_alpha[cbh * L + slot] = r_al[ln];
+                    a.rec_beta[cbh * L + slot] = r_be[ln];
                 }
             }
             if (work) {
@@ -375,8 +388,8 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
             live = false;
             *s_abort = 1;
         }
-        const size_t bh = (size_t)item_of(k);
-        const int hd = s_meta[k * 2 + 0], ln = s_meta[k * 2 + 1];
+        const size_t bh = (size_t)item_of(k), cbh = cb_of(k);        // output, cache
+        const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
         const bool work = live && !meta_bad(hd, ln);
         const bool fold = work && (ln + 1 >= L);
         const int nrec = ln + 1;
@@ -494,7 +507,7 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
                     }
                 }
                 const unsigned long long tt = f2pack(fc[kFcT], fc[kFcT]);
-                float4 *ck4 = reinterpret_cast<float4 *>(a.ckpt + (bh * DV + uu * kGdnRows) * DK);
+                float4 *ck4 = reinterpret_cast<float4 *>(a.ckpt + (cbh * DV + uu * kGdnRows) * DK);
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
                     float4 o;

@@ -57,7 +57,7 @@ class GDNDims(ctypes.Structure):
 class GDNCacheC(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("ckpt", "rec_k", "rec_v", "rec_alpha", "rec_beta", "ring_head", "ring_len",
-                 "arrive", "err")]
+                 "arrive", "err", "slots")] + [("capacity", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -270,57 +270,64 @@ class GDNCache:
     ring_len: torch.Tensor
     arrive: torch.Tensor
     err: torch.Tensor
+    slots: torch.Tensor | None = None      # [batch] int32 cache slot of each batch row (None: row b -> slot b)
+    capacity: int = 0                      # sequences the cache holds (0: batch)
 
-    def c_struct(self) -> GDNCacheC:
-        return GDNCacheC(*(_ptr(getattr(self, f)) for f, _ in GDNCacheC._fields_))
+    def c_struct(self, slots=None) -> GDNCacheC:
+        """The C struct; ``slots`` (int32 [batch] on the device) overrides the cache's map."""
+        sl = self.slots if slots is None else slots
+        vals = [_ptr(getattr(self, f)) for f, _ in GDNCacheC._fields_[:-2]]
+        return GDNCacheC(*vals, _ptr(sl), int(self.capacity))
 
 
 def gdn_dims(batch, nheads, dk, dv, L=16) -> GDNDims:
     return GDNDims(batch, nheads, dk, dv, L)
 
 
-def gdn_cache(dims: GDNDims, ckpt=None, device="cuda") -> GDNCache:
-    b, H, dk, dv, L = dims.batch, dims.nheads, dims.dk, dims.dv, dims.L
+def gdn_cache(dims: GDNDims, ckpt=None, device="cuda", capacity: int = 0) -> GDNCache:
+    """Allocate an empty-ring cache for ``capacity`` sequences (0: dims.batch)."""
+    H, dk, dv, L = dims.nheads, dims.dk, dims.dv, dims.L
+    b = capacity if capacity > 0 else dims.batch
     z = lambda *s, dtype=torch.float32: torch.zeros(*s, dtype=dtype, device=device)  # noqa: E731
     if ckpt is None:
         ckpt = z(b, H, dv, dk)
     return GDNCache(dims=dims, ckpt=ckpt, rec_k=z(b, H, L, dk, dtype=torch.bfloat16),
                     rec_v=z(b, H, L, dv, dtype=torch.bfloat16), rec_alpha=z(b, H, L), rec_beta=z(b, H, L),
                     ring_head=z(b, dtype=torch.int32), ring_len=z(b, dtype=torch.int32),
-                    arrive=z(b, dtype=torch.int32), err=z(1, dtype=torch.int32))
+                    arrive=z(b, dtype=torch.int32), err=z(1, dtype=torch.int32), capacity=int(capacity))
 
 
-def gdn_decode(cache: GDNCache, q, k, v, alpha, beta, o=None, stream=None) -> torch.Tensor:
+def gdn_decode(cache: GDNCache, q, k, v, alpha, beta, o=None, stream=None, slots=None) -> torch.Tensor:
     d = cache.dims
     if o is None:
         o = torch.empty(d.batch, d.nheads, d.dv, dtype=torch.float32, device=q.device)
-    cs = cache.c_struct()
+    cs = cache.c_struct(slots)
     _check(_lib.replayssm_gdn_decode(ctypes.byref(d), ctypes.byref(cs), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                                      _ptr(beta), _ptr(o), _stream(stream)))
     return o
 
 
-def gdn_flush(cache: GDNCache, mask=None, stream=None) -> None:
-    cs = cache.c_struct()
+def gdn_flush(cache: GDNCache, mask=None, stream=None, slots=None) -> None:
+    cs = cache.c_struct(slots)
     _check(_lib.replayssm_gdn_flush(ctypes.byref(cache.dims), ctypes.byref(cs), _ptr(mask), _stream(stream)))
 
 
-def gdn_verify(cache: GDNCache, q, k, v, alpha, beta, o=None, stream=None) -> torch.Tensor:
+def gdn_verify(cache: GDNCache, q, k, v, alpha, beta, o=None, stream=None, slots=None) -> torch.Tensor:
     """Score T drafts per sequence (q, k [b, T, H, dk], v [b, T, H, dv], alpha, beta
     [b, T, H]); returns o [b, T, H, dv].  Appends the drafts' records."""
     d = cache.dims
     T = alpha.shape[1]
     if o is None:
         o = torch.empty(d.batch, T, d.nheads, d.dv, dtype=torch.float32, device=q.device)
-    cs = cache.c_struct()
+    cs = cache.c_struct(slots)
     _check(_lib.replayssm_gdn_verify(ctypes.byref(d), ctypes.byref(cs), T, _ptr(q), _ptr(k), _ptr(v),
                                      _ptr(alpha), _ptr(beta), _ptr(o), _stream(stream)))
     return o
 
 
-def gdn_rollback(cache: GDNCache, T: int, accepted, stream=None) -> None:
+def gdn_rollback(cache: GDNCache, T: int, accepted, stream=None, slots=None) -> None:
     """Keep accepted[b] of the T drafts of the last verify (int32 device tensor)."""
-    cs = cache.c_struct()
+    cs = cache.c_struct(slots)
     _check(_lib.replayssm_gdn_rollback(ctypes.byref(cache.dims), ctypes.byref(cs), T, _ptr(accepted),
                                        _stream(stream)))
 

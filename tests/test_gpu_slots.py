@@ -170,3 +170,84 @@ def test_duplicate_free_map_serves_a_changing_batch():
             if a is not None:
                 assert torch.equal(a[s:s + 1], getattr(own[s], f)), f"slot {s} {f}"
     assert int(big.err.item()) == 0
+
+
+# ------------------------------------------------------------------ Gated DeltaNet
+
+GDN_FIELDS = ("ckpt", "rec_k", "rec_v", "rec_alpha", "rec_beta", "ring_head", "ring_len")
+
+
+def _gdn_pair(shape, capacity, seed):
+    from ssm_decode_state_gb300 import replayssm as rs
+    big_shape = gen.GDNShape(capacity, shape.nheads, shape.dk, shape.dv, shape.L)
+    S0 = to_dev(gen.gdn_random_state(big_shape, seed))
+    dims = rs.gdn_dims(shape.batch, shape.nheads, shape.dk, shape.dv, shape.L)
+    big = rs.gdn_cache(dims, ckpt=S0.clone(), capacity=capacity)
+    rng = np.random.default_rng(seed)
+    slots = rng.choice(capacity, size=shape.batch, replace=False).astype(np.int32)
+    small = rs.gdn_cache(dims, ckpt=S0[torch.from_numpy(slots).long()].clone())
+    big.slots = torch.from_numpy(slots).cuda()
+    return rs, big, small, slots
+
+
+def _gdn_check(big, small, slots, before=None):
+    idx = torch.from_numpy(slots).long().cuda()
+    for f in GDN_FIELDS:
+        assert torch.equal(getattr(big, f)[idx], getattr(small, f)), f
+    if before is not None:
+        for f, b0 in before.items():
+            mask = torch.ones(getattr(big, f).shape[0], dtype=torch.bool, device="cuda")
+            mask[idx] = False
+            assert torch.equal(getattr(big, f)[mask], b0[mask]), f"unmapped slots of {f} changed"
+    assert int(big.err.item()) == 0 and int(small.err.item()) == 0
+
+
+def _gdn_dev(st):
+    return tuple(to_dev(a, torch.bfloat16) for a in (st.q, st.k, st.v)) + (to_dev(st.alpha), to_dev(st.beta))
+
+
+@pytest.mark.parametrize("shape,capacity", [
+    (gen.GDNShape(batch=24, nheads=32, dk=128, dv=128, L=4), 40),     # persistent decode
+    (gen.GDNShape(batch=3, nheads=4, dk=64, dv=32, L=4), 7),          # per-tile decode
+], ids=["persistent", "per_tile"])
+def test_gdn_decode_through_slot_map(shape, capacity):
+    rs, big, small, slots = _gdn_pair(shape, capacity, 400 + capacity)
+    before = {f: getattr(big, f).clone() for f in GDN_FIELDS}
+    for t in range(2 * shape.L + 1):
+        args = _gdn_dev(gen.gdn_step_inputs(shape, 400, t))
+        assert torch.equal(rs.gdn_decode(big, *args), rs.gdn_decode(small, *args)), f"o differs at step {t}"
+    _gdn_check(big, small, slots, before)
+
+
+def test_gdn_verify_rollback_flush_through_slot_map():
+    shape = gen.GDNShape(batch=4, nheads=4, dk=64, dv=64, L=8)
+    rs, big, small, slots = _gdn_pair(shape, 9, 41)
+    before = {f: getattr(big, f).clone() for f in GDN_FIELDS}
+    T = 3
+    for t in range(8):
+        args = _gdn_dev(gen.gdn_draft_inputs(shape, 41, t, T))
+        assert torch.equal(rs.gdn_verify(big, *args), rs.gdn_verify(small, *args)), f"verify o differs at {t}"
+        acc = torch.from_numpy(gen.accepted_counts(shape.batch, T, 41, t)).cuda()
+        rs.gdn_rollback(big, T, acc)
+        rs.gdn_rollback(small, T, acc)
+        if t % 3 == 2:
+            mask = torch.tensor([1, 0, 1, 1], dtype=torch.uint8, device="cuda")
+            rs.gdn_flush(big, mask)
+            rs.gdn_flush(small, mask)
+        _gdn_check(big, small, slots)
+    _gdn_check(big, small, slots, before)
+
+
+def test_gdn_slot_out_of_range_is_flagged_and_skipped():
+    shape = gen.GDNShape(batch=24, nheads=32, dk=128, dv=128, L=4)
+    rs, big, small, slots = _gdn_pair(shape, 30, 43)
+    bad = slots.copy()
+    bad[3] = -1
+    s3 = int(slots[3])
+    ck3 = big.ckpt[s3].clone()
+    rs.gdn_decode(big, *_gdn_dev(gen.gdn_step_inputs(shape, 43, 0)), slots=torch.from_numpy(bad).cuda())
+    torch.cuda.synchronize()
+    assert int(big.err.item()) & rs.DEVERR_SLOT
+    assert big.ring_len[s3].item() == 0 and torch.equal(big.ckpt[s3], ck3)
+    assert big.ring_len[int(slots[0])].item() == 1
+    assert not big.arrive.any().item()

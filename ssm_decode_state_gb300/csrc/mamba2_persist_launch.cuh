@@ -20,18 +20,21 @@ rssm_status launch_decode_persistent_ck(const rssm_mamba2_dims *d, const M2Args 
     if (!d->io_bf16 || d->dstate != 128 || d->headdim != 64 || d->nheads > 4096) return RSSM_ERR_UNSUPPORTED;
     const int hpg = d->nheads / d->ngroups;
     const int sms = sm_count();
-    // heads per work item: the per-item work (records, weights, record term)
-    // is what limits this kernel, so take the largest item that still leaves
-    // at least 12 items per SM (balance across SMs); small batches get smaller
-    // items so that every SM has work
-    int hpi = 0;
+    // heads per work item: the largest item that still leaves about one item per SM
+    // (items >= 4/5 of the SMs).  An item's preparation (records, weights, record
+    // term) is a chain of dependent latencies, so fewer, larger items win as long as
+    // the SMs stay busy; measured at batches 1-192 (us per step with 1 / 2 / 4 / 8
+    // heads per item): batch 2 8.97 / 7.85 / 8.66 / 11.18, batch 8 18.19 / 13.78 /
+    // 11.61 / 11.37, batch 64 112.4 / 65.6 / 49.1 / 48.7, batch 192 329.8 / 181.8 /
+    // 140.4 / 134.0
+    int hpi = 1;
     for (int c : {8, 4, 2, 1}) {
         if (hpg % c) continue;
-        if ((long long)d->batch * d->nheads / c >= 12LL * sms || c == 1) { hpi = c; break; }
+        if ((long long)d->batch * d->nheads / c * 5 >= 4LL * sms) { hpi = c; break; }
     }
     const long long items = (long long)d->batch * d->nheads / hpi;
     // every batch: at batches 1-2 (fewer items than SMs) the persistent kernel still
-    // beats the per-tile kernel (7.4 vs 15.0 us at batch 1, 9.0 vs 12.1 at batch 2)
+    // beats the per-tile kernel (7.3 vs 15.0 us at batch 1, 7.9 vs 12.1 at batch 2)
     if (items < 1 || items > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;
     const int grid = (int)(items < sms ? items : sms);
     const int max_my = (int)((items + grid - 1) / grid);   // ring pointers of these are kept in smem

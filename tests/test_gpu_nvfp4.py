@@ -106,10 +106,10 @@ def test_exact_decode_per_tile():
     _exact_decode(gen.Mamba2Shape(batch=3, nheads=8, headdim=32, dstate=64, ngroups=2, L=8), 32)
 
 
-@pytest.mark.parametrize("batch", [1, 5, 32, 64])
+@pytest.mark.parametrize("batch", [1, 2, 5])
 def test_exact_decode_small_batches(batch):
-    """Smaller batches run the persistent kernel with 1 (batches 1, 5), 2 (32)
-    or 4 (64) heads per work item."""
+    """Smaller batches run the persistent kernel with 1 (batch 1), 2 (batch 2)
+    or 4 (batch 5) heads per work item."""
     _exact_decode(gen.Mamba2Shape(batch=batch, nheads=128, headdim=64, dstate=128, ngroups=8, L=16), 40 + batch)
 
 

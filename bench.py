@@ -160,6 +160,24 @@ def _timed(stream, fn, steps):
     return e0.elapsed_time(e1)
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Each value's maximum over the ranks (the slowest replica's times), after a
+    barrier; one process (dist None): the values themselves."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    dist.barrier()
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_value(world: int, units_per_rank: float, ms: float) -> float:
+    """Whole-job throughput of `world` independent replicas: every rank's units
+    over the slowest rank's time (ms)."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def run_native(args, rank, world, local_rank):
     import torch
     import __graft_entry__
@@ -251,7 +269,7 @@ def run_native(args, rank, world, local_rank):
         lens = np.where(lens + 1 >= L, 0, lens + 1)
     stag_ms = _timed(stream, lambda t: rs.decode(cache, *pool[t % POOL], y=y), Ks)
     assert int(cache.err.item()) == 0
-    staggered = {"us_per_step": round(stag_ms * 1e3 / Ks, 1), "value": round(world * B * Ks / (stag_ms / 1e3), 1),
+    staggered = {"us_per_step": round(stag_ms * 1e3 / Ks, 1), "value": round(replica_value(world, B * Ks, stag_ms), 1),
                  "alg_GBps": round(stag_bytes / (stag_ms / 1e3) / 1e9, 1), "steps": Ks,
                  "ring_len_at_start": "b mod L"}
     cache.ring_len.zero_()                      # the later measurements start aligned again
@@ -322,13 +340,10 @@ def run_native(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
 
-    times = torch.tensor([ms, e2e_ms, conv_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms, e2e_ms, conv_ms = times.tolist()
+    ms, e2e_ms, conv_ms = max_over_ranks([ms, e2e_ms, conv_ms], dist, dev)
     if rank != 0:
         return
-    value = world * B * K / (ms / 1e3)
+    value = replica_value(world, B * K, ms)
     per_launch_s = ms / 1e3 / K
     achieved = alg_bytes / K / per_launch_s / 1e9
     peak, peak_src = peaks()
@@ -346,7 +361,7 @@ def run_native(args, rank, world, local_rank):
                      "kernel": "m2_decode_persistent",
                      "alg_bytes_per_launch": int(alg_bytes / K),
                      "peak_source": f"{peak_src} hbm_gbs (copy), of measured"},
-        "e2e": {"value": round(world * B * Ke / (e2e_ms / 1e3), 1), "unit": UNIT,
+        "e2e": {"value": round(replica_value(world, B * Ke, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                 "copies": "second stream, double-buffered, overlapping the decodes"},
         "step_us": {k: round(statistics.median(v), 1) for k, v in split.items() if v},
@@ -355,7 +370,7 @@ def run_native(args, rank, world, local_rank):
         "clocks": clocks,
     }
     if conv_ms:
-        line["conventional"] = {"value": round(world * B * K / (conv_ms / 1e3), 1),
+        line["conventional"] = {"value": round(replica_value(world, B * K, conv_ms), 1),
                                 "ms_per_step": round(conv_ms / K, 5),
                                 "alg_bytes_per_launch": bm.mamba2_conventional(u) * B,
                                 "replay_speedup": round(conv_ms / ms, 3)}

@@ -1,0 +1,68 @@
+"""The N > 1 path of the bench on CPU: two ranks over gloo (the path has no
+exchange step, so N GPUs run N independent replicas; only the timing and the
+reporting meet across ranks).
+
+* The timings every rank reports are each value's maximum over the ranks (the
+  slowest replica), and the whole-job value is all ranks' units over that time.
+* Under N ranks the reference arm runs on rank 0 alone; the other ranks exit
+  without work or output.
+"""
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+from types import SimpleNamespace
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist            # noqa: E402
+import torch.multiprocessing as mp          # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out_dir):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    # rank r measured (r + 1) * 10 ms, (r + 1) * 20 ms, 7 ms
+    got = bench.max_over_ranks([(rank + 1) * 10.0, (rank + 1) * 20.0, 7.0], dist, "cpu")
+    value = bench.replica_value(world, 256 * 100, got[0])
+    args = SimpleNamespace(cpu_seqs=1, cpu_steps=1, steps=1, warmup=0)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(args, rank, world)
+    dist.barrier()
+    dist.destroy_process_group()
+    with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+        json.dump({"max": got, "value": value, "stdout": buf.getvalue()}, f)
+
+
+def test_two_ranks_over_gloo(tmp_path):
+    world = 2
+    mp.spawn(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    res = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(world)]
+    for r in res:
+        assert r["max"] == [20.0, 40.0, 7.0]                 # the slowest rank's times on every rank
+        assert r["value"] == pytest.approx(2 * 256 * 100 / 0.020)
+    assert res[1]["stdout"] == ""                            # rank 1: no work, no line
+    line = json.loads(res[0]["stdout"].strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_single_process_passes_values_through():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks([3.0, 1.5]) == [3.0, 1.5]
+    assert bench.replica_value(1, 1000, 500.0) == pytest.approx(2000.0)

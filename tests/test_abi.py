@@ -146,3 +146,23 @@ def test_gdn_checks(rs):
     assert lib.replayssm_gdn_verify(ctypes.byref(d4), ctypes.byref(c2), 2, FAKE, FAKE, FAKE, FAKE,
                                     FAKE, FAKE, None) == 2
     assert lib.replayssm_gdn_rollback(ctypes.byref(d4), ctypes.byref(c), 2, None, None) == 1
+
+
+def test_capacity_checks(rs):
+    """Cache capacity: negative, or below the batch without a slot map, is a
+    shape error for both caches, before anything is launched; with a slot map any
+    positive capacity passes the host checks."""
+    lib = rs._lib
+    d = _m2(rs, batch=4)
+    assert _decode(rs, d, _cache(rs, capacity=-1)) == 3
+    assert _decode(rs, d, _cache(rs, slots=None, capacity=3)) == 3
+    assert lib.replayssm_rollback(ctypes.byref(d), ctypes.byref(_cache(rs, slots=None, capacity=2)), 1,
+                                  FAKE, None) == 3
+    assert lib.replayssm_flush(ctypes.byref(d), ctypes.byref(_cache(rs, capacity=-5)), None, None) == 3
+    g = rs.GDNDims(4, 4, 64, 64, 16)
+    base = {f: FAKE for f, _ in rs.GDNCacheC._fields_}
+    for kw in ({"capacity": -1}, {"slots": None, "capacity": 3}):
+        c = rs.GDNCacheC(**{**base, **kw})
+        assert lib.replayssm_gdn_decode(ctypes.byref(g), ctypes.byref(c), FAKE, FAKE, FAKE, FAKE,
+                                        FAKE, FAKE, None) == 3
+        assert lib.replayssm_gdn_rollback(ctypes.byref(g), ctypes.byref(c), 1, FAKE, None) == 3

@@ -213,7 +213,8 @@ def _f16sr_mutants():
         return ((r >> 8) | (r << 8)) & 0xFFFF
 
     def round_to_nearest(v, r):
-        return np.asarray(v, np.float32).astype(np.float16)
+        with np.errstate(over="ignore"):                   # values above 65504 become inf here
+            return np.asarray(v, np.float32).astype(np.float16)
 
     def round_up_on_equal(v, r):
         v = np.asarray(v, np.float32)

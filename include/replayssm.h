@@ -142,8 +142,10 @@ typedef struct {
  *   len + 1 >= L: flush fused into this step (AT Pulse §Technical analysis:
  *                 every L steps the buffer is folded into the checkpoint):
  *                 h_c <- exp(A S) h_c + sum_j exp(A (S - S_j)) dt_j x_j B_j^T
- *                 over the buffered records and the current token, the read
- *                 copy is re-quantised, ring_head <- (ring_head + len + 1) mod L,
+ *                 over the buffered records and the current token (computed in
+ *                 float32; an FP16 checkpoint is then rounded stochastically with
+ *                 cache->sr_seed), the read copy is re-quantised from the stored
+ *                 checkpoint, ring_head <- (ring_head + len + 1) mod L,
  *                 ring_len <- 0; the current token is not stored.
  * y is the replay output above in every case.  Non-flush steps read the FP8
  * copy when dims->read_copy = 1 and the NVFP4 copy when it is 2.
@@ -182,8 +184,9 @@ rssm_status replayssm_decode_noalloc(const rssm_mamba2_dims *dims, const rssm_ma
  * Standalone flush (WittyWires §What happened: the checkpoint is updated when
  * the buffer fills): for every sequence with mask[b] != 0 (mask = NULL: all),
  * fold its ring_len records into the checkpoint with the same arithmetic as
- * the fused flush, re-quantise the read copy, ring_head <- (ring_head +
- * ring_len) mod L, ring_len <- 0.  mask is a device array of batch bytes.
+ * the fused flush (FP16 checkpoints rounded stochastically with cache->sr_seed),
+ * re-quantise the read copy, ring_head <- (ring_head + ring_len) mod L,
+ * ring_len <- 0.  mask is a device array of batch bytes.
  */
 rssm_status replayssm_flush(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
                             const uint8_t *mask, void *stream);
@@ -197,7 +200,8 @@ rssm_status replayssm_flush(const rssm_mamba2_dims *dims, const rssm_mamba2_cach
  * replayssm_flush).  Draft i (1-based) is scored against the checkpoint, the
  * buffered records and drafts 1..i; the T drafts are appended at slots
  * (ring_head + ring_len + i - 1) mod L and ring_len += T.  Drafts are never
- * folded by a verify.  1 <= T <= min(L, 8).  Reads use the FP32 checkpoint.
+ * folded by a verify.  1 <= T <= min(L, 8).  Reads use the checkpoint itself
+ * (float32 or FP16), not the read copy.
  */
 rssm_status replayssm_verify(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
                              int32_t T, const float *dt, const void *x, const void *B,

@@ -172,6 +172,22 @@ def max_over_ranks(values, dist=None, device="cpu"):
     return t.tolist()
 
 
+def memory_report(H: int, P: int, N: int, G: int, L: int, layers: int = 24,
+                  budget_bytes: int = 100 * 2 ** 30) -> dict:
+    """Cache memory per sequence and layer for the replay variants against the
+    conventional state, and the sequences a budget holds for `layers` SSM layers."""
+    kw = dict(nheads=H, headdim=P, dstate=N, ngroups=G, L=L)
+    out = {"layers": layers, "budget_GiB": budget_bytes / 2 ** 30}
+    for name, extra in (("fp32", {}), ("fp32_fp8_copy", {"read_copy": 1}),
+                        ("fp16_nvfp4_copy", {"read_copy": 2, "ckpt_f16": True})):
+        c = bm.mamba2_cache_bytes(**kw, **extra)
+        out[name] = {"bytes_per_seq_layer": c["total"], "ring_bytes": c["ring"],
+                     "sequences": bm.sequences_that_fit(budget_bytes, layers, **kw, **extra)["replay"]}
+    out["conventional"] = {"bytes_per_seq_layer": bm.mamba2_cache_bytes(**kw)["conventional"],
+                           "sequences": bm.sequences_that_fit(budget_bytes, layers, **kw)["conventional"]}
+    return out
+
+
 def replica_value(world: int, units_per_rank: float, ms: float) -> float:
     """Whole-job throughput of `world` independent replicas: every rank's units
     over the slowest rank's time (ms)."""
@@ -347,6 +363,7 @@ def run_native(args, rank, world, local_rank):
     per_launch_s = ms / 1e3 / K
     achieved = alg_bytes / K / per_launch_s / 1e9
     peak, peak_src = peaks()
+    memory = memory_report(H, P, N, G, L)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
@@ -368,6 +385,7 @@ def run_native(args, rank, world, local_rank):
         "staggered": staggered,
         "gpu_launches": K,
         "clocks": clocks,
+        "memory": memory,
     }
     if conv_ms:
         line["conventional"] = {"value": round(replica_value(world, B * K, conv_ms), 1),

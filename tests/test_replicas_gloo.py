@@ -66,3 +66,16 @@ def test_single_process_passes_values_through():
     import bench
     assert bench.max_over_ranks([3.0, 1.5]) == [3.0, 1.5]
     assert bench.replica_value(1, 1000, 500.0) == pytest.approx(2000.0)
+
+
+def test_memory_report_of_the_bench_line():
+    """The bench line's memory report: per-sequence cache bytes of each replay
+    variant against the conventional state, and sequences in 100 GiB for 24 layers."""
+    sys.path.insert(0, ROOT)
+    import bench
+    m = bench.memory_report(128, 64, 128, 8, 16)
+    json.dumps(m)                                            # serialisable
+    assert m["fp32"]["bytes_per_seq_layer"] == 4194304 + 16 * 20992 + 12
+    assert m["conventional"] == {"bytes_per_seq_layer": 4194304, "sequences": 1066}
+    assert m["fp32"]["sequences"] == 987 and m["fp16_nvfp4_copy"]["sequences"] == 1464
+    assert m["fp32_fp8_copy"]["bytes_per_seq_layer"] == m["fp32"]["bytes_per_seq_layer"] + 1081344

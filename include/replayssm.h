@@ -170,7 +170,12 @@ rssm_status replayssm_decode(const rssm_mamba2_dims *dims, const rssm_mamba2_cac
  *    before anything is enqueued.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *  - The first call on a device looks up the array's device address with that
- *    device current; make that first call before any stream capture.
+ *    device current; make that first call before any stream capture.  The
+ *    address is kept until the process exits, so do not use this entry point
+ *    after a cudaDeviceReset (or any other teardown of the device's primary
+ *    context) in the same process.
+ *  - Every host-side check of replayssm_decode runs before anything is
+ *    enqueued, so a rejected call leaves the shared counters untouched.
  *  - Each call clears the counters it uses (an asynchronous memset on
  *    `stream`) and then enqueues the decode.
  *  - All calls share the one array: calls that can overlap on the GPU (other

@@ -27,7 +27,9 @@ std::mutex g_setup_mutex;
 int32_t *g_scratch_ptr[64] = {nullptr};
 
 // Device address of the counters on the current device, looked up once per
-// device (with that device current).
+// device (with that device current) and kept for the life of the process: a
+// cudaDeviceReset reloads the library's device code elsewhere, so the cached
+// address would then be stale (the header forbids use across a reset).
 rssm_status scratch_for_current_device(int32_t **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RSSM_ERR_CUDA;
@@ -49,11 +51,15 @@ rssm_status scratch_for_current_device(int32_t **out) {
 extern "C" rssm_status replayssm_decode_noalloc(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
                                                 const float *dt, const void *x, const void *B, const void *C,
                                                 float *y, void *stream) {
-    if (!dims || !cache) return RSSM_ERR_NULL;
+    // every host-side check first, so that a call rejected here enqueues nothing
+    // (in particular, clears no counters another call may still be using)
+    rssm::TileGeom geom;
+    rssm_status v = rssm::check_decode_call(dims, cache, dt, x, B, C, y, false, &geom);
+    if (v != RSSM_OK) return v;
     // the counters are indexed by cache slot: the cache's capacity (batch without a
     // slot map) must fit the fixed array
     const int cap = cache->capacity > 0 ? cache->capacity : dims->batch;
-    if (dims->batch < 1 || cache->capacity < 0 || cap > kNoAllocMaxBatch) return RSSM_ERR_SHAPE;
+    if (cap > kNoAllocMaxBatch) return RSSM_ERR_SHAPE;
     int32_t *scratch = nullptr;
     rssm_status s = scratch_for_current_device(&scratch);
     if (s != RSSM_OK) return s;

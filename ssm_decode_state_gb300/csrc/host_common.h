@@ -75,6 +75,12 @@ inline bool choose_geom(int batch, int heads, int rows, int cols, TileGeom &g, i
     return g.split > 0;
 }
 
+// All host-side checks of a replay decode call (dims, cache, token buffers,
+// launch geometry); need_arrive = false accepts a cache without arrival counters.
+rssm_status check_decode_call(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c, const float *dt,
+                              const void *x, const void *B, const void *C, const float *y, bool need_arrive,
+                              TileGeom *geom);
+
 // Device-side ring rollback shared by the Mamba-2 and GDN caches (launch only).
 rssm_status launch_ring_rollback(int batch, int L, int T, const int32_t *accepted, const int32_t *slots, int cap,
                                  int32_t *ring_head, int32_t *ring_len, uint32_t *err, cudaStream_t st);

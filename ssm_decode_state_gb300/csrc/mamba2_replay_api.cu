@@ -163,16 +163,34 @@ rssm_status launch_ring_rollback(int batch, int L, int T, const int32_t *accepte
 
 using namespace rssm;
 
+namespace rssm {
+
+// Every host-side check of a replay decode call.  The no-alloc decode runs it
+// with the arrival counters not yet supplied (it provides them itself, but only
+// after the call is known to be valid).
+rssm_status check_decode_call(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c, const float *dt,
+                              const void *x, const void *B, const void *C, const float *y, bool need_arrive,
+                              TileGeom *geom) {
+    rssm_status s = check_dims(d);
+    if (s != RSSM_OK) return s;
+    if (!c) return RSSM_ERR_NULL;
+    rssm_mamba2_cache probe = *c;
+    if (!need_arrive && !probe.arrive) probe.arrive = reinterpret_cast<int32_t *>(16);
+    if ((s = check_cache(d, &probe)) != RSSM_OK) return s;
+    if (!dt || !x || !B || !C || !y) return RSSM_ERR_NULL;
+    if (!aligned16(x) || !aligned16(B) || !aligned16(C)) return RSSM_ERR_ALIGN;
+    if (!choose_geom(d->batch, d->nheads, d->headdim, d->dstate, *geom)) return RSSM_ERR_UNSUPPORTED;
+    return RSSM_OK;
+}
+
+}  // namespace rssm
+
 extern "C" rssm_status replayssm_decode(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c,
                                         const float *dt, const void *x, const void *B, const void *C,
                                         float *y, void *stream) {
-    rssm_status s = check_dims(d);
-    if (s != RSSM_OK) return s;
-    if ((s = check_cache(d, c)) != RSSM_OK) return s;
-    if (!dt || !x || !B || !C || !y) return RSSM_ERR_NULL;
-    if (!aligned16(x) || !aligned16(B) || !aligned16(C)) return RSSM_ERR_ALIGN;
     TileGeom g;
-    if (!choose_geom(d->batch, d->nheads, d->headdim, d->dstate, g)) return RSSM_ERR_UNSUPPORTED;
+    rssm_status s = check_decode_call(d, c, dt, x, B, C, y, true, &g);
+    if (s != RSSM_OK) return s;
     M2Args a = make_args(d, c, g);
     a.dt = dt; a.x = x; a.Bin = B; a.Cin = C; a.y = y;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

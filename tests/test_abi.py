@@ -166,3 +166,25 @@ def test_capacity_checks(rs):
         assert lib.replayssm_gdn_decode(ctypes.byref(g), ctypes.byref(c), FAKE, FAKE, FAKE, FAKE,
                                         FAKE, FAKE, None) == 3
         assert lib.replayssm_gdn_rollback(ctypes.byref(g), ctypes.byref(c), 1, FAKE, None) == 3
+
+
+def test_noalloc_checks_before_anything(rs):
+    """replayssm_decode_noalloc runs every host-side check of replayssm_decode
+    (with cache->arrive allowed to be NULL: it supplies the counters itself) and
+    its own capacity limit before it looks up or clears its counter array, so a
+    rejected call enqueues nothing."""
+    lib = rs._lib
+
+    def na(dims, cache, dt=FAKE, x=FAKE):
+        return lib.replayssm_decode_noalloc(ctypes.byref(dims), ctypes.byref(cache), dt, x, FAKE, FAKE,
+                                            FAKE, None)
+
+    assert lib.replayssm_decode_noalloc(None, ctypes.byref(_cache(rs)), FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert na(_m2(rs), _cache(rs, arrive=None), dt=None) == 1
+    assert na(_m2(rs), _cache(rs, arrive=None, ckpt=None)) == 1
+    assert na(_m2(rs), _cache(rs, arrive=None), x=MIS) == 2
+    assert na(_m2(rs, dstate=48), _cache(rs, arrive=None)) == 3
+    # the counter array holds 4096 sequences: a small batch through a slot map into
+    # a larger cache is over the limit, and so is a batch of 4097 without a map
+    assert na(_m2(rs, batch=4), _cache(rs, arrive=None, capacity=5000)) == 3
+    assert na(_m2(rs, batch=4097), _cache(rs, arrive=None, slots=None, capacity=0)) == 3

@@ -46,18 +46,13 @@ def test_noalloc_matches_decode_two_calls(shape):
                                                 torch.cuda.current_stream().cuda_stream)
         assert code == 0, rs.status_string(code)
         torch.cuda.synchronize()
+        # the same kernel with the same arithmetic: only where the counters live differs,
+        # so outputs and checkpoints agree bit for bit (the tolerance gate is implied)
         assert_close(y_new.cpu().numpy(), y_ref.cpu().numpy(), f"noalloc y call {step}")
+        np.testing.assert_array_equal(y_new.cpu().numpy(), y_ref.cpu().numpy())
         np.testing.assert_array_equal(new.ring_len.cpu().numpy(), ref.ring_len.cpu().numpy())
         np.testing.assert_array_equal(new.ring_head.cpu().numpy(), ref.ring_head.cpu().numpy())
-        assert_close(new.ckpt.cpu().numpy(), ref.ckpt.cpu().numpy(), f"noalloc checkpoint call {step}")
+        np.testing.assert_array_equal(new.ckpt.cpu().numpy(), ref.ckpt.cpu().numpy())
         assert int(new.err.item()) == 0
     assert new.ring_len.cpu().tolist() == [0] * shape.batch     # the second call flushed
 
-
-def test_noalloc_rejects_batch_over_limit():
-    from ssm_decode_state_gb300 import replayssm as rs
-    dims = rs.mamba2_dims(4097, 8, 32, 64, 2, 16)
-    cs = rs.Mamba2CacheC()
-    code = rs._lib.replayssm_decode_noalloc(ctypes.byref(dims), ctypes.byref(cs), None, None, None,
-                                            None, None, None)
-    assert code == 3          # RSSM_ERR_SHAPE, nothing enqueued

@@ -62,11 +62,6 @@ class Mamba2Stepwise:
         self.h, y = self._update(self.h, dt, x, B, C)
         return y
 
-    def output_only(self, dt, x, B, C) -> np.ndarray:
-        """y of one token without committing the update."""
-        _, y = self._update(self.h, dt, x, B, C)
-        return y
-
     def verify(self, dt, x, B, C):
         """Score T drafts per sequence (inputs [b, T, ...]) without committing.
 

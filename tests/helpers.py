@@ -11,13 +11,14 @@ import numpy as np
 RTOL = 1e-4
 FLOOR = 1e-2
 
-# The conventional comparison path rewrites its FP32 state in place every
-# token, so its own rounding (about 2^-24 of the state per step) accumulates
-# like a random walk over the steps since the exact start state: after t
-# steps about sqrt(t) * 6e-8 of the state, i.e. sqrt(t) * 6e-6 of the floor.
-# Over up to 1024 steps that is ~2e-4; the gate for that path is 5e-4.  The
-# replay checkpoint is rounded only at flushes (every L steps), which keeps it
-# inside RTOL.
+# The conventional (in-place) comparison paths of both layer types rewrite
+# their FP32 state in place every token, so their own rounding (about 2^-24 of
+# the state per step) accumulates like a random walk over the steps since the
+# exact start state: after t steps about sqrt(t) * 6e-8 of the state, i.e.
+# sqrt(t) * 6e-6 of the floor.  Over up to 1024 steps that is ~2e-4; the gate
+# for those paths is 5e-4.  Every replay path (Mamba-2 and Gated DeltaNet
+# decode, fold, verify, rollback) rounds its checkpoint only at flushes and
+# takes RTOL.
 RTOL_INPLACE = 5e-4
 
 

@@ -7,7 +7,7 @@ import torch
 from oracle.fp8 import quantize_rows
 from oracle.gdn import GDNStepwise
 from ssm_decode_state_gb300 import inputs as gen
-from tests.helpers import RTOL_INPLACE, assert_close, rel_err, to_dev
+from tests.helpers import RTOL, RTOL_INPLACE, assert_close, rel_err, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -121,10 +121,9 @@ class GDNRun:
         oc = self.rs.gdn_conventional_decode(self.dims, self.conv, q, k, v, al, be)
         s = self.sample
         oo = self.oracle.step(st.q[s], st.k[s], st.v[s], st.alpha[s], st.beta[s])
-        # the gated delta fold applies its L rank-one updates one after the
-        # other, rounding the state once per record like the in-place path, so
-        # both GDN paths take the in-place gate
-        e = assert_close(o.cpu().numpy()[s], oo, f"gdn replay o step {t}", RTOL_INPLACE)
+        # the replay path (output, fold) takes the FP32 gate; the in-place
+        # comparison path rounds its state every token and takes its own
+        e = assert_close(o.cpu().numpy()[s], oo, f"gdn replay o step {t}", RTOL)
         self.max_err = max(self.max_err, e)
         assert_close(oc.cpu().numpy()[s], oo, f"gdn conventional o step {t}", RTOL_INPLACE)
         fold = self.len + 1 >= self.shape.L
@@ -133,7 +132,7 @@ class GDNRun:
         assert int(self.cache.err.item()) == 0
         if fold:
             e = rel_err(self.cache.ckpt.cpu().numpy()[s], self.oracle.S)
-            assert e <= RTOL_INPLACE, f"gdn checkpoint after step {t}: {e:.3e}"
+            assert e <= RTOL, f"gdn checkpoint after step {t}: {e:.3e}"
 
 
 @pytest.mark.parametrize("dk,dv,L", [(16, 16, 4), (32, 24, 16), (64, 64, 8)])
@@ -155,7 +154,7 @@ def test_gdn_flush_standalone():
     assert r.cache.ring_head.cpu().tolist() == [5, 0, 5]
     ck = r.cache.ckpt.cpu().numpy()
     for b in (0, 2):
-        assert rel_err(ck[b], r.oracle.S[b]) <= RTOL_INPLACE
+        assert rel_err(ck[b], r.oracle.S[b]) <= RTOL
 
 
 def test_gdn_b256_sampled():
@@ -309,7 +308,7 @@ class GDNPersistRun:
                                to_dev(st.alpha), to_dev(st.beta))
         s = self.sample
         oo = self.oracle.step(st.q[s], st.k[s], st.v[s], st.alpha[s], st.beta[s])
-        assert_close(o.cpu().numpy()[s], oo, f"gdn persistent o step {t}", RTOL_INPLACE)
+        assert_close(o.cpu().numpy()[s], oo, f"gdn persistent o step {t}", RTOL)
         fold = self.len + 1 >= L
         slot = (self.head + self.len) % L
         self.head = np.where(fold, (self.head + self.len + 1) % L, self.head)
@@ -330,7 +329,7 @@ class GDNPersistRun:
         for i, b in enumerate(s):
             if fold[b]:
                 e = rel_err(self.cache.ckpt[b].cpu().numpy(), self.oracle.S[i])
-                assert e <= RTOL_INPLACE, f"gdn checkpoint of seq {b} after step {t}: {e:.3e}"
+                assert e <= RTOL, f"gdn checkpoint of seq {b} after step {t}: {e:.3e}"
 
     def flush(self, mask):
         self.rs.gdn_flush(self.cache, torch.tensor(mask, dtype=torch.uint8, device="cuda"))
@@ -364,7 +363,7 @@ def test_gdn_persistent_with_standalone_flush():
     r.flush([1, 0] * 8)
     for i, b in enumerate(r.sample):
         if b % 2 == 0:
-            assert rel_err(r.cache.ckpt[b].cpu().numpy(), r.oracle.S[i]) <= RTOL_INPLACE
+            assert rel_err(r.cache.ckpt[b].cpu().numpy(), r.oracle.S[i]) <= RTOL
     for t in range(3, 14):
         r.step(t)
 

@@ -186,6 +186,22 @@ rssm_status replayssm_decode_noalloc(const rssm_mamba2_dims *dims, const rssm_ma
                                      float *y, void *stream);
 
 /*
+ * Test hook of the failure-detection path (the pages have no counterpart):
+ * replayssm_decode at a serving shape (persistent kernel, FP32 checkpoint),
+ * except that the consumer warps first wait on a barrier that nothing arrives
+ * on.  That wait gives up after ~2 s like every wait in the kernels, so the
+ * kernel takes its abort path on a healthy GPU: it sets RSSM_DEVERR_TIMEOUT in
+ * *cache->err, lets every copy it started land, and exits.  The ring pointers
+ * are committed at kernel start as usual, but outputs, records and the
+ * checkpoint are left partly written: the cache is not usable afterwards.
+ * Arguments and host-side errors are those of replayssm_decode;
+ * RSSM_ERR_UNSUPPORTED for shapes the persistent kernel does not serve.
+ */
+rssm_status replayssm_test_stalled_decode(const rssm_mamba2_dims *dims, const rssm_mamba2_cache *cache,
+                                          const float *dt, const void *x, const void *B, const void *C,
+                                          float *y, void *stream);
+
+/*
  * Standalone flush (WittyWires §What happened: the checkpoint is updated when
  * the buffer fills): for every sequence with mask[b] != 0 (mask = NULL: all),
  * fold its ring_len records into the checkpoint with the same arithmetic as

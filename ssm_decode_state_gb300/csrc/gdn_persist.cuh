@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
             const size_t cbh = cb_of(k);                     // cache
             for (int uu = 0; uu < NU; ++uu) {
                 const int t = issued, s = t % S;
-                if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort);
+                if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort) && !*s_abort;
                 if (!ok) break;
                 mbar_arrive_expect_tx(full + s, lay.stage_bytes);
                 bulk_g2s(stages + s * lay.stage_bytes, a.ckpt + (cbh * DV + uu * kGdnRows) * DK, lay.stage_bytes,
@@ -185,11 +185,16 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
             }
         }
         if (!ok) {
+            // a wait gave up, or another warp did: tell everyone
             *s_abort = 1;
             flag_error(a.err, RSSM_DEVERR_TIMEOUT);
-            for (int u = issued - S < 0 ? 0 : issued - S; u < issued; ++u)
-                mbar_wait(full + (u % S), (uint32_t)((u / S) & 1));
         }
+        // the copies in flight must land before the CTA ends.  Normally the
+        // consumers waited for every one, but after an abort they stop waiting;
+        // the stages of older units were refilled only after every consumer warp
+        // waited for them (an aborted warp's release is seen above as the abort)
+        for (int u = issued - S < 0 ? 0 : issued - S; u < issued; ++u)
+            mbar_wait(full + (u % S), (uint32_t)((u / S) & 1));
         return;
     }
 
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
         int k = 0;
         for (; k < n_my; ++k) {
             const int r = k % RB;
-            if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort);
+            if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort) && !*s_abort;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const size_t bh = (size_t)item_of(k), cbh = cb_of(k);    // inputs, cache

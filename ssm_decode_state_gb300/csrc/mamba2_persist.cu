@@ -12,6 +12,12 @@ rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &ar
     return d->ckpt_f16 ? launch_decode_persistent_f16(d, args, st) : launch_decode_persistent_ck<0>(d, args, st);
 }
 
+// The same launch with the bounded-wait test hook on (float32 checkpoints).
+rssm_status launch_decode_persistent_stalled(const rssm_mamba2_dims *d, const M2Args &args, cudaStream_t st) {
+    if (d->ckpt_f16) return RSSM_ERR_UNSUPPORTED;
+    return launch_decode_persistent_ck<0>(d, args, st, 1);
+}
+
 }  // namespace rssm
 
 #include "mamba2_verify_persist.cuh"

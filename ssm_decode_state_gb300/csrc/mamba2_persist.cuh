@@ -41,6 +41,7 @@ struct PersistCfg {
     int stages;    // S: checkpoint tiles in flight
     int recbufs;   // RB: record buffers in flight
     int arrivals;  // items per sequence = H / HPI
+    int stall;     // test hook: the consumers first wait on a barrier nothing arrives on
 };
 
 // Threads of a CTA: NC consumers + the tile warp and the record warp.
@@ -172,6 +173,8 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             mbar_init(pempty + i, kPConsumers / 32);
         }
         *s_abort = 0;
+        // the bounded-wait test's barrier (count 1, never arrived on), beside the flag
+        if (pc.stall) mbar_init(reinterpret_cast<uint64_t *>(smraw + lay.flag_off + 8), 1);
         fence_mbar_init();
     }
     for (int i = tid; i < H; i += blockDim.x) {
@@ -224,7 +227,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             const int nu = f8 ? HPI / Q8 : f4 ? HPI / Q4 : f16 ? HPI / Q16 : HPI;
             for (int uu = 0; uu < nu; ++uu) {
                 const int t = issued, s = t % S;
-                if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort);
+                if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort) && !*s_abort;
                 if (!ok) break;
                 unsigned char *dst = stages + s * lay.stage_bytes;
                 if (f4) {
@@ -254,12 +257,16 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             }
         }
         if (!ok) {
-            // a wait gave up: tell everyone, then let the copies in flight land
+            // a wait gave up, or another warp did: tell everyone
             *s_abort = 1;
             flag_error(a.err, RSSM_DEVERR_TIMEOUT);
-            for (int u = issued - S < 0 ? 0 : issued - S; u < issued; ++u)
-                mbar_wait(full + (u % S), (uint32_t)((u / S) & 1));
         }
+        // the copies in flight must land before the CTA ends.  Normally the
+        // consumers waited for every one, but after an abort they stop waiting;
+        // the stages of older units were refilled only after every consumer warp
+        // waited for them (an aborted warp's release is seen above as the abort)
+        for (int u = issued - S < 0 ? 0 : issued - S; u < issued; ++u)
+            mbar_wait(full + (u % S), (uint32_t)((u / S) & 1));
         return;
     }
 
@@ -274,7 +281,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         int k = 0;
         for (; k < n_my; ++k) {
             const int r = k % RB;
-            if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort);
+            if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort) && !*s_abort;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const int it = item_of(k), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;
@@ -480,6 +487,13 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         const int r = k % RB, ia = k % 3;
         const int it = item_of(k), b = item_b(it), h0 = item_h0(it), sb = s_meta[k * 3 + 2];
         const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
+        // test hook of the failure path: a wait that runs out (nothing arrives on
+        // this barrier), so that the abort below is taken on a healthy kernel
+        if (k == 0 && pc.stall && live &&
+            !pwait(reinterpret_cast<uint64_t *>(smraw + lay.flag_off + 8), 0u, s_abort)) {
+            live = false;
+            *s_abort = 1;
+        }
         // the item's records and its prepared arrays
         if (live && !pwait(pfull + ia, (uint32_t)((k / 3) & 1), s_abort)) {
             live = false;

@@ -15,8 +15,10 @@ constexpr int kPersistVPT = 8;
 // Returns RSSM_ERR_UNSUPPORTED (without launching) when the shape is not one
 // the persistent kernel handles; the caller then uses the per-tile kernel.
 // CK: checkpoint precision of the instantiations (0 float32, 1 FP16).
+// stall = 1 is the bounded-wait test hook (the consumers' first wait runs out).
 template <int CK>
-rssm_status launch_decode_persistent_ck(const rssm_mamba2_dims *d, const M2Args &args, cudaStream_t st) {
+rssm_status launch_decode_persistent_ck(const rssm_mamba2_dims *d, const M2Args &args, cudaStream_t st,
+                                        int stall = 0) {
     if (!d->io_bf16 || d->dstate != 128 || d->headdim != 64 || d->nheads > 4096) return RSSM_ERR_UNSUPPORTED;
     const int hpg = d->nheads / d->ngroups;
     const int sms = sm_count();
@@ -56,6 +58,7 @@ rssm_status launch_decode_persistent_ck(const rssm_mamba2_dims *d, const M2Args 
     pc.stages = stages;
     pc.recbufs = recbufs;
     pc.arrivals = d->nheads / hpi;
+    pc.stall = stall;
     constexpr int VPT = kPersistVPT;
     void *k = nullptr;
 #define RSSM_PD(RC)                                                                         \

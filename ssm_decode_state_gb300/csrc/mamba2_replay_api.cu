@@ -7,6 +7,7 @@ namespace rssm {
 
 rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &a, cudaStream_t st);
 rssm_status launch_verify_persistent(const rssm_mamba2_dims *d, const M2Args &a, cudaStream_t st);
+rssm_status launch_decode_persistent_stalled(const rssm_mamba2_dims *d, const M2Args &a, cudaStream_t st);
 
 namespace {
 
@@ -198,6 +199,17 @@ extern "C" rssm_status replayssm_decode(const rssm_mamba2_dims *d, const rssm_ma
     s = launch_decode_persistent(d, a, st);
     if (s != RSSM_ERR_UNSUPPORTED) return s;
     return launch<kDecode, 1>(d, a, g, st);
+}
+
+extern "C" rssm_status replayssm_test_stalled_decode(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c,
+                                                     const float *dt, const void *x, const void *B, const void *C,
+                                                     float *y, void *stream) {
+    TileGeom g;
+    rssm_status s = check_decode_call(d, c, dt, x, B, C, y, true, &g);
+    if (s != RSSM_OK) return s;
+    M2Args a = make_args(d, c, g);
+    a.dt = dt; a.x = x; a.Bin = B; a.Cin = C; a.y = y;
+    return launch_decode_persistent_stalled(d, a, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" rssm_status replayssm_flush(const rssm_mamba2_dims *d, const rssm_mamba2_cache *c,

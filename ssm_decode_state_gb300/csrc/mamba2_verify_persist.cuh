@@ -180,7 +180,7 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             const int it = item_of(k), sb = s_meta[k * 3 + 2], h0 = item_h0(it);
             for (int hh = 0; hh < HPI; ++hh) {
                 const int t = k * HPI + hh, s = t % S;
-                if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort);
+                if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort) && !*s_abort;
                 if (!ok) break;
                 const size_t tile = ((size_t)sb * H + h0 + hh) * P;
                 mbar_arrive_expect_tx(full + s, P * N * 4);
@@ -189,11 +189,16 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             }
         }
         if (!ok) {
+            // a wait gave up, or another warp did: tell everyone
             *s_abort = 1;
             flag_error(a.err, RSSM_DEVERR_TIMEOUT);
-            for (int u = issued - S < 0 ? 0 : issued - S; u < issued; ++u)
-                mbar_wait(full + (u % S), (uint32_t)((u / S) & 1));
         }
+        // the copies in flight must land before the CTA ends.  Normally the
+        // consumers waited for every one, but after an abort they stop waiting;
+        // the stages of older units were refilled only after every consumer warp
+        // waited for them (an aborted warp's release is seen above as the abort)
+        for (int u = issued - S < 0 ? 0 : issued - S; u < issued; ++u)
+            mbar_wait(full + (u % S), (uint32_t)((u / S) & 1));
         return;
     }
 
@@ -209,7 +214,7 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
         int k = 0;
         for (; k < n_my; ++k) {
             const int r = k % RB;
-            if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort);
+            if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort) && !*s_abort;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const int it = item_of(k), b = item_b(it), h0 = item_h0(it), g = h0 / hpg;

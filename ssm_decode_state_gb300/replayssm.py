@@ -26,6 +26,7 @@ EXPORTS = [
     "replayssm_requant", "replayssm_conventional_decode", "replayssm_conventional_verify",
     "replayssm_conventional_select", "replayssm_gdn_decode", "replayssm_gdn_flush", "replayssm_gdn_verify",
     "replayssm_gdn_rollback", "replayssm_gdn_conventional_decode", "replayssm_status_string", "replayssm_version",
+    "replayssm_test_stalled_decode",
 ]
 
 DEVERR_RING_META = 0x1
@@ -65,6 +66,7 @@ _I = ctypes.c_int32
 _sig = {
     "replayssm_decode": [_P, _P, _P, _P, _P, _P, _P, _P],
     "replayssm_decode_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P],
+    "replayssm_test_stalled_decode": [_P, _P, _P, _P, _P, _P, _P, _P],
     "replayssm_flush": [_P, _P, _P, _P],
     "replayssm_verify": [_P, _P, _I, _P, _P, _P, _P, _P, _P],
     "replayssm_rollback": [_P, _P, _I, _P, _P],
@@ -202,6 +204,18 @@ def decode_noalloc(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None, slots=N
     cs.arrive = None
     _check(_lib.replayssm_decode_noalloc(ctypes.byref(d), ctypes.byref(cs), _ptr(dt), _ptr(x), _ptr(B),
                                          _ptr(C), _ptr(y), _stream(stream)))
+    return y
+
+
+def stalled_decode(cache: Mamba2Cache, dt, x, B, C, y=None, stream=None) -> torch.Tensor:
+    """The bounded-wait test hook (replayssm_test_stalled_decode): a decode whose
+    first wait runs out; the cache is not usable afterwards."""
+    d = cache.dims
+    if y is None:
+        y = torch.empty(d.batch, d.nheads, d.headdim, dtype=torch.float32, device=dt.device)
+    cs = cache._seeded()
+    _check(_lib.replayssm_test_stalled_decode(ctypes.byref(d), ctypes.byref(cs), _ptr(dt), _ptr(x), _ptr(B),
+                                              _ptr(C), _ptr(y), _stream(stream)))
     return y
 
 

@@ -79,3 +79,26 @@ def test_memory_report_of_the_bench_line():
     assert m["conventional"] == {"bytes_per_seq_layer": 4194304, "sequences": 1066}
     assert m["fp32"]["sequences"] == 987 and m["fp16_nvfp4_copy"]["sequences"] == 1464
     assert m["fp32_fp8_copy"]["bytes_per_seq_layer"] == m["fp32"]["bytes_per_seq_layer"] + 1081344
+
+
+def test_period_weighted_step():
+    """The figure beside the headline: one flush period from the per-step medians."""
+    sys.path.insert(0, ROOT)
+    import bench
+    split = {"nonflush": [170.0, 168.0, 172.0], "flush": [370.0]}
+    pw = bench.period_weighted(split, 16, 256)
+    assert pw["us_per_step"] == pytest.approx((15 * 170.0 + 370.0) / 16)
+    assert pw["value"] == pytest.approx(256 / (pw["us_per_step"] * 1e-6), rel=1e-6)
+    assert bench.period_weighted({"nonflush": [1.0], "flush": []}, 16, 256) is None
+
+
+def test_all_cores_oracle_baseline():
+    """The oracle on every host core: spawned processes on their own sequences;
+    the rate counts every process's sequence-steps over the slowest one."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from ssm_decode_state_gb300 import inputs as gen
+    shape = gen.Mamba2Shape(8, 4, 16, 16, 1, 16)
+    rate, el, cores, sample = bench.oracle_rate_all_cores(shape, 5, 2, 3, cores=2)
+    assert cores == 2 and el > 0 and rate == pytest.approx(2 * 2 * 3 / el)
+    assert "2 processes" in sample

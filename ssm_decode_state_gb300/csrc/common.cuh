@@ -274,6 +274,43 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
         : "r"(w));
 }
 
+// Four E4M3 codes (byte k = column k) -> their values as two f16 pairs, columns
+// (0, 1) and (2, 3), by the hardware conversion (E4M3 values are exact in f16).
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+    const __half2_raw c = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+    lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
+    hi = (uint32_t)c.x | ((uint32_t)c.y << 16);
+}
+
+// D += A B for one 16 x 8 x 16 tile: the warp-level MMA, f16 operands, FP32
+// accumulation.  Fragment registers as the PTX ISA lays them out for
+// m16n8k16 (A row-major: a0 rows g, a1 rows g + 8, a2 / a3 the same rows at
+// k + 8; B column-major: b0 k = 2t, 2t + 1, b1 k + 8; D d0, d1 row g, d2, d3
+// row g + 8, columns 2t, 2t + 1; g = lane / 4, t = lane % 4).
+__device__ __forceinline__ void mma_f16_16x8x16(float &d0, float &d1, float &d2, float &d3, uint32_t a0,
+                                                uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two E2M1 codes (low nibble first) -> their values as one f16 pair (exact).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t h;
+    asm("{ .reg .b8 b0; cvt.u8.u32 b0, %1; cvt.rn.f16x2.e2m1x2 %0, b0; }" : "=r"(h) : "r"(byte));
+    return h;
+}
+
+// Lane-wise product of two f16 pairs, rounded to nearest.
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // acc + a.lo * c.lo + a.hi * c.hi: f16 pairs, products exact, FP32
 // accumulation (mixed-precision fma of sm_100 and later).
 __device__ __forceinline__ float fma_f16_pair(uint32_t a, uint32_t c, float acc) {
@@ -441,6 +478,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// `count` arrivals at once (release semantics, like mbar_arrive).
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {

@@ -62,7 +62,7 @@ struct PSmem {
     int full_off, empty_off, rfull_off, rempty_off;
     int rec_off, rx_off, rB_off, rC_off, rdt_off, rec_bytes;
     int meta_off, cb_off, w_off, decay_off, rt_off, wx_off, ad_off, flag_off, total;
-    int pfull_off, pempty_off, wcb_off, sfx_off;
+    int pfull_off, pempty_off, wcb_off, sfx_off, cq_off, ch_off;
     // RC: read copy (0 none, 1 FP8, 2 NVFP4); CK: checkpoint precision (0 float32, 1 FP16)
     __host__ __device__ PSmem(int P, int N, int L, int HPI, int S, int RB, int H, int MY, int RC, int CK) {
         const int KM = L + 1;
@@ -97,7 +97,9 @@ struct PSmem {
         rt_off = o;    o += up(3 * HPI * P * 4, 16);        // [3][HPI][P] (rows owned per warp)
         wx_off = o;    o += up(KM * P * 4, 16);             // [KM][P]  (rows owned per warp)
         wcb_off = o;   o += up(3 * HPI * KM * 4, 16);       // [3][HPI][KM]  w_j (B_j . C_t)
-        sfx_off = o;   o += up(HPI * (KM + 1) * 4, 16);     // [HPI][KM + 1] suffix sums (prep only)
+        cq_off = o;    o += up(3 * N * 2, 16);              // [3][N] C_t (bf16) of the item
+        ch_off = o;    o += up(3 * (N * 2 + 16), 16);       // [3] C_t as f16 x 2^e, then e (read copies)
+        sfx_off = o;   o += up(2 * HPI * (KM + 1) * 4, 16); // [2 warps][HPI][KM + 1] suffix sums (prep only)
         ad_off = o;    o += up(2 * H * 4, 16);              // A[H], D[H]
         flag_off = o;  o += 16;
         total = o;
@@ -141,6 +143,8 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     uint64_t *pempty = reinterpret_cast<uint64_t *>(smraw + lay.pempty_off);
     float *s_wcb = reinterpret_cast<float *>(smraw + lay.wcb_off);
     float *s_sfx = reinterpret_cast<float *>(smraw + lay.sfx_off);
+    uint16_t *s_cq = reinterpret_cast<uint16_t *>(smraw + lay.cq_off);
+    unsigned char *s_ch = smraw + lay.ch_off;
 
     const int grid = gridDim.x;
     const int n_my = (pc.items - (int)blockIdx.x + grid - 1) / grid;
@@ -158,6 +162,9 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     auto nv4_item = [&](int hd, int ln) { return q4 && !meta_bad(hd, ln) && ln + 1 < L; };
     // a non-flush item of an FP16 checkpoint without read copy: Q16 heads per stage
     auto h16_item = [&](int hd, int ln) { return CK && RC == 0 && !meta_bad(hd, ln) && ln + 1 < L; };
+    // an item that folds: its consumers read its record buffer (x and B for the fold) and
+    // release it; every other item's buffer is released by the preparation
+    auto fold_item = [&](int hd, int ln) { return !meta_bad(hd, ln) && ln + 1 >= L; };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -169,7 +176,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             mbar_init(rempty + r, kPConsumers / 32);
         }
         for (int i = 0; i < 3; ++i) {
-            mbar_init(pfull + i, kPrepThreads / 32);     // one arrival per preparation warp
+            mbar_init(pfull + i, 1);                     // the preparing warp's lane 0
             mbar_init(pempty + i, kPConsumers / 32);
         }
         *s_abort = 0;
@@ -336,12 +343,16 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
     if (warp >= 2 + kPConsumers / 32) {
         // ============================ item-preparation warps ============================
         // Per item, ahead of the consumers: append the token to the ring, B_j . C_t,
-        // the decay weights, and the record term of every row of every head.  Item
-        // arrays are triple-buffered (ia = item % 3); pempty says the consumers are
-        // done with a buffer, pfull hands a prepared one over.
-        const int ptid = tid - 64 - kPConsumers, pw = ptid >> 5;
+        // the decay weights, and the record term of every row of every head.  The two
+        // warps take alternate items (each item's chain of dependent steps is short of
+        // work, so two items in flight double the rate).  Item arrays are
+        // triple-buffered (ia = item % 3); pempty says the consumers are done with a
+        // buffer, pfull hands a prepared one over.
+        const int pw = (tid - 64 - kPConsumers) >> 5, ptid = lane;
+        constexpr int PT = 32;                           // threads per item
+        float *sfx = s_sfx + pw * HPI * (KM + 1);        // this warp's suffix sums
         bool live = true;
-        for (int kk = 0; kk < n_my; ++kk) {
+        for (int kk = pw; kk < n_my; kk += 2) {
             const int r = kk % RB, ia = kk % 3;
             // the preparation only writes the cache (the ring appends): b is the item's slot
             const int it = item_of(kk), b = s_meta[kk * 3 + 2], h0 = item_h0(it), g = h0 / hpg;
@@ -368,7 +379,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 // no one reads during this launch; the token is already in the record buffer
                 const int slot = hd + ln < L ? hd + ln : hd + ln - L;
                 const int nBC = (h0 % hpg == 0) ? 2 * CB : 0;   // the group's first chunk writes B and C
-                for (int idx = ptid; idx < HPI * CX + nBC + HPI; idx += kPrepThreads) {
+                for (int idx = ptid; idx < HPI * CX + nBC + HPI; idx += PT) {
                     if (idx < HPI * CX) {
                         const int hh = idx / CX, c = idx - hh * CX;
                         const size_t bh = (size_t)b * H + h0 + hh;
@@ -393,7 +404,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 // per head gives every S_j and the total
                 if (ptid < HPI) {
                     const float *dth = r_dt + ptid * KM;
-                    float *sf = s_sfx + ptid * (KM + 1);
+                    float *sf = sfx + ptid * (KM + 1);
                     float acc = 0.0f;
                     for (int j = ln; j >= 0; --j) {
                         sf[j] = acc;
@@ -402,8 +413,8 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                     sf[KM] = acc;
                 }
                 // B_j . C_t: 8 lanes per record, 16 columns per lane as bf16 pairs, then a
-                // 3-level butterfly; each warp takes 4 records at a time
-                for (int jb = pw * 4; jb < nrec; jb += 8) {
+                // 3-level butterfly; 4 records at a time
+                for (int jb = 0; jb < nrec; jb += 4) {
                     const int j = jb + (lane >> 3);
                     float acc = 0.0f;
                     if (j < nrec) {
@@ -427,21 +438,21 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                     if (j < nrec && (lane & 7) == 0) cb[j] = acc;
                 }
             }
-            prep_sync();                                 // S_j and B_j . C_t
+            __syncwarp();                                // S_j and B_j . C_t
             if (work) {
                 // w_j = exp(A S_j) dt_j, w_j (B_j . C_t), and exp(A S) per head
-                for (int idx = ptid; idx < HPI * nrec; idx += kPrepThreads) {
+                for (int idx = ptid; idx < HPI * nrec; idx += PT) {
                     const int hh = idx / nrec, j = idx - hh * nrec;
-                    const float wv = expf(s_A[h0 + hh] * s_sfx[hh * (KM + 1) + j]) * r_dt[hh * KM + j];
+                    const float wv = expf(s_A[h0 + hh] * sfx[hh * (KM + 1) + j]) * r_dt[hh * KM + j];
                     w[hh * KM + j] = wv;
                     wcb[hh * KM + j] = wv * cb[j];
                 }
-                if (ptid < HPI) dec[ptid] = expf(s_A[h0 + ptid] * s_sfx[ptid * (KM + 1) + KM]);
+                if (ptid < HPI) dec[ptid] = expf(s_A[h0 + ptid] * sfx[ptid * (KM + 1) + KM]);
             }
-            prep_sync();                                 // w, w (B . C)
+            __syncwarp();                                // w, w (B . C)
             if (work) {
                 // record term of every row: 8 consecutive rows of one head per thread
-                for (int o = ptid; o < HPI * P / 8; o += kPrepThreads) {
+                for (int o = ptid; o < HPI * P / 8; o += PT) {
                     const int hh = o / (P / 8), r0 = (o - hh * (P / 8)) * 8;
                     const uint16_t *xh = r_x + hh * KM * P + r0;
                     const float *wc = wcb + hh * KM;
@@ -469,8 +480,36 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                                          fmaf(Dh, bf16lo(xl.w), acc[6]), fmaf(Dh, bf16hi(xl.w), acc[7]));
                 }
             }
+            // C_t goes with the item's arrays, so that the consumers of an item that does
+            // not fold never read its record buffer: the preparation releases that buffer
+            // itself and the record warp can run further ahead
+            if (lane < N / 8)
+                reinterpret_cast<uint4 *>(s_cq + ia * N)[lane] = reinterpret_cast<const uint4 *>(r_C)[lane];
+            if constexpr (RC != 0) {
+                // for the read-copy MMA: C_t as f16 pairs times 2^e, e set from the item's
+                // largest |C_t| so that it lands just below 2^15 (exact and overflow-free;
+                // only values below max|C_t| 2^-29 lose bits), and e itself
+                static_assert(N == 128, "4 columns per lane");
+                float cv[4], cmax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    cv[i] = bf16_at(r_C, lane * 4 + i);
+                    cmax = fmaxf(cmax, fabsf(cv[i]));
+                }
+                cmax = group_max<32>(cmax);
+                const int ce = cmax > 0.0f ? min(max(14 - ilogbf(cmax), -120), 120) : 0;
+                const float cs = pow2f(ce);
+                const __half2 p0 = __floats2half2_rn(cv[0] * cs, cv[1] * cs), p1 = __floats2half2_rn(cv[2] * cs, cv[3] * cs);
+                unsigned char *ch = s_ch + ia * (N * 2 + 16);
+                reinterpret_cast<uint2 *>(ch)[lane] =
+                    make_uint2(*reinterpret_cast<const uint32_t *>(&p0), *reinterpret_cast<const uint32_t *>(&p1));
+                if (lane == 0) *reinterpret_cast<int *>(ch + N * 2) = ce;
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(pfull + ia);      // item kk is prepared
+            if (lane == 0) {
+                mbar_arrive(pfull + ia);                 // item kk is prepared
+                if (!fold_item(hd, ln)) mbar_arrive_n(rempty + r, kPConsumers / 32);
+            }
         }
         if (ptid == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
         return;
@@ -499,7 +538,8 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             live = false;
             *s_abort = 1;
         }
-        if (live && !pwait(rfull + r, (uint32_t)((k / RB) & 1), s_abort)) {
+        const bool fitem = fold_item(hd, ln);
+        if (fitem && live && !pwait(rfull + r, (uint32_t)((k / RB) & 1), s_abort)) {
             live = false;
             *s_abort = 1;
         }
@@ -509,7 +549,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
         const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
         const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
-        const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
+        const uint16_t *r_C = s_cq + ia * N;             // C_t, from the prepared item
         const float *w = s_w + ia * HPI * KM, *dec = s_decay + ia * HPI, *rt = s_rt + ia * HPI * P;
         const float4 cfr = make_float4(bf16_at(r_C, col4 * 4 + 0), bf16_at(r_C, col4 * 4 + 1),
                                        bf16_at(r_C, col4 * 4 + 2), bf16_at(r_C, col4 * 4 + 3));
@@ -559,27 +599,22 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 }
             }
         } else if (nv4_item(hd, ln)) {
-            // NVFP4 codes, Q4 heads per stage.  Lane (blk, rsub) takes the 16-column
-            // block blk = lane & 7 of rows rsub and rsub + 4 (rsub = lane >> 3) of the
-            // warp's 8 rows: its block sums need one block scale each, then the 8
-            // lanes of a row reduce them.  Codes become f16 pairs in hardware; C_t
-            // enters as f16 pairs times 2^e, e set from the item's largest |C_t| so
-            // that it lands just below 2^15: the scaling is exact and cannot
-            // overflow, and only values below max|C_t| 2^-29 lose bits (f16
-            // subnormals).  Products are exact, sums FP32; 2^-e comes off at the end.
-            const int blk = lane & 7, rsub = lane >> 3;
-            float cmax = 0.0f;
+            // NVFP4 codes, Q4 heads per stage, through the warp-level f16 MMA as on the
+            // FP8 path (same k order: lane (g, t) takes columns 32 t .. 32 t + 31 of
+            // rows g and g + 8 of each 16-row tile, 16 bytes of codes per row).  Codes
+            // become f16 pairs in hardware and are multiplied by their block's E4M3
+            // scale in f16 (a 2-bit times a 4-bit significand, between 2^-10 and 2688:
+            // exact), so the MMA's A holds code x block scale; C_t enters as f16 times
+            // 2^e (see the FP8 path) and the row scale comes after the reduction.
+            constexpr int MT = Q4 >= 2 ? Q4 / 2 : 1;       // 16-row tiles per warp and stage
+            const int g = lane >> 2, t4 = lane & 3;
+            const unsigned char *ch = s_ch + ia * (N * 2 + 16);
+            const float cinv = pow2f(-*reinterpret_cast<const int *>(ch + N * 2));
+            uint32_t bf[16];                             // B fragments: [kt][0, 1]
 #pragma unroll
-            for (int i = 0; i < 16; ++i) cmax = fmaxf(cmax, fabsf(bf16_at(r_C, blk * 16 + i)));
-            cmax = group_max<32>(cmax);
-            const int ce = cmax > 0.0f ? min(max(14 - ilogbf(cmax), -120), 120) : 0;
-            const float cs = pow2f(ce), cinv = pow2f(-ce);
-            uint32_t cp[8];                              // pairs (2i, 2i + 1) of the block
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const __half2 pr = __floats2half2_rn(bf16_at(r_C, blk * 16 + 2 * i) * cs,
-                                                     bf16_at(r_C, blk * 16 + 2 * i + 1) * cs);
-                cp[i] = *reinterpret_cast<const uint32_t *>(&pr);
+            for (int q = 0; q < 4; ++q) {
+                const uint4 w = g == 0 ? reinterpret_cast<const uint4 *>(ch)[t4 * 4 + q] : make_uint4(0u, 0u, 0u, 0u);
+                bf[4 * q] = w.x; bf[4 * q + 1] = w.y; bf[4 * q + 2] = w.z; bf[4 * q + 3] = w.w;
             }
             for (int uu = 0; uu < HPI / Q4; ++uu, ++u) {
                 const int s = u % S;
@@ -589,56 +624,96 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 }
                 const unsigned char *stg = stages + s * lay.stage_bytes;
                 const float *sc = reinterpret_cast<const float *>(stg + Q4 * HB4);
-                uint2 qc[Q4][2];
-                uint32_t sbc[Q4][2];
+                uint4 qv[MT][2];                         // 32 codes of rows g, g + 8 of each tile
+                uint32_t bsc[MT][2];                     // their two block scales (E4M3 bytes)
+                float rsv[MT][2];
 #pragma unroll
-                for (int hq = 0; hq < Q4; ++hq) {
+                for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const int row = cw * VPT + rsub + 4 * m;
-                        qc[hq][m] = *reinterpret_cast<const uint2 *>(stg + hq * HB4 + row * (N / 2) + blk * 8);
-                        sbc[hq][m] = stg[hq * HB4 + P * N / 2 + row * (N / 16) + blk];
+                    for (int hv2 = 0; hv2 < 2; ++hv2) {
+                        const int hq = 2 * mt + hv2, row = cw * VPT + g;
+                        if (hq < Q4) {
+                            const unsigned char *hb = stg + hq * HB4;
+                            qv[mt][hv2] = *reinterpret_cast<const uint4 *>(hb + row * (N / 2) + 16 * t4);
+                            bsc[mt][hv2] = *reinterpret_cast<const uint16_t *>(hb + P * N / 2 + row * (N / 16) + 2 * t4);
+                            rsv[mt][hv2] = sc[hq * P + row];
+                        } else {
+                            qv[mt][hv2] = make_uint4(0u, 0u, 0u, 0u);
+                            bsc[mt][hv2] = 0u;
+                            rsv[mt][hv2] = 0.0f;
+                        }
                     }
-                }
-                // the row scale of the (head, row) this lane ends up with after the reduction
-                float rsv;
-                {
-                    const int vi = reduced_index<8, Q4 * 2>(0);
-                    rsv = sc[(vi >> 1) * P + cw * VPT + rsub + 4 * (vi & 1)];
                 }
                 __syncwarp();                            // the warp is done with the stage
                 if (lane == 0) mbar_arrive(empty + s);
                 if (!work) continue;
-                float part[Q4 * 2];
 #pragma unroll
-                for (int hq = 0; hq < Q4; ++hq) {
+                for (int mt = 0; mt < MT; ++mt) {
+                    // block scales as f16 pairs (s, s): blocks 2t (k-tiles 0-3) and 2t + 1 (4-7)
+                    uint32_t sp[2][2];
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        uint32_t pa[4], pb[4];
-                        e2m1x8_to_f16x2(qc[hq][m].x, pa);
-                        e2m1x8_to_f16x2(qc[hq][m].y, pb);
-                        float acc = 0.0f;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) acc = fma_f16_pair(pa[i], cp[i], acc);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) acc = fma_f16_pair(pb[i], cp[4 + i], acc);
-                        part[hq * 2 + m] = acc * e4m3_value(sbc[hq][m]);
+                    for (int hv2 = 0; hv2 < 2; ++hv2) {
+                        uint32_t lo, hi;
+                        e4m3x4_to_f16x2(bsc[mt][hv2], lo, hi);
+                        sp[hv2][0] = __byte_perm(lo, 0u, 0x1010);
+                        sp[hv2][1] = __byte_perm(lo, 0u, 0x3232);
                     }
-                }
-                group_reduce<8, Q4 * 2>(part);
-                if (reduced_writer<8, Q4 * 2>()) {
-                    const int vi = reduced_index<8, Q4 * 2>(0);
-                    const int hh = uu * Q4 + (vi >> 1), row = cw * VPT + rsub + 4 * (vi & 1);
-                    a.y[((size_t)b * H + h0 + hh) * P + row] =
-                        fmaf(dec[hh], (part[0] * cinv) * rsv, rt[hh * P + row]);
+                    const uint32_t w0[4] = {qv[mt][0].x, qv[mt][0].y, qv[mt][0].z, qv[mt][0].w};
+                    const uint32_t w1[4] = {qv[mt][1].x, qv[mt][1].y, qv[mt][1].z, qv[mt][1].w};
+                    // two accumulator sets (even and odd k-tiles): two short dependent chains
+                    float dd[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll
+                    for (int kt = 0; kt < 8; ++kt) {
+                        // k-tile kt: bytes 2 kt, 2 kt + 1 of the row's 16 (codes 4 kt .. 4 kt + 3)
+                        const uint32_t h0w = (w0[kt >> 1] >> (16 * (kt & 1))) & 0xffffu;
+                        const uint32_t h1w = (w1[kt >> 1] >> (16 * (kt & 1))) & 0xffffu;
+                        const int bi = kt >> 2;
+                        const uint32_t a0 = hmul2_u32(e2m1x2_to_f16x2(h0w & 0xffu), sp[0][bi]);
+                        const uint32_t a2 = hmul2_u32(e2m1x2_to_f16x2(h0w >> 8), sp[0][bi]);
+                        const uint32_t a1 = hmul2_u32(e2m1x2_to_f16x2(h1w & 0xffu), sp[1][bi]);
+                        const uint32_t a3 = hmul2_u32(e2m1x2_to_f16x2(h1w >> 8), sp[1][bi]);
+                        float (&dk)[4] = dd[kt & 1];
+                        mma_f16_16x8x16(dk[0], dk[1], dk[2], dk[3], a0, a1, a2, a3, bf[2 * kt], bf[2 * kt + 1]);
+                    }
+                    const float d0 = dd[0][0] + dd[1][0], d2 = dd[0][2] + dd[1][2];
+                    if (t4 == 0) {
+#pragma unroll
+                        for (int hv2 = 0; hv2 < 2; ++hv2) {
+                            const int hq = 2 * mt + hv2;
+                            if (hq < Q4) {
+                                const int hh = uu * Q4 + hq, row = cw * VPT + g;
+                                const float dsum = hv2 ? d2 : d0;
+                                a.y[((size_t)b * H + h0 + hh) * P + row] =
+                                    fmaf(dec[hh], (dsum * cinv) * rsv[mt][hv2], rt[hh * P + row]);
+                            }
+                        }
+                    }
                 }
             }
         } else if (fp8_item(hd, ln)) {
-            // C_t of this lane's columns as bfloat16 pairs (0, 2) and (1, 3)
-            const uint2 craw = *reinterpret_cast<const uint2 *>(r_C + col4 * 4);
-            const uint32_t ce = __byte_perm(craw.x, craw.y, 0x5410), co = __byte_perm(craw.x, craw.y, 0x7632);
-            // FP8 codes, Q8 heads per stage: take every code and scale this thread
-            // needs, release the stage, then decode and reduce head by head
+            // FP8 codes, Q8 heads per stage: a warp's rows of the stage are its 8 rows of
+            // each of the Q8 heads, and their products with C_t go through the warp-level
+            // f16 MMA (m16n8k16, FP32 accumulation) as a matrix-vector product: the codes
+            // are A (rows x dstate; every E4M3 value is exact in f16, converted in
+            // hardware), C_t is column 0 of B, the other columns zero.  One MMA replaces
+            // 256 scalar multiply-adds; the SIMT form of this product was bound by
+            // instruction issue.  dstate is the MMA's reduction axis, so its order is
+            // free: lane (g, t) = (lane >> 2, lane & 3) takes the 32 consecutive codes
+            // 32 t .. 32 t + 31 of rows g and g + 8 of each 16-row tile, and k-tile kt
+            // reads their bytes 4 kt .. 4 kt + 3 (two 16-byte loads per row); lanes
+            // 0-3 hold C_t (as f16 times 2^e, prepared with the item) in the same order,
+            // which is the natural order of its column pairs.  Products are exact;
+            // 2^-e comes off at the end.
+            constexpr int MT = Q8 >= 2 ? Q8 / 2 : 1;       // 16-row tiles per warp and stage
+            const int g = lane >> 2, t4 = lane & 3;
+            const unsigned char *ch = s_ch + ia * (N * 2 + 16);
+            const float cinv = pow2f(-*reinterpret_cast<const int *>(ch + N * 2));
+            uint32_t bf[16];                             // B fragments: [kt][0, 1] = pairs 16 t + 2 kt + (0, 1)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 w = g == 0 ? reinterpret_cast<const uint4 *>(ch)[t4 * 4 + q] : make_uint4(0u, 0u, 0u, 0u);
+                bf[4 * q] = w.x; bf[4 * q + 1] = w.y; bf[4 * q + 2] = w.z; bf[4 * q + 3] = w.w;
+            }
             for (int uu = 0; uu < HPI / Q8; ++uu, ++u) {
                 const int s = u % S;
                 if (live && !pwait(full + s, (uint32_t)((u / S) & 1), s_abort)) {
@@ -646,42 +721,63 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                     *s_abort = 1;
                 }
                 const unsigned char *stg = stages + s * lay.stage_bytes;
-                const uint32_t *q = reinterpret_cast<const uint32_t *>(stg);
                 const float *sc = reinterpret_cast<const float *>(stg + Q8 * P * N);
-                uint32_t qc[Q8][VPT];
+                // rows g and g + 8 of tile mt are stage rows 16 mt + g (+ 8): head
+                // (16 mt + g (+ 8)) / 8 of the stage, row cw * 8 + g of that head
+                uint4 qv[MT][2][2];
+                float rsv[MT][2];
 #pragma unroll
-                for (int hq = 0; hq < Q8; ++hq) {
+                for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-                    for (int v = 0; v < VPT; ++v) qc[hq][v] = q[hq * (P * N / 4) + (cw * VPT + v) * G4 + lane];
-                }
-                // the row scale of the (head, row) this lane ends up with after the reduction
-                float rsv;
-                {
-                    const int vi = reduced_index<G4, Q8 * VPT>(0), hq = vi / VPT;
-                    rsv = sc[hq * P + cw * VPT + (vi - hq * VPT)];
+                    for (int hv2 = 0; hv2 < 2; ++hv2) {
+                        const int hq = 2 * mt + hv2;
+                        if (hq < Q8) {
+                            const unsigned char *rowp = stg + hq * (P * N) + (cw * VPT + g) * N + 32 * t4;
+                            qv[mt][hv2][0] = *reinterpret_cast<const uint4 *>(rowp);
+                            qv[mt][hv2][1] = *reinterpret_cast<const uint4 *>(rowp + 16);
+                            rsv[mt][hv2] = sc[hq * P + cw * VPT + g];
+                        } else {
+                            qv[mt][hv2][0] = qv[mt][hv2][1] = make_uint4(0u, 0u, 0u, 0u);
+                            rsv[mt][hv2] = 0.0f;
+                        }
+                    }
                 }
                 __syncwarp();                            // the warp is done with the stage
                 if (lane == 0) mbar_arrive(empty + s);
                 if (!work) continue;
-                // codes enter the dot at 2^-120 of their value; the Q8 x 8 row sums of the
-                // stage go through one transposed reduction, then each is scaled back
-                // (exactly) and by its row scale
-                float part[Q8 * VPT];
 #pragma unroll
-                for (int hq = 0; hq < Q8; ++hq) {
+                for (int mt = 0; mt < MT; ++mt) {
+                    const uint32_t w0[8] = {qv[mt][0][0].x, qv[mt][0][0].y, qv[mt][0][0].z, qv[mt][0][0].w,
+                                            qv[mt][0][1].x, qv[mt][0][1].y, qv[mt][0][1].z, qv[mt][0][1].w};
+                    const uint32_t w1[8] = {qv[mt][1][0].x, qv[mt][1][0].y, qv[mt][1][0].z, qv[mt][1][0].w,
+                                            qv[mt][1][1].x, qv[mt][1][1].y, qv[mt][1][1].z, qv[mt][1][1].w};
+                    // two accumulator sets (even and odd k-tiles): two short dependent chains
+                    float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f, d3 = 0.0f, e0 = 0.0f, e1 = 0.0f, e2 = 0.0f, e3 = 0.0f;
 #pragma unroll
-                    for (int v = 0; v < VPT; ++v) {
-                        uint32_t ev, od;
-                        e4m3_to_bf16_pairs(qc[hq][v], ev, od);
-                        part[hq * VPT + v] = fma_bf16_pair(od, co, fma_bf16_pair(ev, ce, 0.0f));
+                    for (int kt = 0; kt < 8; kt += 2) {
+                        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+                        e4m3x4_to_f16x2(w0[kt], a0, a2);     // row g: k-pairs (2t, 2t+1), (2t+8, 2t+9)
+                        e4m3x4_to_f16x2(w1[kt], a1, a3);     // row g + 8
+                        e4m3x4_to_f16x2(w0[kt + 1], c0, c2);
+                        e4m3x4_to_f16x2(w1[kt + 1], c1, c3);
+                        mma_f16_16x8x16(d0, d1, d2, d3, a0, a1, a2, a3, bf[2 * kt], bf[2 * kt + 1]);
+                        mma_f16_16x8x16(e0, e1, e2, e3, c0, c1, c2, c3, bf[2 * kt + 2], bf[2 * kt + 3]);
                     }
-                }
-                group_reduce<G4, Q8 * VPT>(part);
-                if (reduced_writer<G4, Q8 * VPT>()) {
-                    const int vi = reduced_index<G4, Q8 * VPT>(0), hq = vi / VPT;
-                    const int hh = uu * Q8 + hq, row = cw * VPT + (vi - hq * VPT);
-                    a.y[((size_t)b * H + h0 + hh) * P + row] =
-                        fmaf(dec[hh], (part[0] * 0x1p120f) * rsv, rt[hh * P + row]);
+                    d0 += e0;
+                    d2 += e2;
+                    // column 0 of D: rows g (d0) and g + 8 (d2) in the lanes with t = 0
+                    if (t4 == 0) {
+#pragma unroll
+                        for (int hv2 = 0; hv2 < 2; ++hv2) {
+                            const int hq = 2 * mt + hv2;
+                            if (hq < Q8) {
+                                const int hh = uu * Q8 + hq, row = cw * VPT + g;
+                                const float dsum = hv2 ? d2 : d0;
+                                a.y[((size_t)b * H + h0 + hh) * P + row] =
+                                    fmaf(dec[hh], (dsum * cinv) * rsv[mt][hv2], rt[hh * P + row]);
+                            }
+                        }
+                    }
                 }
             }
         } else {
@@ -788,7 +884,7 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         }
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(rempty + r);                     // record buffer r may be refilled
+            if (fitem) mbar_arrive(rempty + r);          // record buffer r may be refilled
             mbar_arrive(pempty + ia);                    // and the item arrays ia
         }
     }

@@ -34,7 +34,7 @@ struct VSmem {
     int stage_bytes, stages_off;
     int full_off, empty_off, rfull_off, rempty_off, pfull_off, pempty_off;
     int rec_off, rx_off, rB_off, rC_off, rdt_off, rec_bytes;
-    int meta_off, decay_off, wf_off, fdec_off, rt_off, cb_off, wcb_off, sfx_off, sff_off, wx_off, ad_off, flag_off;
+    int meta_off, decay_off, wf_off, fdec_off, rt_off, cq_off, cb_off, wcb_off, sfx_off, sff_off, wx_off, ad_off, flag_off;
     int total;
     __host__ __device__ VSmem(int P, int N, int L, int T, int HPI, int S, int RB, int H, int MY) {
         const int KM = L + T;
@@ -62,6 +62,7 @@ struct VSmem {
         wf_off = o;    o += up(3 * HPI * KM * 4, 16);       // [3][HPI][KM]   fold weights
         fdec_off = o;  o += up(3 * HPI * 4, 16);            // [3][HPI]       fold decay
         rt_off = o;    o += up(3 * HPI * T * P * 4, 16);    // [3][HPI][T][P] record terms
+        cq_off = o;    o += up(3 * T * N * 2, 16);          // [3][T][N] the drafts' C (bf16)
         // the preparation warps' own scratch
         cb_off = o;    o += up(T * KM * 4, 16);             // [T][KM]        B_j . C_i
         wcb_off = o;   o += up(HPI * T * KM * 4, 16);       // [HPI][T][KM]   w_ij (B_j . C_i)
@@ -106,6 +107,7 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
     float *s_fdec = reinterpret_cast<float *>(smraw + lay.fdec_off);
     float *s_rt = reinterpret_cast<float *>(smraw + lay.rt_off);
     float *s_wx = reinterpret_cast<float *>(smraw + lay.wx_off);
+    uint16_t *s_cq = reinterpret_cast<uint16_t *>(smraw + lay.cq_off);
     float *s_A = reinterpret_cast<float *>(smraw + lay.ad_off), *s_D = s_A + H;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smraw + lay.flag_off);
 
@@ -118,6 +120,9 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
         return (bg % G) * hpg + c * HPI;
     };
     auto meta_bad = [&](int hd, int ln) { return hd < 0 || hd >= L || ln < 0 || ln > L; };
+    // an item that pre-flushes: its consumers fold the buffered records (x and B from the
+    // record buffer) and release that buffer; every other buffer the preparation releases
+    auto pre_item = [&](int hd, int ln) { return !meta_bad(hd, ln) && ln + T > L; };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -423,7 +428,13 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(pfull + ia);      // item kk is prepared
+            // the drafts' C goes with the item's arrays, so that the consumers of an item
+            // without a pre-flush never read its record buffer
+            for (int c = ptid; c < T * N / 8; c += kPrepThreads)
+                reinterpret_cast<uint4 *>(s_cq + ia * T * N)[c] = reinterpret_cast<const uint4 *>(r_C)[c];
+            prep_sync();                                 // both warps are done with the buffer
+            if (lane == 0) mbar_arrive(pfull + ia);      // item kk is prepared (one arrival per warp)
+            if (ptid == 0 && !pre_item(hd, ln)) mbar_arrive_n(rempty + r, NC / 32);
         }
         if (ptid == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
         return;
@@ -442,17 +453,18 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             live = false;
             *s_abort = 1;
         }
-        if (live && !pwait(rfull + r, (uint32_t)((k / RB) & 1), s_abort)) {
+        const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
+        const bool pitem = pre_item(hd, ln);
+        if (pitem && live && !pwait(rfull + r, (uint32_t)((k / RB) & 1), s_abort)) {
             live = false;
             *s_abort = 1;
         }
-        const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
         const bool work = live && !meta_bad(hd, ln);
         const bool pre = work && (ln + T > L);
         const unsigned char *rb = smraw + lay.rec_off + r * lay.rec_bytes;
         const uint16_t *r_x = reinterpret_cast<const uint16_t *>(rb + lay.rx_off);
         const uint16_t *r_B = reinterpret_cast<const uint16_t *>(rb + lay.rB_off);
-        const uint16_t *r_C = reinterpret_cast<const uint16_t *>(rb + lay.rC_off);
+        const uint16_t *r_C = s_cq + ia * T * N;         // the drafts' C, from the prepared item
         const float *dec = s_decay + ia * HPI * T, *rt = s_rt + ia * HPI * T * P;
         const float *wf = s_wf + ia * HPI * KM, *fdec = s_fdec + ia * HPI;
         float4 cfr[TQ];
@@ -547,7 +559,7 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
         }
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(rempty + r);                     // record buffer r may be refilled
+            if (pitem) mbar_arrive(rempty + r);          // record buffer r may be refilled
             mbar_arrive(pempty + ia);                    // and the item arrays ia
         }
     }

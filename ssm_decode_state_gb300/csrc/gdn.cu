@@ -13,7 +13,7 @@
 // sum_j beta_j d_j v_j[r].  The flush folds the records into every row,
 // oldest first: s <- alpha_j s + beta_j (v_j[r] - alpha_j (s . k_j)) k_j.
 #include "common.cuh"
-#include "gdn_persist.cuh"
+#include "gdn_verify_persist.cuh"
 #include "host_common.h"
 
 namespace rssm {
@@ -625,6 +625,43 @@ rssm_status launch(void *k, const rssm_gdn_dims *d, GArgs &a, const TileGeom &g,
     return launch_status();
 }
 
+// Persistent verify at the serving head shape (dk = dv = 128, T <= 4, L <= 16)
+// when every SM gets at least two items; RSSM_ERR_UNSUPPORTED (nothing launched)
+// otherwise.
+rssm_status launch_verify_persistent(const rssm_gdn_dims *d, const rssm_gdn_cache *c, int T, const uint16_t *q,
+                                     const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
+                                     float *o, cudaStream_t st) {
+    if (d->dk != 128 || d->dv != 128 || d->L > kGdnMaxRec || T > kGdnVT) return RSSM_ERR_UNSUPPORTED;
+    const int sms = sm_count();
+    const long long items = (long long)d->batch * d->nheads;
+    if (items < 2LL * sms || items > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;
+    const int grid = sms;
+    const int max_my = (int)((items + grid - 1) / grid);
+    if (max_my > 4096) return RSSM_ERR_UNSUPPORTED;
+    constexpr int RB = 4;
+    int stages = 0;
+    size_t smem = 0;
+    for (int s = 6; s >= 2; --s) {
+        const GVPSmem lay(128, 128, d->L, T, s, RB, max_my);
+        if (lay.total <= 227 * 1024) { stages = s; smem = lay.total; break; }
+    }
+    if (!stages) return RSSM_ERR_UNSUPPORTED;
+    GPArgs a{};
+    a.H = d->nheads; a.L = d->L; a.items = (int)items; a.max_my = max_my; a.stages = stages; a.recbufs = RB;
+    a.T = T;
+    a.ckpt = c->ckpt; a.rec_k = c->rec_k; a.rec_v = c->rec_v; a.rec_alpha = c->rec_alpha; a.rec_beta = c->rec_beta;
+    a.ring_head = c->ring_head; a.ring_len = c->ring_len; a.arrive = c->arrive; a.err = c->err;
+    a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.o = o;
+    a.slots = c->slots; a.cap = cache_capacity(d, c);
+    void *kern = (void *)gdn_verify_persistent<128, 128>;
+    rssm_status s = ensure_smem((const void *)kern, smem);
+    if (s != RSSM_OK) return s;
+    void *params[] = {&a};
+    if (cudaLaunchKernel(kern, dim3(grid), dim3(256 + 64 + kPrepThreads), params, smem, st) != cudaSuccess)
+        return RSSM_ERR_CUDA;
+    return launch_status();
+}
+
 // Persistent decode at the serving head shape (dk = dv = 128) when every SM
 // gets at least two items; RSSM_ERR_UNSUPPORTED (nothing launched) otherwise.
 rssm_status launch_persistent(const rssm_gdn_dims *d, const rssm_gdn_cache *c, const uint16_t *q,
@@ -707,6 +744,9 @@ extern "C" rssm_status replayssm_gdn_verify(const rssm_gdn_dims *d, const rssm_g
     if (T < 1 || T > kMaxT || T > d->L) return RSSM_ERR_RING;
     if (!q || !k || !v || !alpha || !beta || !o) return RSSM_ERR_NULL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return RSSM_ERR_ALIGN;
+    // serving shapes: the persistent pipelined verify (it appends the drafts itself)
+    s = launch_verify_persistent(d, c, T, q, k, v, alpha, beta, o, static_cast<cudaStream_t>(stream));
+    if (s != RSSM_ERR_UNSUPPORTED) return s;
     TileGeom g;
     if (!choose_geom(d->batch, d->nheads, d->dv, d->dk, g)) return RSSM_ERR_UNSUPPORTED;
     GArgs a = make_args(d, g);

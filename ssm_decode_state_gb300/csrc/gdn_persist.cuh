@@ -42,6 +42,7 @@ struct GPArgs {
     float *o;
     const int32_t *slots;   // [batch] cache slot of each batch row; nullptr: row b uses slot b
     int cap;                // sequences the cache arrays hold
+    int T;                  // drafts per sequence (verify only)
 };
 
 constexpr int kGdnRows = 64;     // state rows per stage
@@ -86,6 +87,159 @@ struct GPSmem {
         total = o;
     }
 };
+
+// Fold constants of nr records (the preparation warps' share of a fold): the
+// Gram entries C_ij = (k_i . k_j) prod_{i<m<j} alpha_m (i < j), the prefix
+// products a_j = prod_{m<j} alpha_m, the suffix products g_j = prod_{m>j}
+// alpha_m and the total product A, into fc (one warp, nr <= 16).
+template <int DK>
+__device__ __forceinline__ void gdn_fold_constants(float *fc, const uint16_t *r_k, const float *r_al, int nr) {
+    constexpr int CK = DK / 8;                           // 16-byte chunks per k row
+    const int lane = threadIdx.x & 31;
+    // lane l: row i = l / 2 of the Gram matrix, columns j0 .. j0 + 7 (j0 = 8 (l % 2)),
+    // eight independent bf16-pair dot products over dk
+    {
+        const int i = lane >> 1, j0 = (lane & 1) * 8;
+        float g8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) g8[q] = 0.0f;
+        if (i < nr) {
+            for (int cc = 0; cc < CK; ++cc) {
+                const int c = (cc + (lane >> 1)) % CK;   // rows start on different chunks
+                const uint4 ki = *reinterpret_cast<const uint4 *>(r_k + i * DK + c * 8);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int j = j0 + q < nr ? j0 + q : i;
+                    const uint4 kj = *reinterpret_cast<const uint4 *>(r_k + j * DK + c * 8);
+                    float t = g8[q];
+                    t = fma_bf16_pair(ki.x, kj.x, t);
+                    t = fma_bf16_pair(ki.y, kj.y, t);
+                    t = fma_bf16_pair(ki.z, kj.z, t);
+                    t = fma_bf16_pair(ki.w, kj.w, t);
+                    g8[q] = t;
+                }
+            }
+            // C_ij = K_ij prod_{i<m<j} alpha_m for j > i
+            float pa = 1.0f;
+            for (int m = i + 1; m < j0; ++m) pa *= r_al[m];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int j = j0 + q;
+                if (j > i && j < nr) {
+                    fc[i * kGdnMaxRec + j] = g8[q] * pa;
+                    pa *= r_al[j];
+                }
+            }
+        }
+    }
+    if (lane < nr) {
+        float pa = 1.0f, pg = 1.0f;
+        for (int m = 0; m < lane; ++m) pa *= r_al[m];
+        for (int m = lane + 1; m < nr; ++m) pg *= r_al[m];
+        fc[kFcA + lane] = pa;
+        fc[kFcG + lane] = pg;
+    }
+    if (lane == 0) {
+        float pt = 1.0f;
+        for (int m = 0; m < nr; ++m) pt *= r_al[m];
+        fc[kFcT] = pt;
+    }
+}
+
+// A consumer warp's share of a fold: its 8 rows cw + 8 v (v < VPT) of stage uu,
+// held in hv, take the nrec records' rank-one updates s <- alpha_j s + beta_j
+// (v_j[r] - alpha_j (s . k_j)) k_j, oldest first, re-associated: with p_j =
+// s_c . k_j, d_j = s_j . k_j = a_j p_j + sum_{i<j} C_ij e_i and e_j = beta_j
+// (v_j[r] - alpha_j d_j), the folded row is A s_c + sum_j e_j g_j k_j (fc holds
+// C, a, g, A).  Rows no longer wait on one another's reductions record by
+// record; the state is rounded once.  The rows are stored to ck4 (the stage's
+// first row in the cache); sf is the warp's [16][8] scratch.
+template <int DK, int DV, int VPT>
+__device__ __forceinline__ void gdn_fold_stage(float4 (&hv)[VPT], int nrec, const uint16_t *r_k, const uint16_t *r_v,
+                                               const float *r_al, const float *r_be, const float *fc, float *sf,
+                                               int uu, int cw, float4 *ck4) {
+    constexpr int NC = 256, RSTEP = NC / (DK / 4);
+    const int lane = threadIdx.x & 31, col4 = lane, ctid = cw * 32 + lane;
+    // projections of the warp's 8 rows, 4 records at a time; after the
+    // reduction lane l holds row l / 4, record 4 q + l % 4
+    float pq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float t[VPT * 4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = q * 4 + jj;
+            float4 kj = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < nrec) {
+                const uint2 kraw = *reinterpret_cast<const uint2 *>(r_k + j * DK + col4 * 4);
+                kj = make_float4(bf16lo(kraw.x), bf16hi(kraw.x), bf16lo(kraw.y), bf16hi(kraw.y));
+            }
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                float d = hv[v].x * kj.x;
+                d = fmaf(hv[v].y, kj.y, d);
+                d = fmaf(hv[v].z, kj.z, d);
+                d = fmaf(hv[v].w, kj.w, d);
+                t[v * 4 + jj] = d;
+            }
+        }
+        group_reduce<32, VPT * 4>(t);
+        pq[q] = t[0];
+    }
+    // each lane of a quad gathers its row's projections and runs the recurrence
+    float p[kGdnMaxRec];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int src = 0; src < 4; ++src) p[q * 4 + src] = __shfl_sync(0xffffffffu, pq[q], (lane & ~3) + src);
+    const int vrow = lane >> 2, row = uu * kGdnRows + cw + RSTEP * vrow;
+    float acc[kGdnMaxRec], f[kGdnMaxRec];
+#pragma unroll
+    for (int m = 0; m < kGdnMaxRec; ++m) acc[m] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kGdnMaxRec; ++j) {
+        f[j] = 0.0f;
+        if (j < nrec) {
+            const float dj = fmaf(fc[kFcA + j], p[j], acc[j]);
+            const float ej = r_be[j] * fmaf(-r_al[j], dj, bf16_at(r_v, j * DV + row));
+            f[j] = ej * fc[kFcG + j];
+#pragma unroll
+            for (int m = j + 1; m < kGdnMaxRec; ++m) acc[m] = fmaf(fc[j * kGdnMaxRec + m], ej, acc[m]);
+        }
+    }
+    if ((lane & 3) == 0) {
+#pragma unroll
+        for (int j = 0; j < kGdnMaxRec; ++j) sf[j * 8 + vrow] = f[j];
+    }
+    __syncwarp();
+    // rank-nrec update, then the decayed state in one fma
+    unsigned long long acc01[VPT], acc23[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) acc01[v] = acc23[v] = 0ull;
+    for (int j = 0; j < nrec; ++j) {
+        const uint2 kraw = *reinterpret_cast<const uint2 *>(r_k + j * DK + col4 * 4);
+        const unsigned long long b01 = f2pack(bf16lo(kraw.x), bf16hi(kraw.x));
+        const unsigned long long b23 = f2pack(bf16lo(kraw.y), bf16hi(kraw.y));
+        const float4 fa = *reinterpret_cast<const float4 *>(sf + j * 8);
+        const float4 fb = *reinterpret_cast<const float4 *>(sf + j * 8 + 4);
+        const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const unsigned long long cc = f2pack(fv[v], fv[v]);
+            acc01[v] = fma2(cc, b01, acc01[v]);
+            acc23[v] = fma2(cc, b23, acc23[v]);
+        }
+    }
+    const unsigned long long tt = f2pack(fc[kFcT], fc[kFcT]);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        float4 o;
+        f2unpack(fma2(tt, f2pack(hv[v].x, hv[v].y), acc01[v]), o.x, o.y);
+        f2unpack(fma2(tt, f2pack(hv[v].z, hv[v].w), acc23[v]), o.z, o.w);
+        st_stream(ck4 + ctid + v * NC, o);
+    }
+    __syncwarp();                                        // sf is rewritten by the next stage
+}
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persistent(const GPArgs a) {
@@ -315,61 +469,7 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
 #pragma unroll
                 for (int m = 0; m < MV; ++m) s_rt[ib * DV + lane + 32 * m] = racc[m];
             }
-            if (work && ln + 1 >= L) {
-                // fold constants: C_ij = (k_i . k_j) prod_{i<m<j} alpha_m (i < j), the
-                // prefix products a_j = prod_{m<j} alpha_m, suffix products g_j =
-                // prod_{m>j} alpha_m and the total product A
-                const int nr = ln + 1;
-                float *fc = s_fc + ib * kFcStride;
-                // lane l: row i = l / 2 of the Gram matrix, columns j0 .. j0 + 7 (j0 = 8 (l % 2)),
-                // eight independent bf16-pair dot products over dk
-                {
-                    const int i = lane >> 1, j0 = (lane & 1) * 8;
-                    float g8[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) g8[q] = 0.0f;
-                    if (i < nr) {
-                        for (int cc = 0; cc < CK; ++cc) {
-                            const int c = (cc + (lane >> 1)) % CK;   // rows start on different chunks
-                            const uint4 ki = *reinterpret_cast<const uint4 *>(r_k + i * DK + c * 8);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const int j = j0 + q < nr ? j0 + q : i;
-                                const uint4 kj = *reinterpret_cast<const uint4 *>(r_k + j * DK + c * 8);
-                                float t = g8[q];
-                                t = fma_bf16_pair(ki.x, kj.x, t);
-                                t = fma_bf16_pair(ki.y, kj.y, t);
-                                t = fma_bf16_pair(ki.z, kj.z, t);
-                                t = fma_bf16_pair(ki.w, kj.w, t);
-                                g8[q] = t;
-                            }
-                        }
-                        // C_ij = K_ij prod_{i<m<j} alpha_m for j > i
-                        float pa = 1.0f;
-                        for (int m = i + 1; m < j0; ++m) pa *= r_al[m];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int j = j0 + q;
-                            if (j > i && j < nr) {
-                                fc[i * kGdnMaxRec + j] = g8[q] * pa;
-                                pa *= r_al[j];
-                            }
-                        }
-                    }
-                }
-                if (lane < nr) {
-                    float pa = 1.0f, pg = 1.0f;
-                    for (int m = 0; m < lane; ++m) pa *= r_al[m];
-                    for (int m = lane + 1; m < nr; ++m) pg *= r_al[m];
-                    fc[kFcA + lane] = pa;
-                    fc[kFcG + lane] = pg;
-                }
-                if (lane == 0) {
-                    float pt = 1.0f;
-                    for (int m = 0; m < nr; ++m) pt *= r_al[m];
-                    fc[kFcT] = pt;
-                }
-            }
+            if (work && ln + 1 >= L) gdn_fold_constants<DK>(s_fc + ib * kFcStride, r_k, r_al, ln + 1);
             __syncwarp();
             if (lane == 0) mbar_arrive(pfull + ib);      // item kk is prepared
         }
@@ -433,95 +533,10 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
                 const int row = uu * kGdnRows + cw + RSTEP * reduced_index<G4, VPT>(0);
                 a.o[bh * DV + row] = part[0] + rt[row];
             }
-            if (fold) {
-                // The L sequential rank-one updates of a row, re-associated: with
-                // p_j = s_c . k_j, d_j = s_j . k_j = a_j p_j + sum_{i<j} C_ij e_i and
-                // e_j = beta_j (v_j[r] - alpha_j d_j), the folded row is
-                // A s_c + sum_j e_j g_j k_j.  Rows no longer wait on one another's
-                // reductions record by record.
-                const float *fc = s_fc + ib * kFcStride;
-                float *sf = s_f + cw * (kGdnMaxRec * 8);
-                // projections of the warp's 8 rows, 4 records at a time; after the
-                // reduction lane l holds row l / 4, record 4 q + l % 4
-                float pq[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float t[VPT * 4];
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int j = q * 4 + jj;
-                        float4 kj = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (j < nrec) {
-                            const uint2 kraw = *reinterpret_cast<const uint2 *>(r_k + j * DK + col4 * 4);
-                            kj = make_float4(bf16lo(kraw.x), bf16hi(kraw.x), bf16lo(kraw.y), bf16hi(kraw.y));
-                        }
-#pragma unroll
-                        for (int v = 0; v < VPT; ++v) {
-                            float d = hv[v].x * kj.x;
-                            d = fmaf(hv[v].y, kj.y, d);
-                            d = fmaf(hv[v].z, kj.z, d);
-                            d = fmaf(hv[v].w, kj.w, d);
-                            t[v * 4 + jj] = d;
-                        }
-                    }
-                    group_reduce<32, VPT * 4>(t);
-                    pq[q] = t[0];
-                }
-                // each lane of a quad gathers its row's projections and runs the recurrence
-                float p[kGdnMaxRec];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                    for (int src = 0; src < 4; ++src) p[q * 4 + src] = __shfl_sync(0xffffffffu, pq[q], (lane & ~3) + src);
-                const int vrow = lane >> 2, row = uu * kGdnRows + cw + RSTEP * vrow;
-                float acc[kGdnMaxRec], f[kGdnMaxRec];
-#pragma unroll
-                for (int m = 0; m < kGdnMaxRec; ++m) acc[m] = 0.0f;
-#pragma unroll
-                for (int j = 0; j < kGdnMaxRec; ++j) {
-                    f[j] = 0.0f;
-                    if (j < nrec) {
-                        const float dj = fmaf(fc[kFcA + j], p[j], acc[j]);
-                        const float ej = r_be[j] * fmaf(-r_al[j], dj, bf16_at(r_v, j * DV + row));
-                        f[j] = ej * fc[kFcG + j];
-#pragma unroll
-                        for (int m = j + 1; m < kGdnMaxRec; ++m) acc[m] = fmaf(fc[j * kGdnMaxRec + m], ej, acc[m]);
-                    }
-                }
-                if ((lane & 3) == 0) {
-#pragma unroll
-                    for (int j = 0; j < kGdnMaxRec; ++j) sf[j * 8 + vrow] = f[j];
-                }
-                __syncwarp();
-                // rank-nrec update, then the decayed state in one fma
-                unsigned long long acc01[VPT], acc23[VPT];
-#pragma unroll
-                for (int v = 0; v < VPT; ++v) acc01[v] = acc23[v] = 0ull;
-                for (int j = 0; j < nrec; ++j) {
-                    const uint2 kraw = *reinterpret_cast<const uint2 *>(r_k + j * DK + col4 * 4);
-                    const unsigned long long b01 = f2pack(bf16lo(kraw.x), bf16hi(kraw.x));
-                    const unsigned long long b23 = f2pack(bf16lo(kraw.y), bf16hi(kraw.y));
-                    const float4 fa = *reinterpret_cast<const float4 *>(sf + j * 8);
-                    const float4 fb = *reinterpret_cast<const float4 *>(sf + j * 8 + 4);
-                    const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
-#pragma unroll
-                    for (int v = 0; v < VPT; ++v) {
-                        const unsigned long long cc = f2pack(fv[v], fv[v]);
-                        acc01[v] = fma2(cc, b01, acc01[v]);
-                        acc23[v] = fma2(cc, b23, acc23[v]);
-                    }
-                }
-                const unsigned long long tt = f2pack(fc[kFcT], fc[kFcT]);
-                float4 *ck4 = reinterpret_cast<float4 *>(a.ckpt + (cbh * DV + uu * kGdnRows) * DK);
-#pragma unroll
-                for (int v = 0; v < VPT; ++v) {
-                    float4 o;
-                    f2unpack(fma2(tt, f2pack(hv[v].x, hv[v].y), acc01[v]), o.x, o.y);
-                    f2unpack(fma2(tt, f2pack(hv[v].z, hv[v].w), acc23[v]), o.z, o.w);
-                    st_stream(ck4 + ctid + v * NC, o);
-                }
-                __syncwarp();                            // sf is rewritten by the next stage
-            }
+            if (fold)
+                gdn_fold_stage<DK, DV, VPT>(hv, nrec, r_k, r_v, r_al, r_be, s_fc + ib * kFcStride,
+                                            s_f + cw * (kGdnMaxRec * 8), uu, cw,
+                                            reinterpret_cast<float4 *>(a.ckpt + (cbh * DV + uu * kGdnRows) * DK));
         }
         __syncwarp();
         if (lane == 0) {

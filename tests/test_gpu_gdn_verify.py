@@ -143,6 +143,50 @@ def test_gdn_verify_b256_T4_sampled():
         r.verify(t, gen.accepted_counts(w.shape.batch, w.T, w.seed, t))
 
 
+@pytest.mark.parametrize("T,L", [(1, 4), (2, 8), (3, 16), (4, 4), (4, 16)])
+def test_gdn_persistent_verify_variants(T, L):
+    """The persistent verify (serving head shape, 12 sequences x 32 heads: more
+    items than twice the SMs): draft counts 1..4 and rings of 4..16 over 3 L
+    steps (pre-flushes included), accepted counts on 0..T, against the oracle's
+    causal scoring, the ring model and the draft records."""
+    shape = gen.GDNShape(batch=12, nheads=32, dk=128, dv=128, L=L)
+    r = GDNVerifyRun(shape, 900 + 10 * T + L, T, sample=[0, 5, 11])
+    for t in range(3 * L):
+        r.verify(t, gen.accepted_counts(shape.batch, T, 900 + T, t))
+
+
+def test_gdn_persistent_mixed_decode_verify():
+    """Persistent decodes (folding on their own schedule) and persistent verifies
+    with rollbacks interleaved on the same cache."""
+    shape = gen.GDNShape(batch=12, nheads=32, dk=128, dv=128, L=8)
+    r = GDNVerifyRun(shape, 57, 3, sample=[1, 10])
+    rng = np.random.default_rng(4)
+    for t in range(20):
+        if t % 3 == 2:
+            r.verify(t, rng.integers(0, 4, size=shape.batch).astype(np.int32))
+        else:
+            r.decode(t)
+
+
+def test_gdn_persistent_verify_bad_ring_pointers():
+    """A sequence with invalid ring pointers is flagged and left untouched by the
+    persistent verify; the other sequences proceed."""
+    from ssm_decode_state_gb300 import replayssm as rs
+    shape = gen.GDNShape(batch=12, nheads=32, dk=128, dv=128, L=8)
+    r = GDNVerifyRun(shape, 93, 2, sample=[0])
+    r.verify(0, np.full(shape.batch, 2, np.int32))
+    r.cache.ring_len[4] = 9                               # > L
+    before = r.cache.ckpt[4].clone()
+    rk = r.cache.rec_k[4].clone()
+    d = gen.gdn_draft_inputs(shape, 93, 1, 2)
+    rs.gdn_verify(r.cache, *r._dev(d))
+    torch.cuda.synchronize()
+    assert int(r.cache.err.item()) & rs.DEVERR_RING_META
+    assert r.cache.ring_len[4].item() == 9 and r.cache.ring_len[0].item() == 4
+    assert torch.equal(r.cache.ckpt[4], before) and torch.equal(r.cache.rec_k[4], rk)
+    assert not r.cache.arrive.any().item()
+
+
 def test_gdn_rollback_out_of_range():
     """An accepted count above T, or a ring too short to give back T - accepted
     records, leaves the sequence as it is and sets the rollback error bit."""

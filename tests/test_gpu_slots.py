@@ -412,9 +412,12 @@ def test_gdn_decode_through_slot_map(shape, capacity):
     _gdn_check(big, small, slots, before)
 
 
-def test_gdn_verify_rollback_flush_through_slot_map():
-    shape = gen.GDNShape(batch=4, nheads=4, dk=64, dv=64, L=8)
-    rs, big, small, slots, S0 = _gdn_pair(shape, 9, 41)
+@pytest.mark.parametrize("shape,capacity", [
+    (gen.GDNShape(batch=4, nheads=4, dk=64, dv=64, L=8), 9),          # per-tile verify
+    (gen.GDNShape(batch=16, nheads=32, dk=128, dv=128, L=8), 24),     # persistent verify
+], ids=["per_tile", "persistent"])
+def test_gdn_verify_rollback_flush_through_slot_map(shape, capacity):
+    rs, big, small, slots, S0 = _gdn_pair(shape, capacity, 41)
     fol = _GDNFollow(shape, S0, slots)                     # every row
     row_of = {int(sl): r for r, sl in enumerate(slots)}
     before = {f: getattr(big, f).clone() for f in GDN_FIELDS}
@@ -431,7 +434,7 @@ def test_gdn_verify_rollback_flush_through_slot_map():
         fol.verify(t, d, row_of, o, acc_np)
         fol.check(big)
         if t % 3 == 2:
-            mask_np = np.array([1, 0, 1, 1], np.uint8)
+            mask_np = (np.arange(shape.batch) % 4 != 1).astype(np.uint8)
             mask = torch.from_numpy(mask_np).cuda()
             rs.gdn_flush(big, mask)
             rs.gdn_flush(small, mask)

@@ -631,7 +631,7 @@ rssm_status launch(void *k, const rssm_gdn_dims *d, GArgs &a, const TileGeom &g,
 rssm_status launch_verify_persistent(const rssm_gdn_dims *d, const rssm_gdn_cache *c, int T, const uint16_t *q,
                                      const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
                                      float *o, cudaStream_t st) {
-    if (d->dk != 128 || d->dv != 128 || d->L > kGdnMaxRec || T > kGdnVT) return RSSM_ERR_UNSUPPORTED;
+    if (d->dk != 128 || d->dv != 128 || d->L > kGdnMaxL || T > kGdnVT) return RSSM_ERR_UNSUPPORTED;
     const int sms = sm_count();
     const long long items = (long long)d->batch * d->nheads;
     if (items < 2LL * sms || items > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;
@@ -667,7 +667,7 @@ rssm_status launch_verify_persistent(const rssm_gdn_dims *d, const rssm_gdn_cach
 rssm_status launch_persistent(const rssm_gdn_dims *d, const rssm_gdn_cache *c, const uint16_t *q,
                               const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
                               float *o, cudaStream_t st) {
-    if (d->dk != 128 || d->dv != 128 || d->L > kGdnMaxRec) return RSSM_ERR_UNSUPPORTED;
+    if (d->dk != 128 || d->dv != 128 || d->L > kGdnMaxL) return RSSM_ERR_UNSUPPORTED;
     const int sms = sm_count();
     const long long items = (long long)d->batch * d->nheads;
     if (items < 2LL * sms || items > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;

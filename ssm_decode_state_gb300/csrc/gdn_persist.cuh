@@ -47,7 +47,9 @@ struct GPArgs {
 
 constexpr int kGdnRows = 64;     // state rows per stage
 constexpr int kGdnBufs = 4;      // prepared-item buffers
-constexpr int kGdnMaxRec = 16;   // records a fold takes (ring capacity L <= 16)
+constexpr int kGdnMaxL = 16;     // largest ring the persistent kernels take
+constexpr int kGdnMaxRec = 20;   // records a fold may take: L + 1 (a decode after a verify filled
+                                 // the ring folds L buffered records and its token), in fours
 // fold constants of a prepared item: C [16][16], a [16], g [16], A (floats)
 constexpr int kFcA = kGdnMaxRec * kGdnMaxRec, kFcG = kFcA + kGdnMaxRec, kFcT = kFcG + kGdnMaxRec;
 constexpr int kFcStride = kFcT + 4;
@@ -91,46 +93,30 @@ struct GPSmem {
 // Fold constants of nr records (the preparation warps' share of a fold): the
 // Gram entries C_ij = (k_i . k_j) prod_{i<m<j} alpha_m (i < j), the prefix
 // products a_j = prod_{m<j} alpha_m, the suffix products g_j = prod_{m>j}
-// alpha_m and the total product A, into fc (one warp, nr <= 16).
+// alpha_m and the total product A, into fc (one warp, nr <= kGdnMaxRec).
 template <int DK>
 __device__ __forceinline__ void gdn_fold_constants(float *fc, const uint16_t *r_k, const float *r_al, int nr) {
     constexpr int CK = DK / 8;                           // 16-byte chunks per k row
     const int lane = threadIdx.x & 31;
-    // lane l: row i = l / 2 of the Gram matrix, columns j0 .. j0 + 7 (j0 = 8 (l % 2)),
-    // eight independent bf16-pair dot products over dk
-    {
-        const int i = lane >> 1, j0 = (lane & 1) * 8;
-        float g8[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) g8[q] = 0.0f;
-        if (i < nr) {
-            for (int cc = 0; cc < CK; ++cc) {
-                const int c = (cc + (lane >> 1)) % CK;   // rows start on different chunks
-                const uint4 ki = *reinterpret_cast<const uint4 *>(r_k + i * DK + c * 8);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int j = j0 + q < nr ? j0 + q : i;
-                    const uint4 kj = *reinterpret_cast<const uint4 *>(r_k + j * DK + c * 8);
-                    float t = g8[q];
-                    t = fma_bf16_pair(ki.x, kj.x, t);
-                    t = fma_bf16_pair(ki.y, kj.y, t);
-                    t = fma_bf16_pair(ki.z, kj.z, t);
-                    t = fma_bf16_pair(ki.w, kj.w, t);
-                    g8[q] = t;
-                }
-            }
-            // C_ij = K_ij prod_{i<m<j} alpha_m for j > i
-            float pa = 1.0f;
-            for (int m = i + 1; m < j0; ++m) pa *= r_al[m];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int j = j0 + q;
-                if (j > i && j < nr) {
-                    fc[i * kGdnMaxRec + j] = g8[q] * pa;
-                    pa *= r_al[j];
-                }
-            }
+    // the Gram entries of the pairs i < j, one pair per lane and pass: a dot product of
+    // two bf16 rows (bf16-pair FMAs), times the product of the alphas between them;
+    // lanes start on different 16-byte chunks of their rows
+    for (int pidx = lane; pidx < nr * nr; pidx += 32) {
+        const int i = pidx / nr, j = pidx - i * nr;
+        if (i >= j) continue;
+        float t = 0.0f;
+        for (int cc = 0; cc < CK; ++cc) {
+            const int c = (cc + lane) % CK;
+            const uint4 ki = *reinterpret_cast<const uint4 *>(r_k + i * DK + c * 8);
+            const uint4 kj = *reinterpret_cast<const uint4 *>(r_k + j * DK + c * 8);
+            t = fma_bf16_pair(ki.x, kj.x, t);
+            t = fma_bf16_pair(ki.y, kj.y, t);
+            t = fma_bf16_pair(ki.z, kj.z, t);
+            t = fma_bf16_pair(ki.w, kj.w, t);
         }
+        float pa = 1.0f;
+        for (int m = i + 1; m < j; ++m) pa *= r_al[m];
+        fc[i * kGdnMaxRec + j] = t * pa;
     }
     if (lane < nr) {
         float pa = 1.0f, pg = 1.0f;
@@ -162,9 +148,12 @@ __device__ __forceinline__ void gdn_fold_stage(float4 (&hv)[VPT], int nrec, cons
     const int lane = threadIdx.x & 31, col4 = lane, ctid = cw * 32 + lane;
     // projections of the warp's 8 rows, 4 records at a time; after the
     // reduction lane l holds row l / 4, record 4 q + l % 4
-    float pq[4];
+    constexpr int NQ = kGdnMaxRec / 4;
+    float pq[NQ];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NQ; ++q) {
+        pq[q] = 0.0f;
+        if (4 * q >= nrec) continue;                     // warp-uniform
         float t[VPT * 4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -189,7 +178,7 @@ __device__ __forceinline__ void gdn_fold_stage(float4 (&hv)[VPT], int nrec, cons
     // each lane of a quad gathers its row's projections and runs the recurrence
     float p[kGdnMaxRec];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < NQ; ++q)
 #pragma unroll
         for (int src = 0; src < 4; ++src) p[q * 4 + src] = __shfl_sync(0xffffffffu, pq[q], (lane & ~3) + src);
     const int vrow = lane >> 2, row = uu * kGdnRows + cw + RSTEP * vrow;

@@ -168,6 +168,21 @@ def test_gdn_persistent_mixed_decode_verify():
             r.decode(t)
 
 
+def test_gdn_persistent_decode_after_verify_fills_the_ring():
+    """A verify that leaves exactly L records (L = 16, no pre-flush) followed by a
+    persistent decode: the decode folds L + 1 records (the buffered ones and its
+    token); outputs and the later steps stay on the oracle."""
+    shape = gen.GDNShape(batch=12, nheads=32, dk=128, dv=128, L=16)
+    r = GDNVerifyRun(shape, 211, 4, sample=[0, 7, 11])
+    for t in range(12):                                  # 12 buffered records
+        r.decode(t)
+    r.verify(100, np.full(shape.batch, 4, np.int32))     # 12 + 4 = 16: no pre-flush, all accepted
+    assert r.cache.ring_len.cpu().tolist() == [16] * shape.batch
+    for t in range(12, 20):                              # the first of these folds 17 records
+        r.decode(t)
+    assert r.cache.ring_len.cpu().tolist() == [7] * shape.batch
+
+
 def test_gdn_persistent_verify_bad_ring_pointers():
     """A sequence with invalid ring pointers is flagged and left untouched by the
     persistent verify; the other sequences proceed."""

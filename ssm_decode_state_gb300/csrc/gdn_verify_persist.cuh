@@ -36,6 +36,18 @@ namespace rssm {
 
 constexpr int kGdnVT = 4;      // drafts a verify item holds in registers
 
+// Packed float32 pair product (the sm_100 two-wide multiply, each lane rounded
+// as a scalar multiply).
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// A bf16 pair (low element first) as a packed float32 pair (exact).
+__device__ __forceinline__ unsigned long long bf16x2_to_f2(uint32_t w) {
+    return f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 // Byte layout of the verify kernel's shared memory (KM = L + T records).
 struct GVPSmem {
     int stage_bytes, stages_off, full_off, empty_off, rfull_off, rempty_off, pfull_off, pempty_off;
@@ -283,54 +295,59 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_verify_persist
                 // of u(i) and rows 16 c .. 16 c + 15 of its record term: a step's dot product
                 // reduces over the chain's 8 lanes (3 shuffle levels).
                 const int ci = lane >> 3, c8 = lane & 7;
-                float u[16], racc[16];
+                // packed float32 pairs (columns / rows 2m, 2m + 1 of the lane's 16): the
+                // sm_100 two-wide fma, mul and add, each lane of a pair rounded as a scalar op
+                unsigned long long u2[8], racc2[8];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    u[m] = ci < T ? bf16_at(r_q, ci * DK + 16 * c8 + m) : 0.0f;
-                    racc[m] = 0.0f;
+                for (int m = 0; m < 8; ++m) {
+                    u2[m] = ci < T ? bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(r_q + ci * DK + 16 * c8 + 2 * m))
+                                   : 0ull;
+                    racc2[m] = 0ull;
                 }
                 for (int j = ln + T - 1; j >= 0; --j) {
                     const uint4 k0 = *reinterpret_cast<const uint4 *>(r_k + j * DK + 16 * c8);
                     const uint4 k1 = *reinterpret_cast<const uint4 *>(r_k + j * DK + 16 * c8 + 8);
                     const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-                    float kj[16];
+                    unsigned long long kj2[8];
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        kj[2 * m] = bf16lo(kw[m]);
-                        kj[2 * m + 1] = bf16hi(kw[m]);
-                    }
-                    float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
+                    for (int m = 0; m < 8; ++m) kj2[m] = bf16x2_to_f2(kw[m]);
+                    unsigned long long pa = 0ull, pb = 0ull;
 #pragma unroll
-                    for (int m = 0; m < 16; m += 4) {
-                        p0 = fmaf(kj[m], u[m], p0);
-                        p1 = fmaf(kj[m + 1], u[m + 1], p1);
-                        p2 = fmaf(kj[m + 2], u[m + 2], p2);
-                        p3 = fmaf(kj[m + 3], u[m + 3], p3);
+                    for (int m = 0; m < 8; m += 2) {
+                        pa = fma2(kj2[m], u2[m], pa);
+                        pb = fma2(kj2[m + 1], u2[m + 1], pb);
                     }
-                    float d = (p0 + p1) + (p2 + p3);
+                    float d0, d1, d2, d3;
+                    f2unpack(pa, d0, d1);
+                    f2unpack(pb, d2, d3);
+                    float d = (d0 + d2) + (d1 + d3);
                     d += __shfl_xor_sync(0xffffffffu, d, 1);
                     d += __shfl_xor_sync(0xffffffffu, d, 2);
                     d += __shfl_xor_sync(0xffffffffu, d, 4);
                     if (ci < T && j <= ln + ci) {                // chain ci has reached record j
                         const float cf = r_be[j] * d, al = r_al[j];
+                        const unsigned long long cf2 = f2pack(cf, cf), ncf2 = f2pack(-cf, -cf), al2 = f2pack(al, al);
                         const uint4 v0 = *reinterpret_cast<const uint4 *>(r_v + j * DV + 16 * c8);
                         const uint4 v1 = *reinterpret_cast<const uint4 *>(r_v + j * DV + 16 * c8 + 8);
                         const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
                         for (int m = 0; m < 8; ++m) {
-                            racc[2 * m] = fmaf(cf, bf16lo(vw[m]), racc[2 * m]);
-                            racc[2 * m + 1] = fmaf(cf, bf16hi(vw[m]), racc[2 * m + 1]);
+                            racc2[m] = fma2(cf2, bf16x2_to_f2(vw[m]), racc2[m]);
+                            u2[m] = mul2(al2, fma2(ncf2, kj2[m], u2[m]));
                         }
-#pragma unroll
-                        for (int m = 0; m < 16; ++m) u[m] = al * fmaf(-cf, kj[m], u[m]);
                     }
                 }
                 float4 *su = reinterpret_cast<float4 *>(s_u + (ib * TQ + ci) * DK + 16 * c8);
                 float4 *sr = reinterpret_cast<float4 *>(s_rt + (ib * TQ + ci) * DV + 16 * c8);
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    su[m] = make_float4(u[4 * m], u[4 * m + 1], u[4 * m + 2], u[4 * m + 3]);
-                    sr[m] = make_float4(racc[4 * m], racc[4 * m + 1], racc[4 * m + 2], racc[4 * m + 3]);
+                    float a0, a1, a2, a3, b0, b1, b2, b3;
+                    f2unpack(u2[2 * m], a0, a1);
+                    f2unpack(u2[2 * m + 1], a2, a3);
+                    f2unpack(racc2[2 * m], b0, b1);
+                    f2unpack(racc2[2 * m + 1], b2, b3);
+                    su[m] = make_float4(a0, a1, a2, a3);
+                    sr[m] = make_float4(b0, b1, b2, b3);
                 }
                 if (pre) gdn_fold_constants<DK>(s_fc + ib * kFcStride, r_k, r_al, ln);
             }

@@ -297,20 +297,6 @@ __device__ __forceinline__ void mma_f16_16x8x16(float &d0, float &d1, float &d2,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two E2M1 codes (low nibble first) -> their values as one f16 pair (exact).
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-    uint32_t h;
-    asm("{ .reg .b8 b0; cvt.u8.u32 b0, %1; cvt.rn.f16x2.e2m1x2 %0, b0; }" : "=r"(h) : "r"(byte));
-    return h;
-}
-
-// Lane-wise product of two f16 pairs, rounded to nearest.
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
 // acc + a.lo * c.lo + a.hi * c.hi: f16 pairs, products exact, FP32
 // accumulation (mixed-precision fma of sm_100 and later).
 __device__ __forceinline__ float fma_f16_pair(uint32_t a, uint32_t c, float acc) {

@@ -599,22 +599,26 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 }
             }
         } else if (nv4_item(hd, ln)) {
-            // NVFP4 codes, Q4 heads per stage, through the warp-level f16 MMA as on the
-            // FP8 path (same k order: lane (g, t) takes columns 32 t .. 32 t + 31 of
-            // rows g and g + 8 of each 16-row tile, 16 bytes of codes per row).  Codes
-            // become f16 pairs in hardware and are multiplied by their block's E4M3
-            // scale in f16 (a 2-bit times a 4-bit significand, between 2^-10 and 2688:
-            // exact), so the MMA's A holds code x block scale; C_t enters as f16 times
-            // 2^e (see the FP8 path) and the row scale comes after the reduction.
-            constexpr int MT = Q4 >= 2 ? Q4 / 2 : 1;       // 16-row tiles per warp and stage
-            const int g = lane >> 2, t4 = lane & 3;
+            // NVFP4 codes, Q4 heads per stage.  Lane (blk, rsub) takes the 16-column
+            // block blk = lane & 7 of rows rsub and rsub + 4 (rsub = lane >> 3) of the
+            // warp's 8 rows: its block sums need one block scale each, then the 8
+            // lanes of a row reduce them.  Codes become f16 pairs in hardware; C_t
+            // enters as f16 pairs times 2^e (prepared with the item, see the FP8
+            // path), products are exact, sums FP32 through the mixed-precision
+            // fma.rn.f32.f16; 2^-e comes off at the end.  (Through the warp-level MMA,
+            // with the block scales folded into A in f16, this step measured 85.9 us
+            // against 82-83 us for this form: the per-k-tile byte extraction and
+            // scale products cost more than the FMAs they replace.)
+            const int blk = lane & 7, rsub = lane >> 3;
+            // C_t as f16 x 2^e and e, prepared with the item: the block's column pairs
             const unsigned char *ch = s_ch + ia * (N * 2 + 16);
             const float cinv = pow2f(-*reinterpret_cast<const int *>(ch + N * 2));
-            uint32_t bf[16];                             // B fragments: [kt][0, 1]
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 w = g == 0 ? reinterpret_cast<const uint4 *>(ch)[t4 * 4 + q] : make_uint4(0u, 0u, 0u, 0u);
-                bf[4 * q] = w.x; bf[4 * q + 1] = w.y; bf[4 * q + 2] = w.z; bf[4 * q + 3] = w.w;
+            uint32_t cp[8];                              // pairs (2i, 2i + 1) of the block
+            {
+                const uint4 c0 = reinterpret_cast<const uint4 *>(ch)[2 * blk];
+                const uint4 c1 = reinterpret_cast<const uint4 *>(ch)[2 * blk + 1];
+                cp[0] = c0.x; cp[1] = c0.y; cp[2] = c0.z; cp[3] = c0.w;
+                cp[4] = c1.x; cp[5] = c1.y; cp[6] = c1.z; cp[7] = c1.w;
             }
             for (int uu = 0; uu < HPI / Q4; ++uu, ++u) {
                 const int s = u % S;
@@ -624,70 +628,48 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                 }
                 const unsigned char *stg = stages + s * lay.stage_bytes;
                 const float *sc = reinterpret_cast<const float *>(stg + Q4 * HB4);
-                uint4 qv[MT][2];                         // 32 codes of rows g, g + 8 of each tile
-                uint32_t bsc[MT][2];                     // their two block scales (E4M3 bytes)
-                float rsv[MT][2];
+                uint2 qc[Q4][2];
+                uint32_t sbc[Q4][2];
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
+                for (int hq = 0; hq < Q4; ++hq) {
 #pragma unroll
-                    for (int hv2 = 0; hv2 < 2; ++hv2) {
-                        const int hq = 2 * mt + hv2, row = cw * VPT + g;
-                        if (hq < Q4) {
-                            const unsigned char *hb = stg + hq * HB4;
-                            qv[mt][hv2] = *reinterpret_cast<const uint4 *>(hb + row * (N / 2) + 16 * t4);
-                            bsc[mt][hv2] = *reinterpret_cast<const uint16_t *>(hb + P * N / 2 + row * (N / 16) + 2 * t4);
-                            rsv[mt][hv2] = sc[hq * P + row];
-                        } else {
-                            qv[mt][hv2] = make_uint4(0u, 0u, 0u, 0u);
-                            bsc[mt][hv2] = 0u;
-                            rsv[mt][hv2] = 0.0f;
-                        }
+                    for (int m = 0; m < 2; ++m) {
+                        const int row = cw * VPT + rsub + 4 * m;
+                        qc[hq][m] = *reinterpret_cast<const uint2 *>(stg + hq * HB4 + row * (N / 2) + blk * 8);
+                        sbc[hq][m] = stg[hq * HB4 + P * N / 2 + row * (N / 16) + blk];
                     }
+                }
+                // the row scale of the (head, row) this lane ends up with after the reduction
+                float rsv;
+                {
+                    const int vi = reduced_index<8, Q4 * 2>(0);
+                    rsv = sc[(vi >> 1) * P + cw * VPT + rsub + 4 * (vi & 1)];
                 }
                 __syncwarp();                            // the warp is done with the stage
                 if (lane == 0) mbar_arrive(empty + s);
                 if (!work) continue;
+                float part[Q4 * 2];
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    // block scales as f16 pairs (s, s): blocks 2t (k-tiles 0-3) and 2t + 1 (4-7)
-                    uint32_t sp[2][2];
+                for (int hq = 0; hq < Q4; ++hq) {
 #pragma unroll
-                    for (int hv2 = 0; hv2 < 2; ++hv2) {
-                        uint32_t lo, hi;
-                        e4m3x4_to_f16x2(bsc[mt][hv2], lo, hi);
-                        sp[hv2][0] = __byte_perm(lo, 0u, 0x1010);
-                        sp[hv2][1] = __byte_perm(lo, 0u, 0x3232);
+                    for (int m = 0; m < 2; ++m) {
+                        uint32_t pa[4], pb[4];
+                        e2m1x8_to_f16x2(qc[hq][m].x, pa);
+                        e2m1x8_to_f16x2(qc[hq][m].y, pb);
+                        float acc = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc = fma_f16_pair(pa[i], cp[i], acc);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc = fma_f16_pair(pb[i], cp[4 + i], acc);
+                        part[hq * 2 + m] = acc * e4m3_value(sbc[hq][m]);
                     }
-                    const uint32_t w0[4] = {qv[mt][0].x, qv[mt][0].y, qv[mt][0].z, qv[mt][0].w};
-                    const uint32_t w1[4] = {qv[mt][1].x, qv[mt][1].y, qv[mt][1].z, qv[mt][1].w};
-                    // two accumulator sets (even and odd k-tiles): two short dependent chains
-                    float dd[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-#pragma unroll
-                    for (int kt = 0; kt < 8; ++kt) {
-                        // k-tile kt: bytes 2 kt, 2 kt + 1 of the row's 16 (codes 4 kt .. 4 kt + 3)
-                        const uint32_t h0w = (w0[kt >> 1] >> (16 * (kt & 1))) & 0xffffu;
-                        const uint32_t h1w = (w1[kt >> 1] >> (16 * (kt & 1))) & 0xffffu;
-                        const int bi = kt >> 2;
-                        const uint32_t a0 = hmul2_u32(e2m1x2_to_f16x2(h0w & 0xffu), sp[0][bi]);
-                        const uint32_t a2 = hmul2_u32(e2m1x2_to_f16x2(h0w >> 8), sp[0][bi]);
-                        const uint32_t a1 = hmul2_u32(e2m1x2_to_f16x2(h1w & 0xffu), sp[1][bi]);
-                        const uint32_t a3 = hmul2_u32(e2m1x2_to_f16x2(h1w >> 8), sp[1][bi]);
-                        float (&dk)[4] = dd[kt & 1];
-                        mma_f16_16x8x16(dk[0], dk[1], dk[2], dk[3], a0, a1, a2, a3, bf[2 * kt], bf[2 * kt + 1]);
-                    }
-                    const float d0 = dd[0][0] + dd[1][0], d2 = dd[0][2] + dd[1][2];
-                    if (t4 == 0) {
-#pragma unroll
-                        for (int hv2 = 0; hv2 < 2; ++hv2) {
-                            const int hq = 2 * mt + hv2;
-                            if (hq < Q4) {
-                                const int hh = uu * Q4 + hq, row = cw * VPT + g;
-                                const float dsum = hv2 ? d2 : d0;
-                                a.y[((size_t)b * H + h0 + hh) * P + row] =
-                                    fmaf(dec[hh], (dsum * cinv) * rsv[mt][hv2], rt[hh * P + row]);
-                            }
-                        }
-                    }
+                }
+                group_reduce<8, Q4 * 2>(part);
+                if (reduced_writer<8, Q4 * 2>()) {
+                    const int vi = reduced_index<8, Q4 * 2>(0);
+                    const int hh = uu * Q4 + (vi >> 1), row = cw * VPT + rsub + 4 * (vi & 1);
+                    a.y[((size_t)b * H + h0 + hh) * P + row] =
+                        fmaf(dec[hh], (part[0] * cinv) * rsv, rt[hh * P + row]);
                 }
             }
         } else if (fp8_item(hd, ln)) {

@@ -5,11 +5,17 @@
 namespace rssm {
 
 rssm_status launch_decode_persistent_f16(const rssm_mamba2_dims *d, const M2Args &args, cudaStream_t st);
+rssm_status launch_decode_small(const rssm_mamba2_dims *d, const M2Args &args, cudaStream_t st);
 
 // Returns RSSM_ERR_UNSUPPORTED (without launching) when the shape is not one
 // the persistent kernel handles; the caller then uses the per-tile kernel.
+// Small batches of a float32 checkpoint without read copy take the single-pass
+// kernel (mamba2_small.cu), which gives the same bits.
 rssm_status launch_decode_persistent(const rssm_mamba2_dims *d, const M2Args &args, cudaStream_t st) {
-    return d->ckpt_f16 ? launch_decode_persistent_f16(d, args, st) : launch_decode_persistent_ck<0>(d, args, st);
+    if (d->ckpt_f16) return launch_decode_persistent_f16(d, args, st);
+    const rssm_status s = launch_decode_small(d, args, st);
+    if (s != RSSM_ERR_UNSUPPORTED) return s;
+    return launch_decode_persistent_ck<0>(d, args, st);
 }
 
 // The same launch with the bounded-wait test hook on (float32 checkpoints).

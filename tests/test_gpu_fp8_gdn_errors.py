@@ -173,7 +173,7 @@ def test_gdn_b256_sampled():
 def test_bad_ring_pointers_skip_sequence():
     from ssm_decode_state_gb300 import replayssm as rs
     from tests.m2_runner import M2Run
-    for b_, H, P in [(3, 8, 32), (64, 128, 64)]:          # per-tile and persistent kernels
+    for b_, H, P in [(3, 8, 32), (64, 128, 64), (4, 128, 64)]:   # per-tile, persistent, small-batch kernels
         shape = gen.Mamba2Shape(batch=b_, nheads=H, headdim=P, dstate=128 if P == 64 else 64,
                                 ngroups=2, L=8)
         h0 = gen.mamba2_random_state(shape, 5)

@@ -145,7 +145,8 @@ def _dev_step(st):
 @pytest.mark.parametrize("shape,capacity", [
     (gen.Mamba2Shape(batch=3, nheads=8, headdim=32, dstate=64, ngroups=2, L=4), 7),          # per-tile kernel
     (gen.Mamba2Shape(batch=48, nheads=128, headdim=64, dstate=128, ngroups=8, L=4), 80),     # persistent kernel
-], ids=["per_tile", "persistent"])
+    (gen.Mamba2Shape(batch=5, nheads=128, headdim=64, dstate=128, ngroups=8, L=4), 12),      # small-batch kernel
+], ids=["per_tile", "persistent", "small_batch"])
 def test_decode_through_slot_map(shape, capacity):
     rs, prm, big, small, slots, h0 = _pair(shape, capacity, 300 + capacity)
     rows = sorted({0, shape.batch // 2, shape.batch - 1})
@@ -224,12 +225,14 @@ def test_verify_rollback_flush_through_slot_map(shape, capacity, T):
     _check_same(big, small, slots, untouched=before)
 
 
-def test_slot_out_of_range_is_flagged_and_skipped():
+@pytest.mark.parametrize("batch", [32, 8], ids=["persistent", "small_batch"])
+def test_slot_out_of_range_is_flagged_and_skipped(batch):
     """A map entry outside [0, capacity) skips that row (nothing of the cache
     changes for it) and sets the slot error bit; the other rows proceed."""
-    shape = gen.Mamba2Shape(batch=32, nheads=128, headdim=64, dstate=128, ngroups=8, L=4)
+    shape = gen.Mamba2Shape(batch=batch, nheads=128, headdim=64, dstate=128, ngroups=8, L=4)
     rs, prm, big, small, slots, h0 = _pair(shape, 40, 17)
-    fol = _follow_rows(shape, prm, h0, slots, [0, 31])
+    last = batch - 1
+    fol = _follow_rows(shape, prm, h0, slots, [0, last])
     del h0
     bad = slots.copy()
     bad[5] = 40                                            # == capacity
@@ -240,7 +243,7 @@ def test_slot_out_of_range_is_flagged_and_skipped():
     torch.cuda.synchronize()
     assert int(big.err.item()) & rs.DEVERR_SLOT
     big.err.zero_()
-    fol.decode(0, st, {int(slots[0]): 0, int(slots[31]): 31}, y, big)   # the other rows proceed
+    fol.decode(0, st, {int(slots[0]): 0, int(slots[last]): last}, y, big)   # the other rows proceed
     s5 = int(slots[5])
     assert big.ring_len[s5].item() == 0 and torch.equal(big.ckpt[s5], before["ckpt"][s5])
     assert big.ring_len[int(slots[0])].item() == 1

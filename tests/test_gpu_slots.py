@@ -146,7 +146,8 @@ def _dev_step(st):
     (gen.Mamba2Shape(batch=3, nheads=8, headdim=32, dstate=64, ngroups=2, L=4), 7),          # per-tile kernel
     (gen.Mamba2Shape(batch=48, nheads=128, headdim=64, dstate=128, ngroups=8, L=4), 80),     # persistent kernel
     (gen.Mamba2Shape(batch=5, nheads=128, headdim=64, dstate=128, ngroups=8, L=4), 12),      # small-batch kernel
-], ids=["per_tile", "persistent", "small_batch"])
+    (gen.Mamba2Shape(batch=1, nheads=128, headdim=64, dstate=128, ngroups=8, L=4), 9),       # small-batch kernel, batch 1
+], ids=["per_tile", "persistent", "small_batch", "small_batch_1"])
 def test_decode_through_slot_map(shape, capacity):
     rs, prm, big, small, slots, h0 = _pair(shape, capacity, 300 + capacity)
     rows = sorted({0, shape.batch // 2, shape.batch - 1})

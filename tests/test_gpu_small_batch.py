@@ -1,14 +1,14 @@
 """The single-pass small-batch replay decode (batches up to 16 of the serving
 shape with a float32 checkpoint).
 
-Every sequence of batches 1, 3, 8 and 16 is followed by the oracle over 17
+Every sequence of batches 1, 3, 4, 8 and 16 is followed by the oracle over 17
 decode steps from staggered rings (each sequence takes one fused flush, ring
 runs wrap around the ring end): y at every step, the folded checkpoints, the
 appended records and the ring pointers exact, then a standalone flush.  A second
 test drives one cache at batch 32 (above the small-batch limit of 16: the
-persistent kernel) and a copy of it through four slot-mapped batch-8 calls per
-step (the small-batch kernel): both kernels form every sum in the same order, so
-outputs, checkpoints and records must agree bit for bit.
+persistent kernel) and a copy of it through slot-mapped calls of 8 or 4
+sequences per step (the small-batch kernel): both kernels form every sum in the
+same order, so outputs, checkpoints and records must agree bit for bit.
 """
 import numpy as np
 import pytest
@@ -30,7 +30,7 @@ def _serving(batch):
     return gen.Mamba2Shape(batch, s.nheads, s.headdim, s.dstate, s.ngroups, s.L, True), w.seed
 
 
-@pytest.mark.parametrize("batch", [1, 3, 8, 16])
+@pytest.mark.parametrize("batch", [1, 3, 4, 8, 16])
 def test_small_batch_every_sequence(batch):
     from ssm_decode_state_gb300 import replayssm as rs
     shape, seed = _serving(batch)
@@ -71,27 +71,28 @@ def test_small_batch_every_sequence(batch):
     assert_close(cache.ckpt.cpu().numpy(), orc.h, f"batch {batch} flushed checkpoints")
 
 
-def test_small_batch_matches_persistent_bit_for_bit():
+@pytest.mark.parametrize("chunk", [8, 4])
+def test_small_batch_matches_persistent_bit_for_bit(chunk):
     from ssm_decode_state_gb300 import replayssm as rs
     shape, seed = _serving(32)
     prm = gen.mamba2_params(shape, seed)
     h0 = torch.from_numpy(gen.mamba2_random_state(shape, seed)).cuda()
     A, D = torch.from_numpy(prm.A), torch.from_numpy(prm.D)
     dims32 = rs.mamba2_dims(32, shape.nheads, shape.headdim, shape.dstate, shape.ngroups, shape.L)
-    dims8 = rs.mamba2_dims(8, shape.nheads, shape.headdim, shape.dstate, shape.ngroups, shape.L)
+    dimsc = rs.mamba2_dims(chunk, shape.nheads, shape.headdim, shape.dstate, shape.ngroups, shape.L)
     whole = rs.mamba2_cache(dims32, A, D, ckpt=h0.clone())
-    parts = rs.mamba2_cache(dims8, A, D, ckpt=h0.clone(), capacity=32)
+    parts = rs.mamba2_cache(dimsc, A, D, ckpt=h0.clone(), capacity=32)
     lens, heads = _stagger(32, shape.L, shape.L - 1)
     _m2_prefill(whole, shape, prm, seed, lens, heads)
     _m2_prefill(parts, shape, prm, seed, lens, heads)
-    maps = [torch.arange(8 * i, 8 * i + 8, dtype=torch.int32).cuda() for i in range(4)]
+    maps = [torch.arange(c0, c0 + chunk, dtype=torch.int32).cuda() for c0 in range(0, 32, chunk)]
     for t in range(2 * shape.L + 1):
         dt, x, B, C = _dev(gen.mamba2_step_inputs(shape, prm, seed, t))
         y32 = rs.decode(whole, dt, x, B, C)
-        y8 = torch.cat([rs.decode(parts, dt[8 * i:8 * i + 8].contiguous(), x[8 * i:8 * i + 8].contiguous(),
-                                  B[8 * i:8 * i + 8].contiguous(), C[8 * i:8 * i + 8].contiguous(), slots=m)
+        yc = torch.cat([rs.decode(parts, *(v[chunk * i:chunk * i + chunk].contiguous() for v in (dt, x, B, C)),
+                                  slots=m)
                         for i, m in enumerate(maps)])
-        assert torch.equal(y32, y8), f"y differs at step {t}"
+        assert torch.equal(y32, yc), f"y differs at step {t}"
     for f in FIELDS:
         assert torch.equal(getattr(whole, f), getattr(parts, f)), f
     assert int(whole.err.item()) == 0 and int(parts.err.item()) == 0

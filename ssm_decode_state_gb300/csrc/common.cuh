@@ -297,6 +297,27 @@ __device__ __forceinline__ void mma_f16_16x8x16(float &d0, float &d1, float &d2,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A B for one 16 x 8 x 32 tile of E4M3 operands: the warp-level MMA, FP32
+// accumulation.  Each register holds 4 consecutive k of one row of A or one
+// column of B: a0 rows g, a1 rows g + 8, k = 4t .. 4t + 3; a2 / a3 the same rows
+// at k + 16; b0 column g, k = 4t .. 4t + 3, b1 k + 16; D as for m16n8k16 (g =
+// lane / 4, t = lane % 4).  Products of E4M3 values are exact in FP32.
+__device__ __forceinline__ void mma_e4m3_16x8x32(float &d0, float &d1, float &d2, float &d3, uint32_t a0,
+                                                 uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four floats -> four E4M3 codes (byte k = value k), round to nearest even,
+// saturating to the largest finite code, by the hardware conversion.
+__device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float v0, float v1, float v2, float v3) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v2, v3), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
 // acc + a.lo * c.lo + a.hi * c.hi: f16 pairs, products exact, FP32
 // accumulation (mixed-precision fma of sm_100 and later).
 __device__ __forceinline__ float fma_f16_pair(uint32_t a, uint32_t c, float acc) {

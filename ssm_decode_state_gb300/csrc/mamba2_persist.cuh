@@ -485,8 +485,38 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             // itself and the record warp can run further ahead
             if (lane < N / 8)
                 reinterpret_cast<uint4 *>(s_cq + ia * N)[lane] = reinterpret_cast<const uint4 *>(r_C)[lane];
-            if constexpr (RC != 0) {
-                // for the read-copy MMA: C_t as f16 pairs times 2^e, e set from the item's
+            if constexpr (RC == 1) {
+                // for the FP8 read path's E4M3 MMA: C_t 2^e as two E4M3 terms, hi = the
+                // nearest E4M3 and lo = the nearest to 16 (C_t 2^e - hi), e set from the
+                // item's largest |C_t| so that it lands in [2^7, 2^8) (E4M3 reaches 448).
+                // A bf16 value within 2^-14 of that largest one is hi + lo / 16 exactly
+                // (8 significant bits in two 4-bit terms); smaller ones keep an absolute
+                // error below max|C_t| 2^-21.  Then e itself.
+                static_assert(N == 128, "4 columns per lane");
+                float cv[4], cmax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    cv[i] = bf16_at(r_C, lane * 4 + i);
+                    cmax = fmaxf(cmax, fabsf(cv[i]));
+                }
+                cmax = group_max<32>(cmax);
+                const int ce = cmax > 0.0f ? min(max(7 - ilogbf(cmax), -120), 120) : 0;
+                const float cs = pow2f(ce);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) cv[i] *= cs;
+                const uint32_t hw = f32x4_to_e4m3x4(cv[0], cv[1], cv[2], cv[3]);
+                uint32_t h01, h23;
+                e4m3x4_to_f16x2(hw, h01, h23);
+                const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
+                const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
+                const uint32_t lw = f32x4_to_e4m3x4((cv[0] - v01.x) * 16.0f, (cv[1] - v01.y) * 16.0f,
+                                                    (cv[2] - v23.x) * 16.0f, (cv[3] - v23.y) * 16.0f);
+                unsigned char *ch = s_ch + ia * (N * 2 + 16);
+                reinterpret_cast<uint32_t *>(ch)[lane] = hw;
+                reinterpret_cast<uint32_t *>(ch + N)[lane] = lw;
+                if (lane == 0) *reinterpret_cast<int *>(ch + N * 2) = ce;
+            } else if constexpr (RC == 2) {
+                // for the NVFP4 read path: C_t as f16 pairs times 2^e, e set from the item's
                 // largest |C_t| so that it lands just below 2^15 (exact and overflow-free;
                 // only values below max|C_t| 2^-29 lose bits), and e itself
                 static_assert(N == 128, "4 columns per lane");
@@ -675,26 +705,27 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
         } else if (fp8_item(hd, ln)) {
             // FP8 codes, Q8 heads per stage: a warp's rows of the stage are its 8 rows of
             // each of the Q8 heads, and their products with C_t go through the warp-level
-            // f16 MMA (m16n8k16, FP32 accumulation) as a matrix-vector product: the codes
-            // are A (rows x dstate; every E4M3 value is exact in f16, converted in
-            // hardware), C_t is column 0 of B, the other columns zero.  One MMA replaces
-            // 256 scalar multiply-adds; the SIMT form of this product was bound by
-            // instruction issue.  dstate is the MMA's reduction axis, so its order is
-            // free: lane (g, t) = (lane >> 2, lane & 3) takes the 32 consecutive codes
-            // 32 t .. 32 t + 31 of rows g and g + 8 of each 16-row tile, and k-tile kt
-            // reads their bytes 4 kt .. 4 kt + 3 (two 16-byte loads per row); lanes
-            // 0-3 hold C_t (as f16 times 2^e, prepared with the item) in the same order,
-            // which is the natural order of its column pairs.  Products are exact;
-            // 2^-e comes off at the end.
+            // E4M3 MMA (m16n8k32, FP32 accumulation) as a matrix-vector product: the codes
+            // are A as they are stored (rows x dstate, no conversion), C_t 2^e is column 0
+            // of B as two E4M3 terms hi + lo / 16 (prepared with the item), the other
+            // columns zero; products are exact.  dstate is the MMA's reduction axis, so
+            // its order is free: lane (g, t) = (lane >> 2, lane & 3) takes the 32
+            // consecutive codes 32 t .. 32 t + 31 of rows g and g + 8 of each 16-row
+            // tile, and k-tile kt reads their bytes 8 kt .. 8 kt + 7 (a0 / a1 the first
+            // four, a2 / a3 the next four); lanes 0-3 hold C_t's terms in the same order.
+            // 2^-e comes off at the end.  (Through the f16 MMA, each group of four codes
+            // first took two conversions: the consumers' instructions bound the step.)
             constexpr int MT = Q8 >= 2 ? Q8 / 2 : 1;       // 16-row tiles per warp and stage
             const int g = lane >> 2, t4 = lane & 3;
             const unsigned char *ch = s_ch + ia * (N * 2 + 16);
             const float cinv = pow2f(-*reinterpret_cast<const int *>(ch + N * 2));
-            uint32_t bf[16];                             // B fragments: [kt][0, 1] = pairs 16 t + 2 kt + (0, 1)
+            uint32_t bh[8], bl[8];                       // B fragments: word 2 kt + (0, 1) of each term
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 w = g == 0 ? reinterpret_cast<const uint4 *>(ch)[t4 * 4 + q] : make_uint4(0u, 0u, 0u, 0u);
-                bf[4 * q] = w.x; bf[4 * q + 1] = w.y; bf[4 * q + 2] = w.z; bf[4 * q + 3] = w.w;
+            for (int q = 0; q < 2; ++q) {
+                const uint4 wh = g == 0 ? reinterpret_cast<const uint4 *>(ch)[t4 * 2 + q] : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 wl = g == 0 ? reinterpret_cast<const uint4 *>(ch + N)[t4 * 2 + q] : make_uint4(0u, 0u, 0u, 0u);
+                bh[4 * q] = wh.x; bh[4 * q + 1] = wh.y; bh[4 * q + 2] = wh.z; bh[4 * q + 3] = wh.w;
+                bl[4 * q] = wl.x; bl[4 * q + 1] = wl.y; bl[4 * q + 2] = wl.z; bl[4 * q + 3] = wl.w;
             }
             for (int uu = 0; uu < HPI / Q8; ++uu, ++u) {
                 const int s = u % S;
@@ -733,28 +764,24 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                                             qv[mt][0][1].x, qv[mt][0][1].y, qv[mt][0][1].z, qv[mt][0][1].w};
                     const uint32_t w1[8] = {qv[mt][1][0].x, qv[mt][1][0].y, qv[mt][1][0].z, qv[mt][1][0].w,
                                             qv[mt][1][1].x, qv[mt][1][1].y, qv[mt][1][1].z, qv[mt][1][1].w};
-                    // two accumulator sets (even and odd k-tiles): two short dependent chains
-                    float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f, d3 = 0.0f, e0 = 0.0f, e1 = 0.0f, e2 = 0.0f, e3 = 0.0f;
+                    // one accumulator set per term of C_t: two short dependent chains
+                    float dh0 = 0.0f, dh1 = 0.0f, dh2 = 0.0f, dh3 = 0.0f;
+                    float dl0 = 0.0f, dl1 = 0.0f, dl2 = 0.0f, dl3 = 0.0f;
 #pragma unroll
-                    for (int kt = 0; kt < 8; kt += 2) {
-                        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-                        e4m3x4_to_f16x2(w0[kt], a0, a2);     // row g: k-pairs (2t, 2t+1), (2t+8, 2t+9)
-                        e4m3x4_to_f16x2(w1[kt], a1, a3);     // row g + 8
-                        e4m3x4_to_f16x2(w0[kt + 1], c0, c2);
-                        e4m3x4_to_f16x2(w1[kt + 1], c1, c3);
-                        mma_f16_16x8x16(d0, d1, d2, d3, a0, a1, a2, a3, bf[2 * kt], bf[2 * kt + 1]);
-                        mma_f16_16x8x16(e0, e1, e2, e3, c0, c1, c2, c3, bf[2 * kt + 2], bf[2 * kt + 3]);
+                    for (int kt = 0; kt < 4; ++kt) {
+                        mma_e4m3_16x8x32(dh0, dh1, dh2, dh3, w0[2 * kt], w1[2 * kt], w0[2 * kt + 1], w1[2 * kt + 1],
+                                         bh[2 * kt], bh[2 * kt + 1]);
+                        mma_e4m3_16x8x32(dl0, dl1, dl2, dl3, w0[2 * kt], w1[2 * kt], w0[2 * kt + 1], w1[2 * kt + 1],
+                                         bl[2 * kt], bl[2 * kt + 1]);
                     }
-                    d0 += e0;
-                    d2 += e2;
-                    // column 0 of D: rows g (d0) and g + 8 (d2) in the lanes with t = 0
+                    // column 0 of D: rows g (dh0, dl0) and g + 8 (dh2, dl2) in the lanes with t = 0
                     if (t4 == 0) {
 #pragma unroll
                         for (int hv2 = 0; hv2 < 2; ++hv2) {
                             const int hq = 2 * mt + hv2;
                             if (hq < Q8) {
                                 const int hh = uu * Q8 + hq, row = cw * VPT + g;
-                                const float dsum = hv2 ? d2 : d0;
+                                const float dsum = hv2 ? fmaf(dl2, 0.0625f, dh2) : fmaf(dl0, 0.0625f, dh0);
                                 a.y[((size_t)b * H + h0 + hh) * P + row] =
                                     fmaf(dec[hh], (dsum * cinv) * rsv[mt][hv2], rt[hh * P + row]);
                             }

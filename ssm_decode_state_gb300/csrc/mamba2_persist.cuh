@@ -706,26 +706,26 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             // FP8 codes, Q8 heads per stage: a warp's rows of the stage are its 8 rows of
             // each of the Q8 heads, and their products with C_t go through the warp-level
             // E4M3 MMA (m16n8k32, FP32 accumulation) as a matrix-vector product: the codes
-            // are A as they are stored (rows x dstate, no conversion), C_t 2^e is column 0
-            // of B as two E4M3 terms hi + lo / 16 (prepared with the item), the other
-            // columns zero; products are exact.  dstate is the MMA's reduction axis, so
-            // its order is free: lane (g, t) = (lane >> 2, lane & 3) takes the 32
-            // consecutive codes 32 t .. 32 t + 31 of rows g and g + 8 of each 16-row
-            // tile, and k-tile kt reads their bytes 8 kt .. 8 kt + 7 (a0 / a1 the first
-            // four, a2 / a3 the next four); lanes 0-3 hold C_t's terms in the same order.
-            // 2^-e comes off at the end.  (Through the f16 MMA, each group of four codes
-            // first took two conversions: the consumers' instructions bound the step.)
+            // are A as they are stored (rows x dstate, no conversion), and C_t 2^e, as two
+            // E4M3 terms hi + lo / 16 (prepared with the item), is columns 0 (hi) and 1
+            // (lo) of B, the other columns zero: one MMA forms both terms' sums, and
+            // products are exact.  dstate is the MMA's reduction axis, so its order is
+            // free: lane (g, t) = (lane >> 2, lane & 3) takes the 32 consecutive codes
+            // 32 t .. 32 t + 31 of rows g and g + 8 of each 16-row tile, and k-tile kt
+            // reads their bytes 8 kt .. 8 kt + 7 (a0 / a1 the first four, a2 / a3 the
+            // next four); lanes 0-3 hold hi and lanes 4-7 lo in the same order.  2^-e
+            // comes off at the end.  (Through the f16 MMA, each group of four codes first
+            // took two conversions: the consumers' instructions bound the step; with a
+            // separate MMA per term the tensor pipe took ~10 us of a 78 us step.)
             constexpr int MT = Q8 >= 2 ? Q8 / 2 : 1;       // 16-row tiles per warp and stage
             const int g = lane >> 2, t4 = lane & 3;
             const unsigned char *ch = s_ch + ia * (N * 2 + 16);
             const float cinv = pow2f(-*reinterpret_cast<const int *>(ch + N * 2));
-            uint32_t bh[8], bl[8];                       // B fragments: word 2 kt + (0, 1) of each term
+            uint32_t bb[8];                              // B fragments: word 2 kt + (0, 1) of column g's term
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                const uint4 wh = g == 0 ? reinterpret_cast<const uint4 *>(ch)[t4 * 2 + q] : make_uint4(0u, 0u, 0u, 0u);
-                const uint4 wl = g == 0 ? reinterpret_cast<const uint4 *>(ch + N)[t4 * 2 + q] : make_uint4(0u, 0u, 0u, 0u);
-                bh[4 * q] = wh.x; bh[4 * q + 1] = wh.y; bh[4 * q + 2] = wh.z; bh[4 * q + 3] = wh.w;
-                bl[4 * q] = wl.x; bl[4 * q + 1] = wl.y; bl[4 * q + 2] = wl.z; bl[4 * q + 3] = wl.w;
+                const uint4 w = g < 2 ? reinterpret_cast<const uint4 *>(ch + g * N)[t4 * 2 + q] : make_uint4(0u, 0u, 0u, 0u);
+                bb[4 * q] = w.x; bb[4 * q + 1] = w.y; bb[4 * q + 2] = w.z; bb[4 * q + 3] = w.w;
             }
             for (int uu = 0; uu < HPI / Q8; ++uu, ++u) {
                 const int s = u % S;
@@ -764,17 +764,18 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
                                             qv[mt][0][1].x, qv[mt][0][1].y, qv[mt][0][1].z, qv[mt][0][1].w};
                     const uint32_t w1[8] = {qv[mt][1][0].x, qv[mt][1][0].y, qv[mt][1][0].z, qv[mt][1][0].w,
                                             qv[mt][1][1].x, qv[mt][1][1].y, qv[mt][1][1].z, qv[mt][1][1].w};
-                    // one accumulator set per term of C_t: two short dependent chains
-                    float dh0 = 0.0f, dh1 = 0.0f, dh2 = 0.0f, dh3 = 0.0f;
-                    float dl0 = 0.0f, dl1 = 0.0f, dl2 = 0.0f, dl3 = 0.0f;
+                    // two accumulator sets (even and odd k-tiles): two short dependent chains
+                    float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f, d3 = 0.0f, e0 = 0.0f, e1 = 0.0f, e2 = 0.0f, e3 = 0.0f;
 #pragma unroll
-                    for (int kt = 0; kt < 4; ++kt) {
-                        mma_e4m3_16x8x32(dh0, dh1, dh2, dh3, w0[2 * kt], w1[2 * kt], w0[2 * kt + 1], w1[2 * kt + 1],
-                                         bh[2 * kt], bh[2 * kt + 1]);
-                        mma_e4m3_16x8x32(dl0, dl1, dl2, dl3, w0[2 * kt], w1[2 * kt], w0[2 * kt + 1], w1[2 * kt + 1],
-                                         bl[2 * kt], bl[2 * kt + 1]);
+                    for (int kt = 0; kt < 4; kt += 2) {
+                        mma_e4m3_16x8x32(d0, d1, d2, d3, w0[2 * kt], w1[2 * kt], w0[2 * kt + 1], w1[2 * kt + 1],
+                                         bb[2 * kt], bb[2 * kt + 1]);
+                        mma_e4m3_16x8x32(e0, e1, e2, e3, w0[2 * kt + 2], w1[2 * kt + 2], w0[2 * kt + 3],
+                                         w1[2 * kt + 3], bb[2 * kt + 2], bb[2 * kt + 3]);
                     }
-                    // column 0 of D: rows g (dh0, dl0) and g + 8 (dh2, dl2) in the lanes with t = 0
+                    // columns 0 (hi) and 1 (lo) of D: rows g (d0, d1) and g + 8 (d2, d3) in
+                    // the lanes with t = 0
+                    const float dh0 = d0 + e0, dl0 = d1 + e1, dh2 = d2 + e2, dl2 = d3 + e3;
                     if (t4 == 0) {
 #pragma unroll
                         for (int hv2 = 0; hv2 < 2; ++hv2) {

@@ -98,7 +98,7 @@ struct PSmem {
         wx_off = o;    o += up(KM * P * 4, 16);             // [KM][P]  (rows owned per warp)
         wcb_off = o;   o += up(3 * HPI * KM * 4, 16);       // [3][HPI][KM]  w_j (B_j . C_t)
         cq_off = o;    o += up(3 * N * 2, 16);              // [3][N] C_t (bf16) of the item
-        ch_off = o;    o += up(3 * (N * 2 + 16), 16);       // [3] C_t as f16 x 2^e, then e (read copies)
+        ch_off = o;    o += up(3 * (N * 2 + 16), 16);       // [3] C_t for the read copies' products, then e
         sfx_off = o;   o += up(2 * HPI * (KM + 1) * 4, 16); // [2 warps][HPI][KM + 1] suffix sums (prep only)
         ad_off = o;    o += up(2 * H * 4, 16);              // A[H], D[H]
         flag_off = o;  o += 16;
@@ -633,8 +633,8 @@ m2_decode_persistent(const M2Args a, const PersistCfg pc) {
             // block blk = lane & 7 of rows rsub and rsub + 4 (rsub = lane >> 3) of the
             // warp's 8 rows: its block sums need one block scale each, then the 8
             // lanes of a row reduce them.  Codes become f16 pairs in hardware; C_t
-            // enters as f16 pairs times 2^e (prepared with the item, see the FP8
-            // path), products are exact, sums FP32 through the mixed-precision
+            // enters as f16 pairs times 2^e (prepared with the item), products are
+            // exact, sums FP32 through the mixed-precision
             // fma.rn.f32.f16; 2^-e comes off at the end.  (Through the warp-level MMA,
             // with the block scales folded into A in f16, this step measured 85.9 us
             // against 82-83 us for this form: the per-k-tile byte extraction and

@@ -85,6 +85,8 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
     constexpr int TQ = 4;                                // draft slots in registers (T <= 4)
     static_assert(G4 == 32, "a warp owns whole rows");
     static_assert(HPI * TQ == 32 && TQ * VPT == 32, "one (head, draft) pair per lane");
+    static_assert(HPI * TQ * 2 == kPrepThreads && HPI * (P / 8) == kPrepThreads,
+                  "one (head, draft, half) and one (head, 8 rows) per preparation thread");
     extern __shared__ __align__(128) unsigned char smraw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = a.L, H = a.H, G = a.G, hpg = a.hpg, T = a.T, KM = L + T;
@@ -301,20 +303,24 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             float *dec = s_decay + ia * HPI * T, *rt = s_rt + ia * HPI * T * P;
             float *wf = s_wf + ia * HPI * KM, *fdec = s_fdec + ia * HPI;
             if (work) {
-                // drafts' x and dt rows into the ring (per head, read by no other CTA)
+                // drafts' x and dt rows into the ring (per head, read by no other CTA): thread
+                // (head, draft, half) = (ptid / 8, ptid / 2 % 4, ptid % 2) copies half of the
+                // draft's x row, thread (head, draft) = (ptid / 4, ptid % 4) its dt word
                 const int hd2 = pre ? (hd + ln) % L : hd, ln2 = pre ? 0 : ln;
-                for (int idx = ptid; idx < HPI * T * CX + HPI * T; idx += kPrepThreads) {
-                    if (idx < HPI * T * CX) {
-                        const int hh = idx / (T * CX), rr = idx - hh * T * CX, i = rr / CX, c = rr - i * CX;
+                {
+                    const int hh = ptid >> 3, i = (ptid >> 1) & 3, half = ptid & 1;
+                    if (i < T) {
                         const size_t bh = (size_t)b * H + h0 + hh;
                         const int slot = (hd2 + ln2 + i) % L;
-                        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.rec_x) + (bh * L + slot) * P + c * 8) =
-                            *reinterpret_cast<const uint4 *>(r_x + (hh * KM + ln + i) * P + c * 8);
-                    } else {
-                        const int rr = idx - HPI * T * CX, hh = rr / T, i = rr - hh * T;
-                        const size_t bh = (size_t)b * H + h0 + hh;
-                        a.rec_dt[bh * L + (hd2 + ln2 + i) % L] = r_dt[hh * KM + ln + i];
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.rec_x) + (bh * L + slot) * P) +
+                                     half * (CX / 2);
+                        const uint4 *src = reinterpret_cast<const uint4 *>(r_x + (hh * KM + ln + i) * P) + half * (CX / 2);
+#pragma unroll
+                        for (int c = 0; c < CX / 2; ++c) dst[c] = src[c];
                     }
+                    const int hd_ = ptid >> 2, id_ = ptid & 3;
+                    if (ptid < HPI * TQ && id_ < T)
+                        a.rec_dt[((size_t)b * H + h0 + hd_) * L + (hd2 + ln2 + id_) % L] = r_dt[hd_ * KM + ln + id_];
                 }
                 // suffix sums of dt, newest first (suffix_sum's order): one pass per
                 // (head, draft) up to len + i gives that draft's S_ij and its decay;
@@ -376,55 +382,64 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             }
             prep_sync();                                 // suffix sums and B . C
             if (work) {
-                // query weights times B_j . C_i (valid pairs only), and the pre-flush fold weights
-                const int npairs = T * (ln + 1) + T * (T - 1) / 2;
-                for (int idx = ptid; idx < HPI * npairs; idx += kPrepThreads) {
-                    const int hh = idx / npairs;
-                    int i = 0, j = idx - hh * npairs;
-                    while (j >= ln + 1 + i) {
-                        j -= ln + 1 + i;
-                        ++i;
+                // query weights times B_j . C_i (valid pairs only: thread (head, draft, half)
+                // takes records j = half, half + 2, .. <= len + i), and the pre-flush fold
+                // weights (thread (head, part) records j = part, part + 8, .. < len)
+                {
+                    const int hh = ptid >> 3, i = (ptid >> 1) & 3, half = ptid & 1;
+                    if (i < T) {
+                        const float Ah = s_A[h0 + hh];
+                        const float *sf = s_sfx + (hh * T + i) * KM;
+                        float *wc = s_wcb + (hh * T + i) * KM;
+                        for (int j = half; j <= ln + i; j += 2) {
+                            const float wv = expf(Ah * sf[j]) * r_dt[hh * KM + j];
+                            wc[j] = wv * s_cb[i * KM + j];
+                        }
                     }
-                    const int e = (hh * T + i) * KM + j;
-                    const float wv = expf(s_A[h0 + hh] * s_sfx[e]) * r_dt[hh * KM + j];
-                    s_wcb[e] = wv * s_cb[i * KM + j];
-                }
-                if (pre) {
-                    for (int idx = ptid; idx < HPI * ln; idx += kPrepThreads) {
-                        const int hh = idx / ln, j = idx - hh * ln;
-                        wf[hh * KM + j] = expf(s_A[h0 + hh] * s_sff[hh * KM + j]) * r_dt[hh * KM + j];
+                    if (pre) {
+                        const int part = ptid & 7;
+                        for (int j = part; j < ln; j += 8)
+                            wf[hh * KM + j] = expf(s_A[h0 + hh] * s_sff[hh * KM + j]) * r_dt[hh * KM + j];
                     }
                 }
             }
             prep_sync();                                 // w (B . C)
             if (work) {
-                // record terms: 8 consecutive rows of one (head, draft) per thread
-                for (int o = ptid; o < HPI * T * (P / 8); o += kPrepThreads) {
-                    const int hi = o / (P / 8), r0 = (o - hi * (P / 8)) * 8, hh = hi / T, i = hi - hh * T;
-                    const uint16_t *xh = r_x + hh * KM * P + r0;
-                    const float *wc = s_wcb + hi * KM;
-                    float acc[8];
+                // record terms: 8 consecutive rows of one head per thread, for every draft
+                // (each x row loaded and converted once for the T drafts)
+                const int hh = ptid >> 3, r0 = (ptid & 7) * 8;
+                const uint16_t *xh = r_x + hh * KM * P + r0;
+                const float *wch = s_wcb + hh * T * KM;
+                float acc[TQ][8];
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) acc[v] = 0.0f;
-                    for (int j = 0; j <= ln + i; ++j) {
-                        const float c = wc[j];
-                        const uint4 xr = *reinterpret_cast<const uint4 *>(xh + j * P);
-                        acc[0] = fmaf(c, bf16lo(xr.x), acc[0]);
-                        acc[1] = fmaf(c, bf16hi(xr.x), acc[1]);
-                        acc[2] = fmaf(c, bf16lo(xr.y), acc[2]);
-                        acc[3] = fmaf(c, bf16hi(xr.y), acc[3]);
-                        acc[4] = fmaf(c, bf16lo(xr.z), acc[4]);
-                        acc[5] = fmaf(c, bf16hi(xr.z), acc[5]);
-                        acc[6] = fmaf(c, bf16lo(xr.w), acc[6]);
-                        acc[7] = fmaf(c, bf16hi(xr.w), acc[7]);
+                for (int i = 0; i < TQ; ++i) {
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) acc[i][v] = 0.0f;
+                }
+                for (int j = 0; j < ln + T; ++j) {
+                    const uint4 xr = *reinterpret_cast<const uint4 *>(xh + j * P);
+                    const float xv[8] = {bf16lo(xr.x), bf16hi(xr.x), bf16lo(xr.y), bf16hi(xr.y),
+                                         bf16lo(xr.z), bf16hi(xr.z), bf16lo(xr.w), bf16hi(xr.w)};
+#pragma unroll
+                    for (int i = 0; i < TQ; ++i) {
+                        if (i < T && j <= ln + i) {
+                            const float c = wch[i * KM + j];
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) acc[i][v] = fmaf(c, xv[v], acc[i][v]);
+                        }
                     }
-                    const uint4 xl = *reinterpret_cast<const uint4 *>(xh + (ln + i) * P);
-                    const float dh = s_D[h0 + hh];
-                    float4 *dst = reinterpret_cast<float4 *>(rt + hi * P + r0);
-                    dst[0] = make_float4(fmaf(dh, bf16lo(xl.x), acc[0]), fmaf(dh, bf16hi(xl.x), acc[1]),
-                                         fmaf(dh, bf16lo(xl.y), acc[2]), fmaf(dh, bf16hi(xl.y), acc[3]));
-                    dst[1] = make_float4(fmaf(dh, bf16lo(xl.z), acc[4]), fmaf(dh, bf16hi(xl.z), acc[5]),
-                                         fmaf(dh, bf16lo(xl.w), acc[6]), fmaf(dh, bf16hi(xl.w), acc[7]));
+                }
+                const float dh = s_D[h0 + hh];
+#pragma unroll
+                for (int i = 0; i < TQ; ++i) {
+                    if (i < T) {
+                        const uint4 xl = *reinterpret_cast<const uint4 *>(xh + (ln + i) * P);
+                        float4 *dst = reinterpret_cast<float4 *>(rt + (hh * T + i) * P + r0);
+                        dst[0] = make_float4(fmaf(dh, bf16lo(xl.x), acc[i][0]), fmaf(dh, bf16hi(xl.x), acc[i][1]),
+                                             fmaf(dh, bf16lo(xl.y), acc[i][2]), fmaf(dh, bf16hi(xl.y), acc[i][3]));
+                        dst[1] = make_float4(fmaf(dh, bf16lo(xl.z), acc[i][4]), fmaf(dh, bf16hi(xl.z), acc[i][5]),
+                                             fmaf(dh, bf16lo(xl.w), acc[i][6]), fmaf(dh, bf16hi(xl.w), acc[i][7]));
+                    }
                 }
             }
             __syncwarp();

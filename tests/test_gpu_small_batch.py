@@ -97,3 +97,43 @@ def test_small_batch_matches_persistent_bit_for_bit(chunk):
         assert torch.equal(getattr(whole, f), getattr(parts, f)), f
     assert int(whole.err.item()) == 0 and int(parts.err.item()) == 0
     assert not parts.arrive.any().item()
+
+
+@pytest.mark.parametrize("L,lens", [(32, [32, 31, 0]), (1, [1, 0])], ids=["L32_full_ring", "L1"])
+def test_small_batch_ring_extremes(L, lens):
+    """Ring lengths at the limits: L = 32 with a full ring (len = L, left by a
+    verify), so the decode folds L + 1 = 33 records (list position 32 in every
+    staging and weight array, a second pass of B . C), and L = 1, where every
+    decode folds.  Serving shape, small-batch kernel, against the oracle over a
+    few steps, then a standalone flush; ring pointers exact."""
+    from ssm_decode_state_gb300 import replayssm as rs
+    w = gen.workloads()["mamba2_b256"]
+    s = w.shape
+    batch = len(lens)
+    shape = gen.Mamba2Shape(batch, s.nheads, s.headdim, s.dstate, s.ngroups, L, True)
+    seed = w.seed + 1000 + L
+    prm = gen.mamba2_params(shape, seed)
+    h0 = gen.mamba2_random_state(shape, seed)
+    dims = rs.mamba2_dims(batch, shape.nheads, shape.headdim, shape.dstate, shape.ngroups, L)
+    cache = rs.mamba2_cache(dims, torch.from_numpy(prm.A), torch.from_numpy(prm.D),
+                            ckpt=torch.from_numpy(h0).cuda())
+    lens = np.array(lens)
+    heads = (np.arange(batch) * 7 + 3) % L
+    pre = _m2_prefill(cache, shape, prm, seed, lens, heads)
+    ring = _ring_model(lens, heads, L)
+    orc = Mamba2Stepwise(prm.A, prm.D, shape.ngroups, h0)
+    _m2_oracle_prefill(orc, pre, lens, np.arange(batch))
+    for t in range(3):
+        st = gen.mamba2_step_inputs(shape, prm, seed, t)
+        y = rs.decode(cache, *_dev(st))
+        folded = np.array([f is not None for f in ring.decode([t] * batch)])
+        _check_ring(cache, ring)
+        yo = orc.step(st.dt, st.x, st.B, st.C)
+        assert_close(y.cpu().numpy(), yo, f"L {L} y step {t}")
+        for b in np.nonzero(folded)[0]:
+            e = rel_err(cache.ckpt[int(b)].cpu().numpy(), orc.h[b])
+            assert e <= RTOL, f"L {L} folded checkpoint of seq {b} at step {t}: {e:.3e}"
+    rs.flush(cache)                                # fold what each sequence still buffers
+    ring.flush()
+    _check_ring(cache, ring)
+    assert_close(cache.ckpt.cpu().numpy(), orc.h, f"L {L} flushed checkpoints after 3 steps")

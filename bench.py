@@ -655,10 +655,23 @@ def measure_rows(rs, dev, steps, warmup, which=ROWS):
             alg += bm.gdn_replay_decode(gu, ln, sh.L) * sh.batch
             ln = 0 if ln + 1 >= sh.L else ln + 1
         ms = _timed(stream, lambda t: rs.gdn_decode(cache, *gp[t % 8], o=o), K)
+        assert int(cache.err.item()) == 0
+        # per-step split over two flush periods, each call (fold and decode kernels) between its own events
+        ln0 = int(cache.ring_len[0].item())
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * sh.L)]
+        for i, (s0, s1) in enumerate(evs):
+            s0.record(stream)
+            rs.gdn_decode(cache, *gp[i % 8], o=o)
+            s1.record(stream)
+        torch.cuda.synchronize(dev)
+        split = {"nonflush": [], "flush": []}
+        for i, (s0, s1) in enumerate(evs):
+            split["flush" if (ln0 + i) % sh.L == sh.L - 1 else "nonflush"].append(s0.elapsed_time(s1) * 1e3)
         ms_c = _timed(stream, lambda t: rs.gdn_conventional_decode(dims, state, *gp[t % 8], o=o), K)
         assert int(cache.err.item()) == 0
         out["gdn_decode_b256"] = {"us_per_step": round(ms * 1e3 / K, 1), "seq_tok_s": round(sh.batch * K / (ms / 1e3), 1),
                                   "alg_GBps": round(alg / (ms / 1e3) / 1e9, 1),
+                                  "step_us": {k: round(statistics.median(v), 1) for k, v in split.items()},
                                   "conventional_us_per_step": round(ms_c * 1e3 / K, 1),
                                   "replay_speedup": round(ms_c / ms, 3)}
     if "gdn_verify" in which:

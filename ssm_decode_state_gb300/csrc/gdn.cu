@@ -13,6 +13,7 @@
 // sum_j beta_j d_j v_j[r].  The flush folds the records into every row,
 // oldest first: s <- alpha_j s + beta_j (v_j[r] - alpha_j (s . k_j)) k_j.
 #include "common.cuh"
+#include "gdn_fold_tc.cuh"
 #include "gdn_verify_persist.cuh"
 #include "host_common.h"
 
@@ -692,6 +693,16 @@ rssm_status launch_persistent(const rssm_gdn_dims *d, const rssm_gdn_cache *c, c
     rssm_status s = ensure_smem((const void *)kern, smem);
     if (s != RSSM_OK) return s;
     void *params[] = {&a};
+    // the items that fold this step go to the tensor-core fold kernel first (it
+    // only reads the ring pointers); the decode kernel then skips them
+    if (max_my <= kFtMaxMy) {
+        const FTSmem flay(d->L, max_my);
+        void *fk = (void *)gdn_fold_tc<128, 128>;
+        if ((s = ensure_smem((const void *)fk, flay.total)) != RSSM_OK) return s;
+        a.skip_folds = 1;
+        if (cudaLaunchKernel(fk, dim3(grid), dim3(kFtThreads), params, flay.total, st) != cudaSuccess)
+            return RSSM_ERR_CUDA;
+    }
     if (cudaLaunchKernel(kern, dim3(grid), dim3(256 + 64 + kPrepThreads), params, smem, st) != cudaSuccess)
         return RSSM_ERR_CUDA;
     return launch_status();

@@ -43,6 +43,9 @@ struct GPArgs {
     const int32_t *slots;   // [batch] cache slot of each batch row; nullptr: row b uses slot b
     int cap;                // sequences the cache arrays hold
     int T;                  // drafts per sequence (verify only)
+    int skip_folds;         // decode: leave the items whose sequence folds this step to the
+                            // tensor-core fold kernel, launched just before (it writes their o
+                            // and checkpoint); the decode still commits their ring pointers
 };
 
 constexpr int kGdnRows = 64;     // state rows per stage
@@ -58,7 +61,7 @@ constexpr int kFcStride = kFcT + 4;
 struct GPSmem {
     int stage_bytes, stages_off, full_off, empty_off, rfull_off, rempty_off, pfull_off, pempty_off;
     int rk_off, rv_off, rq_off, ral_off, rbe_off, rec_bytes, rec_off;
-    int meta_off, u_off, rt_off, fc_off, f_off, flag_off, total;
+    int meta_off, list_off, u_off, rt_off, fc_off, f_off, flag_off, total;
     __host__ __device__ GPSmem(int DK, int DV, int L, int S, int RB, int MY) {
         const int KM = L + 1;
         auto up = [](int v, int a) { return (v + a - 1) / a * a; };
@@ -81,11 +84,12 @@ struct GPSmem {
         rec_bytes = up(rbe_off + KM * 4, 128);
         rec_off = o;  o += RB * rec_bytes;
         meta_off = o; o += up(MY * 12, 16);                 // [items of this CTA][head, len, cache slot]
+        list_off = o; o += up(MY * 4, 16);                  // the items this kernel works on, in order
         u_off = o;    o += up(kGdnBufs * DK * 4, 16);       // u_0 per prepared item
         rt_off = o;   o += up(kGdnBufs * DV * 4, 16);       // record term per prepared item
         fc_off = o;   o += up(kGdnBufs * kFcStride * 4, 16); // fold constants per prepared item
         f_off = o;    o += up(8 * kGdnMaxRec * 8 * 4, 16);  // fold coefficients, [warp][j][8 rows]
-        flag_off = o; o += 16;
+        flag_off = o; o += 16;                              // abort flag, number of listed items
         total = o;
     }
 };
@@ -252,6 +256,8 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
     float *s_fc = reinterpret_cast<float *>(smraw + lay.fc_off);
     float *s_f = reinterpret_cast<float *>(smraw + lay.f_off);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smraw + lay.flag_off);
+    int *s_nwork = reinterpret_cast<int *>(smraw + lay.flag_off + 4);
+    int *s_list = reinterpret_cast<int *>(smraw + lay.list_off);
 
     const int grid = gridDim.x;
     const int n_my = (a.items - (int)blockIdx.x + grid - 1) / grid;
@@ -306,8 +312,27 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
             a.arrive[sb] = 0;
         }
     }
-    __syncthreads();                                     // the only CTA-wide barrier
-    if (n_my <= 0) return;
+    __syncthreads();
+    // the items this kernel works on: all of them, or, when the fold kernel has
+    // taken the folding ones, the rest (items with bad ring pointers stay listed)
+    if (warp == 0) {
+        int n = 0;
+        for (int k0 = 0; k0 < n_my; k0 += 32) {
+            const int k = k0 + lane;
+            bool in = k < n_my;
+            if (in && a.skip_folds) {
+                const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
+                in = meta_bad(hd, ln) || ln + 1 < L;
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, in);
+            if (in) s_list[n + __popc(m & ((1u << lane) - 1u))] = k;
+            n += __popc(m);
+        }
+        if (lane == 0) *s_nwork = n;
+    }
+    __syncthreads();
+    const int n_work = *s_nwork;
+    if (n_work <= 0) return;
 
     if (warp == 0) {
         // ================================= tile warp ==================================
@@ -315,8 +340,8 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
         const uint64_t pol = l2_evict_first_policy();
         bool ok = true;
         int issued = 0;
-        for (int k = 0; k < n_my && ok; ++k) {
-            const size_t cbh = cb_of(k);                     // cache
+        for (int w = 0; w < n_work && ok; ++w) {
+            const size_t cbh = cb_of(s_list[w]);             // cache
             for (int uu = 0; uu < NU; ++uu) {
                 const int t = issued, s = t % S;
                 if (t >= S) ok = pwait(empty + s, (uint32_t)(((t / S) - 1) & 1), s_abort) && !*s_abort;
@@ -344,10 +369,10 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
     if (warp == 1) {
         // ================================ record warp =================================
         bool ok = true;
-        int k = 0;
-        for (; k < n_my; ++k) {
-            const int r = k % RB;
-            if (lane == 0 && k >= RB) ok = pwait(rempty + r, (uint32_t)(((k / RB) - 1) & 1), s_abort) && !*s_abort;
+        int w = 0;
+        for (; w < n_work; ++w) {
+            const int k = s_list[w], r = w % RB;
+            if (lane == 0 && w >= RB) ok = pwait(rempty + r, (uint32_t)(((w / RB) - 1) & 1), s_abort) && !*s_abort;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const size_t bh = (size_t)item_of(k), cbh = cb_of(k);    // inputs, cache
@@ -385,7 +410,7 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
         cp_async_wait_all();
         // the copies of the last items may still be in flight: wait (bounded)
         if (lane == 0)
-            for (int kk = k - RB < 0 ? 0 : k - RB; kk < k; ++kk) mbar_wait(rfull + kk % RB, (uint32_t)((kk / RB) & 1));
+            for (int kk = w - RB < 0 ? 0 : w - RB; kk < w; ++kk) mbar_wait(rfull + kk % RB, (uint32_t)((kk / RB) & 1));
         if (!ok && lane == 0) {
             *s_abort = 1;
             flag_error(a.err, RSSM_DEVERR_TIMEOUT);
@@ -397,13 +422,13 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
         // ============================ item-preparation warps ============================
         const int pw = warp - 2 - NC / 32;               // 0 or 1: even or odd items
         bool live = true;
-        for (int kk = pw; kk < n_my; kk += 2) {
-            const int r = kk % RB, ib = kk % kGdnBufs;
-            if (live && kk >= kGdnBufs && !pwait(pempty + ib, (uint32_t)(((kk / kGdnBufs) - 1) & 1), s_abort)) {
+        for (int w = pw; w < n_work; w += 2) {
+            const int kk = s_list[w], r = w % RB, ib = w % kGdnBufs;
+            if (live && w >= kGdnBufs && !pwait(pempty + ib, (uint32_t)(((w / kGdnBufs) - 1) & 1), s_abort)) {
                 live = false;
                 *s_abort = 1;
             }
-            if (live && !pwait(rfull + r, (uint32_t)((kk / RB) & 1), s_abort)) {
+            if (live && !pwait(rfull + r, (uint32_t)((w / RB) & 1), s_abort)) {
                 live = false;
                 *s_abort = 1;
             }
@@ -472,13 +497,13 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
     const int col4 = lane;                               // this lane's 4 columns
     bool live = true;
     int u = 0;                                           // stages consumed so far
-    for (int k = 0; k < n_my; ++k) {
-        const int r = k % RB, ib = k % kGdnBufs;
-        if (live && !pwait(pfull + ib, (uint32_t)((k / kGdnBufs) & 1), s_abort)) {
+    for (int w = 0; w < n_work; ++w) {
+        const int k = s_list[w], r = w % RB, ib = w % kGdnBufs;
+        if (live && !pwait(pfull + ib, (uint32_t)((w / kGdnBufs) & 1), s_abort)) {
             live = false;
             *s_abort = 1;
         }
-        if (live && !pwait(rfull + r, (uint32_t)((k / RB) & 1), s_abort)) {
+        if (live && !pwait(rfull + r, (uint32_t)((w / RB) & 1), s_abort)) {
             live = false;
             *s_abort = 1;
         }

@@ -676,11 +676,17 @@ rssm_status launch_persistent(const rssm_gdn_dims *d, const rssm_gdn_cache *c, c
     const int max_my = (int)((items + grid - 1) / grid);
     if (max_my > 4096) return RSSM_ERR_UNSUPPORTED;
     constexpr int RB = 4;                                // even: each preparation warp keeps its own buffers
+    // the folding items go to the tensor-core fold phase when its shared memory
+    // plan fits next to the per-item lists; otherwise the decode phase folds them
     int stages = 0;
     size_t smem = 0;
-    for (int s = 6; s >= 2; --s) {
-        const GPSmem lay(128, 128, d->L, s, RB, max_my);
-        if (lay.total <= 227 * 1024) { stages = s; smem = lay.total; break; }
+    bool fold_phase = max_my <= kFtMaxMy;
+    for (int pass = 0; pass < 2 && !stages; ++pass, fold_phase = false) {
+        for (int s = 6; s >= 2; --s) {
+            const GStepSmem lay(d->L, s, RB, max_my, fold_phase);
+            if (lay.total <= 227 * 1024) { stages = s; smem = lay.total; break; }
+        }
+        if (stages) break;
     }
     if (!stages) return RSSM_ERR_UNSUPPORTED;
     GPArgs a{};
@@ -689,20 +695,11 @@ rssm_status launch_persistent(const rssm_gdn_dims *d, const rssm_gdn_cache *c, c
     a.ring_head = c->ring_head; a.ring_len = c->ring_len; a.arrive = c->arrive; a.err = c->err;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.o = o;
     a.slots = c->slots; a.cap = cache_capacity(d, c);
+    a.skip_folds = fold_phase ? 1 : 0;
     void *kern = (void *)gdn_decode_persistent<128, 128>;
     rssm_status s = ensure_smem((const void *)kern, smem);
     if (s != RSSM_OK) return s;
     void *params[] = {&a};
-    // the items that fold this step go to the tensor-core fold kernel first (it
-    // only reads the ring pointers); the decode kernel then skips them
-    if (max_my <= kFtMaxMy) {
-        const FTSmem flay(d->L, max_my);
-        void *fk = (void *)gdn_fold_tc<128, 128>;
-        if ((s = ensure_smem((const void *)fk, flay.total)) != RSSM_OK) return s;
-        a.skip_folds = 1;
-        if (cudaLaunchKernel(fk, dim3(grid), dim3(kFtThreads), params, flay.total, st) != cudaSuccess)
-            return RSSM_ERR_CUDA;
-    }
     if (cudaLaunchKernel(kern, dim3(grid), dim3(256 + 64 + kPrepThreads), params, smem, st) != cudaSuccess)
         return RSSM_ERR_CUDA;
     return launch_status();

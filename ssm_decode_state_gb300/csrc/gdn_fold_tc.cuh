@@ -2,10 +2,11 @@
 // tensor cores (serving head shape dk = dv = 128, bf16 token inputs).
 //
 // A decode step whose sequence has L - 1 buffered records folds them and its
-// token into the checkpoint (Gated DeltaNet replay, flush).  This kernel takes
-// exactly those (sequence, head) items of the step, before the decode kernel
-// runs (which then skips them and commits every sequence's ring pointers): it
-// writes their output o = S_c u_0 + record term and their folded checkpoint.
+// token into the checkpoint (Gated DeltaNet replay, flush).  The step kernel at
+// the end of this file takes those (sequence, head) items in a first phase
+// (gdn_fold_phase: their output o = S_c u_0 + record term and their folded
+// checkpoint) and the others in a second one (gdn_decode_phase), over the same
+// shared memory.
 //
 // The fold is the re-associated one of the decode kernel's fused flush: with
 // p_j = s_c . k_j for the nrec records (token last), d_j = a_j p_j +
@@ -23,8 +24,8 @@
 // state about two units in the last place (measured), which the following
 // updates then amplify.
 //
-// One CTA per SM walks the static item list of the decode kernel and takes the
-// items that fold.  Warps:
+// In the fold phase each CTA takes the folding items of its static item list.
+// Warps:
 //  * compute warps 0-7: per item, read the state (64 KiB, staged by the load
 //    warp) into registers and write its three bf16 terms (the MMA's A
 //    operand), one 64-column K-block after the other so that the MMAs of the
@@ -56,18 +57,18 @@ constexpr int kFtRB = 2, kFtPB = 2;                      // record and prepared-
 // tensor-memory columns: P, the Gram matrix, U of F's first term, U of its other two
 constexpr int kFtCols = 512, kFtPCol = 0, kFtGCol = 32, kFtU1Col = 256, kFtU23Col = 384;
 constexpr int kFtURow = 24;                              // rows of the projection operand holding u_0's terms
-constexpr int kFtMaxMy = 512;                            // items per CTA the kernel takes
+constexpr int kFtMaxMy = 512;                            // items per CTA the fold phase takes
 // fold constants of a prepared item (floats): [20][20] the products of alpha
 // between two records, turned into C in place; per record {a_j, g_j, beta_j,
 // alpha_j}; the total product A
 constexpr int kFtRecC = kGdnMaxRec * kGdnMaxRec, kFtTot = kFtRecC + 4 * kGdnMaxRec, kFtFcStride = kFtTot + 4;
 
-// Byte layout of the fold kernel's shared memory (offsets from a 1024-byte
+// Byte layout of the fold phase's shared memory (offsets from a 1024-byte
 // aligned base).
 struct FTSmem {
     int stage_off, planes_off, pop_off, kt_off, rec_off, rec_bytes, rk_off, rv_off, rq_off, ral_off, rbe_off;
-    int u_off, rt_off, fc_off, meta_off, list_off, bar_off, misc_off, total;
-    __host__ __device__ FTSmem(int L, int MY) {
+    int u_off, rt_off, fc_off, bar_off, misc_off, total;
+    __host__ __device__ FTSmem(int L) {
         const int DK = 128, DV = 128, KM = L + 1;
         auto up = [](int v, int a) { return (v + a - 1) / a * a; };
         int o = 0;
@@ -85,31 +86,31 @@ struct FTSmem {
         u_off = o;      o += kFtPB * DK * 4;
         rt_off = o;     o += kFtPB * DV * 4;
         fc_off = o;     o += kFtPB * kFtFcStride * 4;
-        meta_off = o;   o += up(MY * 12, 16);             // [items of this CTA][head, len, cache slot]
-        list_off = o;   o += up(MY * 4, 16);              // the folding items, in order
         bar_off = o;    o += 20 * 8;
-        misc_off = o;   o += 16;                          // tensor-memory base, abort flag, fold count
-        total = o + 1024;                                 // room to align the base
+        misc_off = o;   o += 16;                          // tensor-memory base, abort flag
+        total = o;
     }
 };
 
+// The fold phase of a step: the nf folding items of s_list (indices into this
+// CTA's static item list; s_meta holds their ring pointers as read at kernel
+// start).  sm is the 1024-byte aligned base of the dynamic shared memory.
+// Every thread of the CTA calls it; warps from kFtThreads / 32 on only join
+// its barriers.
 template <int DK, int DV>
-__global__ void __launch_bounds__(kFtThreads, 1) gdn_fold_tc(const GPArgs a) {
+__device__ __forceinline__ void gdn_fold_phase(const GPArgs &a, unsigned char *sm, const int *s_meta,
+                                               const int *s_list, int nf) {
     static_assert(DK == 128 && DV == 128, "serving head shape");
-    extern __shared__ unsigned char ftraw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(ftraw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = a.L, H = a.H;
-    const FTSmem lay(L, a.max_my);
+    const FTSmem lay(L);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + lay.bar_off);
     uint64_t *sfull = bars + 0, *sempty = bars + 1, *rfull = bars + 2, *rempty = bars + 4, *pfull = bars + 6,
              *pempty = bars + 8, *opsP0 = bars + 10, *opsP1 = bars + 11, *mmaG = bars + 12, *mmaP = bars + 13,
              *opsU = bars + 14, *mmaU = bars + 15, *tdone = bars + 16;
+    constexpr int kFtBars = 17;
     uint32_t *s_taddr = reinterpret_cast<uint32_t *>(sm + lay.misc_off);
     volatile int *s_abort = reinterpret_cast<volatile int *>(sm + lay.misc_off + 4);
-    int *s_nfold = reinterpret_cast<int *>(sm + lay.misc_off + 8);
-    int *s_meta = reinterpret_cast<int *>(sm + lay.meta_off);
-    int *s_list = reinterpret_cast<int *>(sm + lay.list_off);
     float *s_u = reinterpret_cast<float *>(sm + lay.u_off);
     float *s_rt = reinterpret_cast<float *>(sm + lay.rt_off);
     float *s_fc = reinterpret_cast<float *>(sm + lay.fc_off);
@@ -118,7 +119,6 @@ __global__ void __launch_bounds__(kFtThreads, 1) gdn_fold_tc(const GPArgs a) {
     auto pop = [&](int pb) { return sm + lay.pop_off + pb * 8192; };
 
     const int grid = gridDim.x;
-    const int n_my = (a.items - (int)blockIdx.x + grid - 1) / grid;
     auto item_of = [&](int k) { return (int)blockIdx.x + k * grid; };   // item = b * H + h
 
     if (tid == 0) {
@@ -142,36 +142,6 @@ __global__ void __launch_bounds__(kFtThreads, 1) gdn_fold_tc(const GPArgs a) {
         *s_abort = 0;
         fence_mbar_init();
     }
-    // ring pointers of this CTA's items (read only: the decode kernel that
-    // follows commits them); an item folds when its sequence holds L - 1 records
-    for (int k = tid; k < n_my; k += blockDim.x) {
-        const int b = item_of(k) / H;
-        const int sb = a.slots ? __ldg(a.slots + b) : b;
-        int hd = -1, ln = 0;
-        if (sb >= 0 && sb < a.cap) {
-            hd = __ldcg(a.ring_head + sb);
-            ln = __ldcg(a.ring_len + sb);
-        }
-        const bool fold = hd >= 0 && hd < L && ln >= 0 && ln <= L && ln + 1 >= L;
-        s_meta[k * 3 + 0] = hd;
-        s_meta[k * 3 + 1] = fold ? ln : -1;
-        s_meta[k * 3 + 2] = sb;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int n = 0;
-        for (int k0 = 0; k0 < n_my; k0 += 32) {
-            const int k = k0 + lane;
-            const bool f = k < n_my && s_meta[k * 3 + 1] >= 0;
-            const unsigned m = __ballot_sync(0xffffffffu, f);
-            if (f) s_list[n + __popc(m & ((1u << lane) - 1u))] = k;
-            n += __popc(m);
-        }
-        if (lane == 0) *s_nfold = n;
-    }
-    __syncthreads();
-    const int nf = *s_nfold;
-    if (nf == 0) return;                                 // no sequence of this CTA folds this step
     if (warp == 10) {
         tc::tmem_alloc(s_taddr, kFtCols);
         tc::tmem_relinquish();
@@ -391,7 +361,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) gdn_fold_tc(const GPArgs a) {
         __syncwarp();
         tc::fence_after();
         tc::tmem_dealloc(taddr, kFtCols);
-    } else {
+    } else if (warp < 8) {
         // ================================ compute warps ================================
         // thread (cw, lane) holds rows cw + 16 v + 8 (lane / 16) (v < 8), columns
         // 4 (lane % 16) .. + 3 of each 64-column K-block
@@ -577,6 +547,111 @@ __global__ void __launch_bounds__(kFtThreads, 1) gdn_fold_tc(const GPArgs a) {
         if (lane == 0) mbar_arrive(tdone);
         if (ctid == 0 && !live) flag_error(a.err, RSSM_DEVERR_TIMEOUT);
     }
+    // the phase is over (its copies and MMAs have completed): its barriers give
+    // their memory back before the next phase lays out its own
+    __syncthreads();
+    if (tid == 0)
+        for (int b = 0; b < kFtBars; ++b) mbar_inval(bars + b);
+    __syncthreads();
+}
+
+// Shared memory of a step: the larger of the two phases' layouts, then the
+// per-item ring pointers and the two item lists (1024 bytes of slack to align
+// the base).
+struct GStepSmem {
+    int meta_off, flist_off, dlist_off, cnt_off, total;
+    __host__ __device__ GStepSmem(int L, int S, int RB, int MY, bool fold_phase) {
+        auto up = [](int v, int a) { return (v + a - 1) / a * a; };
+        int core = GPSmem(128, 128, L, S, RB).total;
+        if (fold_phase) {
+            const int f = FTSmem(L).total;
+            core = core > f ? core : f;
+        }
+        int o = up(core, 16);
+        meta_off = o;  o += up(MY * 12, 16);               // [items of this CTA][head, len, cache slot]
+        flist_off = o; o += up(MY * 4, 16);                // the folding items, in order
+        dlist_off = o; o += up(MY * 4, 16);                // the others, in order
+        cnt_off = o;   o += 16;
+        total = o + 1024;
+    }
+};
+
+// One decode step of the gated delta rule at the serving head shape (dk = dv =
+// 128, bf16 token inputs), with the fused flush: one CTA per SM, a static list
+// of (sequence, head) items per CTA.  The ring pointers of every item are read
+// once at kernel start; the thread that sees a sequence's last arrival commits
+// the new ones (every item of the sequence, in every CTA, has read them by
+// then).  With a.skip_folds, the items whose sequence folds run first in the
+// tensor-core fold phase, the rest in the decode phase; otherwise the decode
+// phase takes every item and folds on the CUDA cores.
+template <int DK, int DV>
+__global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persistent(const GPArgs a) {
+    extern __shared__ unsigned char gdraw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(gdraw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int L = a.L, H = a.H;
+    const GStepSmem lay(L, a.stages, a.recbufs, a.max_my, a.skip_folds != 0);
+    int *s_meta = reinterpret_cast<int *>(sm + lay.meta_off);
+    int *s_flist = reinterpret_cast<int *>(sm + lay.flist_off);
+    int *s_dlist = reinterpret_cast<int *>(sm + lay.dlist_off);
+    int *s_cnt = reinterpret_cast<int *>(sm + lay.cnt_off);
+    const int grid = gridDim.x;
+    const int n_my = (a.items - (int)blockIdx.x + grid - 1) / grid;
+    auto item_of = [&](int k) { return (int)blockIdx.x + k * grid; };   // item = b * H + h
+    auto meta_bad = [&](int hd, int ln) { return hd < 0 || hd >= L || ln < 0 || ln > L; };
+
+    for (int k = tid; k < n_my; k += blockDim.x) {
+        const int it = item_of(k), b = it / H;
+        const int sb = a.slots ? __ldg(a.slots + b) : b;     // the sequence's cache slot
+        if (sb < 0 || sb >= a.cap) {                         // skipped by every warp role
+            s_meta[k * 3 + 0] = -1;
+            s_meta[k * 3 + 1] = 0;
+            s_meta[k * 3 + 2] = 0;
+            if (it % H == 0) flag_error(a.err, RSSM_DEVERR_SLOT);
+            continue;
+        }
+        const int hd = __ldcg(a.ring_head + sb), ln = __ldcg(a.ring_len + sb);
+        s_meta[k * 3 + 0] = hd;
+        s_meta[k * 3 + 1] = ln;
+        s_meta[k * 3 + 2] = sb;
+        if (meta_bad(hd, ln) && it % H == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
+        __threadfence();
+        if (atomicAdd(a.arrive + sb, 1) == H - 1) {
+            __threadfence();
+            if (!meta_bad(hd, ln)) {
+                const bool fold = ln + 1 >= L;
+                a.ring_head[sb] = fold ? (hd + ln + 1) % L : hd;
+                a.ring_len[sb] = fold ? 0 : ln + 1;
+            }
+            a.arrive[sb] = 0;
+        }
+    }
+    __syncthreads();
+    // the two item lists (items with bad ring pointers go to the decode phase,
+    // which skips them)
+    if (warp == 0) {
+        int nf = 0, nd = 0;
+        for (int k0 = 0; k0 < n_my; k0 += 32) {
+            const int k = k0 + lane;
+            const int hd = k < n_my ? s_meta[k * 3 + 0] : 0, ln = k < n_my ? s_meta[k * 3 + 1] : 0;
+            const bool f = k < n_my && a.skip_folds && !meta_bad(hd, ln) && ln + 1 >= L;
+            const bool d = k < n_my && !f;
+            const unsigned mf = __ballot_sync(0xffffffffu, f), md = __ballot_sync(0xffffffffu, d);
+            const unsigned below = (1u << lane) - 1u;
+            if (f) s_flist[nf + __popc(mf & below)] = k;
+            if (d) s_dlist[nd + __popc(md & below)] = k;
+            nf += __popc(mf);
+            nd += __popc(md);
+        }
+        if (lane == 0) {
+            s_cnt[0] = nf;
+            s_cnt[1] = nd;
+        }
+    }
+    __syncthreads();
+    const int nf = s_cnt[0], nd = s_cnt[1];
+    if (nf > 0) gdn_fold_phase<DK, DV>(a, sm, s_meta, s_flist, nf);
+    if (nd > 0) gdn_decode_phase<DK, DV>(a, sm, s_meta, s_dlist, nd);
 }
 
 }  // namespace rssm

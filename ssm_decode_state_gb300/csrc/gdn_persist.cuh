@@ -43,9 +43,8 @@ struct GPArgs {
     const int32_t *slots;   // [batch] cache slot of each batch row; nullptr: row b uses slot b
     int cap;                // sequences the cache arrays hold
     int T;                  // drafts per sequence (verify only)
-    int skip_folds;         // decode: leave the items whose sequence folds this step to the
-                            // tensor-core fold kernel, launched just before (it writes their o
-                            // and checkpoint); the decode still commits their ring pointers
+    int skip_folds;         // decode: the items whose sequence folds this step go to the
+                            // tensor-core fold phase; 0: the decode phase folds them itself
 };
 
 constexpr int kGdnRows = 64;     // state rows per stage
@@ -57,12 +56,13 @@ constexpr int kGdnMaxRec = 20;   // records a fold may take: L + 1 (a decode aft
 constexpr int kFcA = kGdnMaxRec * kGdnMaxRec, kFcG = kFcA + kGdnMaxRec, kFcT = kFcG + kGdnMaxRec;
 constexpr int kFcStride = kFcT + 4;
 
-// Byte layout of the kernel's shared memory.
+// Byte layout of the decode phase's shared memory (the per-item ring pointers
+// and item lists live after it, in the step kernel's common region).
 struct GPSmem {
     int stage_bytes, stages_off, full_off, empty_off, rfull_off, rempty_off, pfull_off, pempty_off;
     int rk_off, rv_off, rq_off, ral_off, rbe_off, rec_bytes, rec_off;
-    int meta_off, list_off, u_off, rt_off, fc_off, f_off, flag_off, total;
-    __host__ __device__ GPSmem(int DK, int DV, int L, int S, int RB, int MY) {
+    int u_off, rt_off, fc_off, f_off, flag_off, total;
+    __host__ __device__ GPSmem(int DK, int DV, int L, int S, int RB) {
         const int KM = L + 1;
         auto up = [](int v, int a) { return (v + a - 1) / a * a; };
         stage_bytes = kGdnRows * DK * 4;
@@ -83,13 +83,11 @@ struct GPSmem {
         rbe_off = ral_off + up(KM * 4, 16);
         rec_bytes = up(rbe_off + KM * 4, 128);
         rec_off = o;  o += RB * rec_bytes;
-        meta_off = o; o += up(MY * 12, 16);                 // [items of this CTA][head, len, cache slot]
-        list_off = o; o += up(MY * 4, 16);                  // the items this kernel works on, in order
         u_off = o;    o += up(kGdnBufs * DK * 4, 16);       // u_0 per prepared item
         rt_off = o;   o += up(kGdnBufs * DV * 4, 16);       // record term per prepared item
         fc_off = o;   o += up(kGdnBufs * kFcStride * 4, 16); // fold constants per prepared item
         f_off = o;    o += up(8 * kGdnMaxRec * 8 * 4, 16);  // fold coefficients, [warp][j][8 rows]
-        flag_off = o; o += 16;                              // abort flag, number of listed items
+        flag_off = o; o += 16;                              // abort flag
         total = o;
     }
 };
@@ -234,15 +232,19 @@ __device__ __forceinline__ void gdn_fold_stage(float4 (&hv)[VPT], int nrec, cons
     __syncwarp();                                        // sf is rewritten by the next stage
 }
 
+// The decode phase of a step (see gdn_decode_persistent): the n_work items of
+// s_list (indices into this CTA's static item list; s_meta holds their ring
+// pointers as read at kernel start).  smraw is the 1024-byte aligned base of
+// the dynamic shared memory.
 template <int DK, int DV>
-__global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persistent(const GPArgs a) {
+__device__ __forceinline__ void gdn_decode_phase(const GPArgs &a, unsigned char *smraw, const int *s_meta,
+                                                 const int *s_list, int n_work) {
     constexpr int NC = 256, VPT = 8, G4 = DK / 4, RSTEP = NC / G4, NU = DV / kGdnRows;
     static_assert(G4 == 32 && NC * VPT * 4 == kGdnRows * DK && DV % kGdnRows == 0, "serving shape");
     constexpr int CK = DK / 8, CV = DV / 8;              // 16-byte chunks per k / v row
-    extern __shared__ __align__(128) unsigned char smraw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = a.L, H = a.H, S = a.stages, RB = a.recbufs;
-    const GPSmem lay(DK, DV, L, S, RB, a.max_my);
+    const GPSmem lay(DK, DV, L, S, RB);
     unsigned char *stages = smraw + lay.stages_off;
     uint64_t *full = reinterpret_cast<uint64_t *>(smraw + lay.full_off);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smraw + lay.empty_off);
@@ -250,17 +252,13 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
     uint64_t *rempty = reinterpret_cast<uint64_t *>(smraw + lay.rempty_off);
     uint64_t *pfull = reinterpret_cast<uint64_t *>(smraw + lay.pfull_off);
     uint64_t *pempty = reinterpret_cast<uint64_t *>(smraw + lay.pempty_off);
-    int *s_meta = reinterpret_cast<int *>(smraw + lay.meta_off);
     float *s_u = reinterpret_cast<float *>(smraw + lay.u_off);
     float *s_rt = reinterpret_cast<float *>(smraw + lay.rt_off);
     float *s_fc = reinterpret_cast<float *>(smraw + lay.fc_off);
     float *s_f = reinterpret_cast<float *>(smraw + lay.f_off);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smraw + lay.flag_off);
-    int *s_nwork = reinterpret_cast<int *>(smraw + lay.flag_off + 4);
-    int *s_list = reinterpret_cast<int *>(smraw + lay.list_off);
 
     const int grid = gridDim.x;
-    const int n_my = (a.items - (int)blockIdx.x + grid - 1) / grid;
     auto item_of = [&](int k) { return (int)blockIdx.x + k * grid; };   // item = b * H + h
     auto meta_bad = [&](int hd, int ln) { return hd < 0 || hd >= L || ln < 0 || ln > L; };
     auto rec = [&](int r) { return smraw + lay.rec_off + r * lay.rec_bytes; };
@@ -283,56 +281,7 @@ __global__ void __launch_bounds__(256 + 64 + kPrepThreads, 1) gdn_decode_persist
         *s_abort = 0;
         fence_mbar_init();
     }
-    // Ring pointers of every item of this CTA, read once; the thread that sees
-    // a sequence's last arrival commits the new ones (every item of the
-    // sequence, in every CTA, has read them by then).
-    for (int k = tid; k < n_my; k += blockDim.x) {
-        const int it = item_of(k), b = it / H;
-        const int sb = a.slots ? __ldg(a.slots + b) : b;     // the sequence's cache slot
-        if (sb < 0 || sb >= a.cap) {                         // skipped by every warp role
-            s_meta[k * 3 + 0] = -1;
-            s_meta[k * 3 + 1] = 0;
-            s_meta[k * 3 + 2] = 0;
-            if (it % H == 0) flag_error(a.err, RSSM_DEVERR_SLOT);
-            continue;
-        }
-        const int hd = __ldcg(a.ring_head + sb), ln = __ldcg(a.ring_len + sb);
-        s_meta[k * 3 + 0] = hd;
-        s_meta[k * 3 + 1] = ln;
-        s_meta[k * 3 + 2] = sb;
-        if (meta_bad(hd, ln) && it % H == 0) flag_error(a.err, RSSM_DEVERR_RING_META);
-        __threadfence();
-        if (atomicAdd(a.arrive + sb, 1) == H - 1) {
-            __threadfence();
-            if (!meta_bad(hd, ln)) {
-                const bool fold = ln + 1 >= L;
-                a.ring_head[sb] = fold ? (hd + ln + 1) % L : hd;
-                a.ring_len[sb] = fold ? 0 : ln + 1;
-            }
-            a.arrive[sb] = 0;
-        }
-    }
     __syncthreads();
-    // the items this kernel works on: all of them, or, when the fold kernel has
-    // taken the folding ones, the rest (items with bad ring pointers stay listed)
-    if (warp == 0) {
-        int n = 0;
-        for (int k0 = 0; k0 < n_my; k0 += 32) {
-            const int k = k0 + lane;
-            bool in = k < n_my;
-            if (in && a.skip_folds) {
-                const int hd = s_meta[k * 3 + 0], ln = s_meta[k * 3 + 1];
-                in = meta_bad(hd, ln) || ln + 1 < L;
-            }
-            const unsigned m = __ballot_sync(0xffffffffu, in);
-            if (in) s_list[n + __popc(m & ((1u << lane) - 1u))] = k;
-            n += __popc(m);
-        }
-        if (lane == 0) *s_nwork = n;
-    }
-    __syncthreads();
-    const int n_work = *s_nwork;
-    if (n_work <= 0) return;
 
     if (warp == 0) {
         // ================================= tile warp ==================================

@@ -411,3 +411,36 @@ def test_gdn_persistent_bad_ring_pointers():
     assert r.cache.ring_len[3].item() == 9
     assert torch.equal(r.cache.ckpt[3], before) and torch.equal(r.cache.rec_k[3], rk)
     assert r.cache.ring_len[0].item() == 2 and not r.cache.arrive.any().item()
+
+
+def test_gdn_cuda_core_fold_when_items_exceed_fold_plan():
+    """More than 512 (sequence, head) items per CTA (batch 2 with enough heads
+    for this GPU's SM count): the tensor-core fold phase's plan leaves no room
+    for the per-item lists, so the decode phase folds on the CUDA cores.  Ring
+    of 4, five decodes through a fused flush: outputs and folded checkpoints of
+    sampled heads against the oracle, ring pointers exact."""
+    from ssm_decode_state_gb300 import replayssm as rs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = (513 * sms + 1) // 2 + 1                      # ceil(2 H / sms) > 512
+    L, seed = 4, 919
+    shape = gen.GDNShape(batch=2, nheads=H, dk=128, dv=128, L=L)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    S0 = torch.randn(2, H, 128, 128, device="cuda", generator=g).mul_(0.1)
+    heads = np.array([0, 1, H // 2, H - 1])
+    oracle = GDNStepwise(S0[:, torch.from_numpy(heads).cuda()].cpu().numpy())
+    cache = rs.gdn_cache(rs.gdn_dims(2, H, 128, 128, L), ckpt=S0)
+    for t in range(L + 1):
+        st = gen.gdn_step_inputs(shape, seed, t)
+        o = rs.gdn_decode(cache, *(to_dev(a, torch.bfloat16) for a in (st.q, st.k, st.v)),
+                          to_dev(st.alpha), to_dev(st.beta))
+        sel = lambda a: a[:, heads]                   # noqa: E731
+        oo = oracle.step(sel(st.q), sel(st.k), sel(st.v), sel(st.alpha), sel(st.beta))
+        assert_close(o[:, torch.from_numpy(heads).cuda()].cpu().numpy(), oo, f"o step {t}", RTOL)
+        ln = (t + 1) % L
+        np.testing.assert_array_equal(cache.ring_len.cpu().numpy(), [ln, ln])
+        np.testing.assert_array_equal(cache.ring_head.cpu().numpy(), [0, 0])   # a full fold wraps to 0
+        assert int(cache.err.item()) == 0
+        if t == L - 1:                                # the fused flush
+            ck = cache.ckpt[:, torch.from_numpy(heads).cuda()].cpu().numpy()
+            e = rel_err(ck, oracle.S)
+            assert e <= RTOL, f"folded checkpoints: {e:.3e}"

@@ -51,6 +51,12 @@
 
 namespace rssm {
 
+// Invalidates an mbarrier so that its memory may hold something else (or a
+// new barrier) afterwards.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 constexpr int kFtCompute = 256;                          // compute threads
 constexpr int kFtThreads = kFtCompute + 96;              // + load, preparation and MMA warps
 constexpr int kFtRB = 2, kFtPB = 2;                      // record and prepared-item buffers

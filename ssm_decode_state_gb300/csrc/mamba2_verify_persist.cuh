@@ -29,6 +29,13 @@
 
 namespace rssm {
 
+// Two-wide float32 product (sm_100+): each lane of the pair rounded once.
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Byte layout of the verify kernel's shared memory (T drafts, KM = L + T).
 struct VSmem {
     int stage_bytes, stages_off;
@@ -482,12 +489,17 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
         const uint16_t *r_C = s_cq + ia * T * N;         // the drafts' C, from the prepared item
         const float *dec = s_decay + ia * HPI * T, *rt = s_rt + ia * HPI * T * P;
         const float *wf = s_wf + ia * HPI * KM, *fdec = s_fdec + ia * HPI;
-        float4 cfr[TQ];
+        // the drafts' C at this lane's 4 columns, as packed pairs (columns 0-1, 2-3).
+        // Draft slot i holds draft i ^ ((lane / 8) % 4): the first two rounds of the
+        // reduction below then trade the same half of every lane's values (no selects)
+        unsigned long long cxy[TQ], czw[TQ];
 #pragma unroll
-        for (int i = 0; i < TQ; ++i)
-            cfr[i] = i < T ? make_float4(bf16_at(r_C, i * N + col4 * 4 + 0), bf16_at(r_C, i * N + col4 * 4 + 1),
-                                         bf16_at(r_C, i * N + col4 * 4 + 2), bf16_at(r_C, i * N + col4 * 4 + 3))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < TQ; ++i) {
+            const int di = i ^ ((lane >> 3) & 3);
+            const bool on = di < T;
+            cxy[i] = f2pack(on ? bf16_at(r_C, di * N + col4 * 4 + 0) : 0.f, on ? bf16_at(r_C, di * N + col4 * 4 + 1) : 0.f);
+            czw[i] = f2pack(on ? bf16_at(r_C, di * N + col4 * 4 + 2) : 0.f, on ? bf16_at(r_C, di * N + col4 * 4 + 3) : 0.f);
+        }
         for (int hh = 0; hh < HPI; ++hh) {
             const int t = k * HPI + hh, s = t % S;
             if (live && !pwait(full + s, (uint32_t)((t / S) & 1), s_abort)) {
@@ -509,14 +521,22 @@ m2_verify_persistent(const M2Args a, const PersistCfg pc) {
             for (int i = 0; i < TQ; ++i) {
 #pragma unroll
                 for (int v = 0; v < VPT; ++v) {
-                    float d = hv[v].x * cfr[i].x;
-                    d = fmaf(hv[v].y, cfr[i].y, d);
-                    d = fmaf(hv[v].z, cfr[i].z, d);
-                    d = fmaf(hv[v].w, cfr[i].w, d);
-                    part[i * VPT + v] = d;
+                    // columns 0 + 2 and 1 + 3 as the two lanes of one packed pair
+                    float lo, hi;
+                    f2unpack(fma2(f2pack(hv[v].z, hv[v].w), czw[i], mul2(f2pack(hv[v].x, hv[v].y), cxy[i])), lo, hi);
+                    part[i * VPT + v] = lo + hi;
                 }
             }
-            group_reduce<G4, TQ * VPT>(part);
+            // reduce the 32 (draft slot, row) values across the warp: with the draft
+            // slots permuted by lane bits 3-4, the rounds over lane bits 4 and 3 keep the
+            // low half and trade the high half on every lane; then the usual exchange
+            // over bits 2-0.  Lane l ends with draft l / 8, row l % 8 (as group_reduce)
+            static_assert(G4 == 32 && TQ * VPT == 32, "one value per lane after the reduction");
+#pragma unroll
+            for (int q = 0; q < 16; ++q) part[q] += __shfl_xor_sync(0xffffffffu, part[q + 16], 16);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) part[q] += __shfl_xor_sync(0xffffffffu, part[q + 8], 8);
+            GroupReduce<4, 8, TQ * VPT>::run(part, lane);
             {
                 const int vi = reduced_index<G4, TQ * VPT>(0);
                 const int i = vi / VPT, row = cw + RSTEP * (vi - i * VPT);

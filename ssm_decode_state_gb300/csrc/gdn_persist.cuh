@@ -95,43 +95,55 @@ struct GPSmem {
 // Fold constants of nr records (the preparation warps' share of a fold): the
 // Gram entries C_ij = (k_i . k_j) prod_{i<m<j} alpha_m (i < j), the prefix
 // products a_j = prod_{m<j} alpha_m, the suffix products g_j = prod_{m>j}
-// alpha_m and the total product A, into fc (one warp, nr <= kGdnMaxRec).
+// alpha_m and the total product A, into fc (one warp, nr <= kGdnMaxRec).  The
+// alphas travel in registers (lane m holds alpha_m); every product of alphas
+// is taken in increasing m.
 template <int DK>
 __device__ __forceinline__ void gdn_fold_constants(float *fc, const uint16_t *r_k, const float *r_al, int nr) {
     constexpr int CK = DK / 8;                           // 16-byte chunks per k row
     const int lane = threadIdx.x & 31;
-    // the Gram entries of the pairs i < j, one pair per lane and pass: a dot product of
-    // two bf16 rows (bf16-pair FMAs), times the product of the alphas between them;
+    const float al = lane < nr ? r_al[lane] : 1.0f;
+    // the pairs i < j, one per lane and pass, numbered j (j - 1) / 2 + i: a dot product
+    // of two bf16 rows (bf16-pair FMAs in two chains), times the alphas between them;
     // lanes start on different 16-byte chunks of their rows
-    for (int pidx = lane; pidx < nr * nr; pidx += 32) {
-        const int i = pidx / nr, j = pidx - i * nr;
-        if (i >= j) continue;
-        float t = 0.0f;
-        for (int cc = 0; cc < CK; ++cc) {
-            const int c = (cc + lane) % CK;
-            const uint4 ki = *reinterpret_cast<const uint4 *>(r_k + i * DK + c * 8);
-            const uint4 kj = *reinterpret_cast<const uint4 *>(r_k + j * DK + c * 8);
-            t = fma_bf16_pair(ki.x, kj.x, t);
-            t = fma_bf16_pair(ki.y, kj.y, t);
-            t = fma_bf16_pair(ki.z, kj.z, t);
-            t = fma_bf16_pair(ki.w, kj.w, t);
+    const int npairs = nr * (nr - 1) / 2;
+    for (int p0 = 0; p0 < npairs; p0 += 32) {
+        const int pidx = p0 + lane;
+        const bool on = pidx < npairs;
+        int j = 1;
+        while ((j + 1) * j / 2 <= pidx) ++j;
+        const int i = pidx - j * (j - 1) / 2;
+        float t0 = 0.0f, t1 = 0.0f;
+        if (on) {
+            for (int cc = 0; cc < CK; ++cc) {
+                const int c = (cc + lane) % CK;
+                const uint4 ki = *reinterpret_cast<const uint4 *>(r_k + i * DK + c * 8);
+                const uint4 kj = *reinterpret_cast<const uint4 *>(r_k + j * DK + c * 8);
+                t0 = fma_bf16_pair(ki.x, kj.x, t0);
+                t1 = fma_bf16_pair(ki.y, kj.y, t1);
+                t0 = fma_bf16_pair(ki.z, kj.z, t0);
+                t1 = fma_bf16_pair(ki.w, kj.w, t1);
+            }
         }
         float pa = 1.0f;
-        for (int m = i + 1; m < j; ++m) pa *= r_al[m];
-        fc[i * kGdnMaxRec + j] = t * pa;
+        for (int m = 0; m < nr; ++m) {
+            const float am = __shfl_sync(0xffffffffu, al, m);
+            if (m > i && m < j) pa *= am;
+        }
+        if (on) fc[i * kGdnMaxRec + j] = (t0 + t1) * pa;
+    }
+    float pre = 1.0f, suf = 1.0f, tot = 1.0f;
+    for (int m = 0; m < nr; ++m) {
+        const float am = __shfl_sync(0xffffffffu, al, m);
+        if (m < lane) pre *= am;
+        if (m > lane) suf *= am;
+        tot *= am;
     }
     if (lane < nr) {
-        float pa = 1.0f, pg = 1.0f;
-        for (int m = 0; m < lane; ++m) pa *= r_al[m];
-        for (int m = lane + 1; m < nr; ++m) pg *= r_al[m];
-        fc[kFcA + lane] = pa;
-        fc[kFcG + lane] = pg;
+        fc[kFcA + lane] = pre;
+        fc[kFcG + lane] = suf;
     }
-    if (lane == 0) {
-        float pt = 1.0f;
-        for (int m = 0; m < nr; ++m) pt *= r_al[m];
-        fc[kFcT] = pt;
-    }
+    if (lane == 0) fc[kFcT] = tot;
 }
 
 // A consumer warp's share of a fold: its 8 rows cw + 8 v (v < VPT) of stage uu,

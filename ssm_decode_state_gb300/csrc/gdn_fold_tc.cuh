@@ -2,13 +2,16 @@
 // tensor cores (serving head shape dk = dv = 128, bf16 token inputs).
 //
 // A decode step whose sequence has L - 1 buffered records folds them and its
-// token into the checkpoint (Gated DeltaNet replay, flush).  The step kernel at
+// token into the checkpoint: the flush of the method (AT Pulse, What happened and
+// Technical analysis, core idea; Gated DeltaNet is one of the layer types it
+// ships kernels for, Capabilities and access).  The step kernel at
 // the end of this file takes those (sequence, head) items in a first phase
 // (gdn_fold_phase: their output o = S_c u_0 + record term and their folded
 // checkpoint) and the others in a second one (gdn_decode_phase), over the same
 // shared memory.
 //
-// The fold is the re-associated one of the decode kernel's fused flush: with
+// The fold is the re-associated form that the decode phase also runs on the
+// CUDA cores (gdn_fold_stage, for more than 512 items per CTA): with
 // p_j = s_c . k_j for the nrec records (token last), d_j = a_j p_j +
 // sum_{i<j} C_ij e_i, e_j = beta_j (v_j[r] - alpha_j d_j), f_j = e_j g_j, the
 // new row is A s_c + sum_j f_j k_j, where C_ij = (k_i . k_j) prod_{i<m<j}

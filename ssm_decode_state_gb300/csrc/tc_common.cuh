@@ -101,10 +101,11 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     return d;
 }
 
-// x = t1 + t2 + t3 exactly for normal float32 x: t1 the nearest bf16 to x, t2
-// the nearest to x - t1 (exact in float32), t3 = x - t1 - t2 (at most eight
-// significant bits are left, so it is a bf16 itself).  Two values per call,
-// as bf16 pairs.
+// x = t1 + t2 + t3 exactly for float32 x = 0 or 2^-110 <= |x| <= the largest
+// finite bf16 (~3.39e38): t1 the nearest bf16 to x, t2 the nearest to x - t1
+// (exact in float32), t3 = x - t1 - t2 (at most eight significant bits are left,
+// so it is a bf16 itself).  Below that range t3 would be subnormal and lose bits;
+// above it t1 rounds to infinity.  Two values per call, as bf16 pairs.
 __device__ __forceinline__ void split3_bf16x2(float x0, float x1, uint32_t &t1, uint32_t &t2, uint32_t &t3) {
     t1 = bf16x2_rn(x0, x1);
     float r0 = x0 - __uint_as_float(t1 << 16), r1 = x1 - __uint_as_float(t1 & 0xffff0000u);
